@@ -1,0 +1,180 @@
+/*
+ * anchorattn.h — C ABI of the GB300 (sm_103a) fused RoPE + AnchorAttention
+ * library (libanchorattn.so).
+ *
+ * The method: "When Precision Meets Position: BFloat16 Breaks Down RoPE in
+ * Long-Context Training" (arXiv 2411.13476). Operation references below name
+ * the page and its section:
+ *   [ARCH §3.4 RoPE]    architecture page, §3.4 "Rotary Positional Embedding
+ *                       (RoPE): The Theoretical Promise", Eq. 6 and Eq. 3.
+ *   [ARCH §3.4 Index]   architecture page, §3.4 "Document Token Indexing"
+ *                       (continuous IDs, Fig. 2 left; reset IDs, Fig. 2 middle).
+ *   [ARCH §3.4 Anchor]  architecture page, §3.4 "AnchorAttention: The Shared
+ *                       Anchor Design", "Core design" and "Mask construction".
+ *   [ARCH §3.2]         architecture page, §3.2 "Big-Picture Architecture":
+ *                       RoPE in fp32, cast to bf16, inner products in bf16.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - Tensors are caller-owned, contiguous, row-major [T, H, D] bf16 (token,
+ *    head, channel), 16-byte aligned device pointers. LSE/D-style per-row
+ *    values are fp32 [H, T].
+ *  - Q and K are passed UN-ROTATED: the library rotates them (RoPE in fp32,
+ *    rounded to bf16) inside its kernels; gradients are returned with respect
+ *    to the un-rotated inputs.
+ *  - Token 0 is the anchor. cu_doclens (host int32[num_docs + 1]) gives the
+ *    document boundaries after it: document k occupies tokens
+ *    [cu[k-1], cu[k]), with cu[0] == 1, cu[num_docs] == T, strictly increasing.
+ *    In AA_MASK_CAUSAL mode cu_doclens is ignored (may be NULL).
+ *  - Every call validates its arguments synchronously and returns a status
+ *    without launching anything on failure. Kernel launches are asynchronous
+ *    on `stream` (NULL = the legacy default stream); launch failures return
+ *    AA_ERR_CUDA. Device-side waits are bounded: a wait that runs out records
+ *    an error word that aa_check_device_error() turns into AA_ERR_TIMEOUT.
+ *  - aa_fwd / aa_bwd / aa_rope_apply allocate no memory. aa_plan allocates the
+ *    plan's device metadata; aa_plan_destroy frees it.
+ *  - A thread-local message describing the last failure is available from
+ *    aa_last_error().
+ */
+#ifndef ANCHORATTN_H
+#define ANCHORATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* aa_stream_t; /* identical to cudaStream_t */
+
+typedef enum {
+  AA_OK = 0,
+  AA_ERR_INVALID_ARG = 1,
+  AA_ERR_UNSUPPORTED = 2,
+  AA_ERR_CUDA = 3,
+  AA_ERR_NO_MEMORY = 4,
+  AA_ERR_TIMEOUT = 5
+} aa_status;
+
+/* Which (query, key) pairs are visible. [ARCH §3.4 Anchor], [ARCH §3.4 Index]
+ * CAUSAL:    j <= i over the whole packed sequence (full attention baseline).
+ * INTRA_DOC: j <= i and same document; the anchor is a one-token document.
+ * ANCHOR:    INTRA_DOC plus key 0 (the anchor) visible to every query; the
+ *            anchor query sees only itself. */
+typedef enum { AA_MASK_CAUSAL = 0, AA_MASK_INTRA_DOC = 1, AA_MASK_ANCHOR = 2 } aa_mask_mode;
+
+/* Position IDs [ARCH §3.4 Index]. RESET: anchor 0, every document 1..N_k.
+ * CONTINUOUS: 0..T-1 across documents. CAUSAL mode always uses 0..T-1. */
+typedef enum { AA_POS_RESET = 0, AA_POS_CONTINUOUS = 1 } aa_pos_mode;
+
+/* Pairing of rotated coordinates. ADJACENT = Eq. 6 of [ARCH §3.4 RoPE]
+ * (pairs (2p, 2p+1)); HALF pairs (p, p + D/2); NONE disables the rotation. */
+typedef enum { AA_ROPE_ADJACENT = 0, AA_ROPE_HALF = 1, AA_ROPE_NONE = 2 } aa_rope_layout;
+
+typedef struct {
+  int32_t total_tokens;  /* T >= 2, anchor included; T < 2^30                 */
+  int32_t num_q_heads;   /* Hq >= 1                                            */
+  int32_t num_kv_heads;  /* Hkv >= 1, Hq % Hkv == 0 (grouped-query attention)  */
+  int32_t head_dim;      /* D: 64 or 128                                       */
+  double rope_base;      /* theta_p = rope_base^(-2p/D); > 1                   */
+  float softmax_scale;   /* <= 0 selects 1/sqrt(D)                             */
+  int32_t pos_shift;     /* Delta added to every position (Eq. 3); >= 0       */
+  int32_t mask_mode;     /* aa_mask_mode                                       */
+  int32_t pos_mode;      /* aa_pos_mode                                        */
+  int32_t rope_layout;   /* aa_rope_layout                                     */
+  int32_t host_only;     /* 1: build host metadata only (no GPU needed);
+                            compute calls on such a plan return
+                            AA_ERR_INVALID_ARG                                 */
+} aa_config;
+
+typedef struct aa_plan_s* aa_plan_t;
+
+/* Build the plan for one packing [ARCH §3.4 Anchor "Mask construction",
+ * §3.4 Index]: per-token document and position IDs, each query row's visible
+ * key interval, the live 128x128 tile lists (fully cross-document tiles are
+ * dropped; the anchor column is folded in separately), longest-first work
+ * order, and the two-level fp32 cos/sin tables of Eq. 6 built in fp64.
+ * cu_doclens: host int32[num_docs + 1] (see conventions). Device metadata is
+ * uploaded with copies ordered on `stream`. On success *out owns everything;
+ * release it with aa_plan_destroy. */
+aa_status aa_plan(const aa_config* cfg, const int32_t* cu_doclens_host, int32_t num_docs,
+                  aa_stream_t stream, aa_plan_t* out);
+
+/* Free a plan (synchronises the device). NULL is accepted. */
+aa_status aa_plan_destroy(aa_plan_t plan);
+
+/* Copy the per-token document index (anchor = 0, documents 1..K; all 0 in
+ * CAUSAL mode) and position ID (shift included) into caller host buffers of
+ * T int32 each. Either pointer may be NULL. */
+aa_status aa_plan_metadata(aa_plan_t plan, int32_t* doc_id_host, int32_t* pos_id_host);
+
+/* unmasked_pairs: visible (query, key) pairs of the mask (the T^2/K + T count
+ * of [ARCH §3.4 Anchor], "Reduction in attention computations"), anchor pairs
+ * included. live_tiles: 128x128 blocks of the mask holding a visible pair.
+ * causal_tiles: blocks with any j <= i (what full causal attention visits).
+ * Any pointer may be NULL. */
+aa_status aa_plan_stats(aa_plan_t plan, int64_t* unmasked_pairs, int64_t* live_tiles,
+                        int64_t* causal_tiles);
+
+/* Work the kernels perform: fwd_tiles = (q-tile, k-tile, head) MMA tiles of
+ * the forward pass; bwd_tiles = the same count for the backward pass (one
+ * tile = one 128x128 block of one query head). Any pointer may be NULL. */
+aa_status aa_plan_work(aa_plan_t plan, int64_t* fwd_tiles, int64_t* bwd_tiles);
+
+/* Rotate x [T, num_heads, D] bf16 into y (same shape; y may equal x) with the
+ * plan's positions: y = R_pos x (inverse = 0) or R_pos^T x (inverse = 1),
+ * fp32 arithmetic, round-to-nearest-even to bf16 [ARCH §3.4 RoPE Eq. 6,
+ * ARCH §3.2]. num_heads is independent of the plan's head counts. */
+aa_status aa_rope_apply(aa_plan_t plan, const void* x, void* y, int32_t num_heads,
+                        int32_t inverse, aa_stream_t stream);
+
+/* Forward [ARCH §3.4 Anchor, §3.4 RoPE]: for every query row i and head h,
+ *   O_i = sum_{j visible} softmax_j(scale * (R_i q_i).(R_j k_j)) v_j,
+ *   LSE_i = ln sum_{j visible} exp(scale * (R_i q_i).(R_j k_j)).
+ * q [T,Hq,D], k/v [T,Hkv,D] bf16 in; o [T,Hq,D] bf16, lse [Hq,T] fp32 out.
+ * Query head h reads kv head h / (Hq / Hkv). */
+aa_status aa_fwd(aa_plan_t plan, const void* q, const void* k, const void* v, void* o,
+                 float* lse, aa_stream_t stream);
+
+/* Bytes of device scratch aa_bwd needs (fp32 dQ accumulator, per-row D,
+ * anchor partial sums). */
+size_t aa_bwd_workspace_bytes(aa_plan_t plan);
+
+/* Backward of aa_fwd: given dout = dL/dO, writes dq [T,Hq,D], dk/dv
+ * [T,Hkv,D] bf16 = gradients with respect to the UN-ROTATED q, k and v
+ * (dq = R^T dq~, dk = R^T dk~). q, k, v, o and lse must be the forward's
+ * inputs and outputs. workspace: caller-owned device memory of at least
+ * aa_bwd_workspace_bytes(plan) bytes, 256-byte aligned, contents ignored.
+ * dK/dV of the anchor sum over every query row (and over the group's query
+ * heads). dQ is accumulated with fp32 atomics, so its last bits may vary
+ * between runs; every other output is run-to-run deterministic. */
+aa_status aa_bwd(aa_plan_t plan, const void* q, const void* k, const void* v, const void* o,
+                 const float* lse, const void* dout, void* dq, void* dk, void* dv,
+                 void* workspace, size_t workspace_bytes, aa_stream_t stream);
+
+/* Synchronise `stream`, read and clear the plan's device error word.
+ * Returns AA_ERR_TIMEOUT if a bounded device wait ran out since the last
+ * check, AA_OK otherwise. */
+aa_status aa_check_device_error(aa_plan_t plan, aa_stream_t stream);
+
+/* Diagnostics: limit (nanoseconds) of every bounded device wait for this
+ * plan; 0 makes each wait give up after its first poll (the kernels then
+ * drain their in-flight copies and MMAs and return with the error word set).
+ * The default is 2e9 ns. */
+aa_status aa_set_wait_limit(aa_plan_t plan, uint64_t nanoseconds);
+
+/* Measurement hook: when both are non-NULL CUDA events (cudaEvent_t),
+ * aa_bwd records `start` immediately before and `stop` immediately after the
+ * launch of its main tile kernel, on the call's stream, so that kernel can be
+ * timed on its own. NULL, NULL (the default) disables the recording. The
+ * events are caller-owned and must outlive the calls that record them. */
+aa_status aa_set_bwd_timing_events(aa_plan_t plan, void* start, void* stop);
+
+const char* aa_status_string(aa_status status);
+const char* aa_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* ANCHORATTN_H */

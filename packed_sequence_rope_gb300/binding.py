@@ -1,0 +1,200 @@
+"""ctypes binding of libanchorattn.so: argument marshalling only.
+
+Every step of the path runs in the library's CUDA kernels; torch supplies the
+device memory and the stream. There is no fallback: if the library is
+missing or a call fails, an exception is raised.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import numpy as np
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libanchorattn.so")
+
+MASK_CAUSAL, MASK_INTRA_DOC, MASK_ANCHOR = 0, 1, 2
+POS_RESET, POS_CONTINUOUS = 0, 1
+ROPE_ADJACENT, ROPE_HALF, ROPE_NONE = 0, 1, 2
+STATUS = {0: "AA_OK", 1: "AA_ERR_INVALID_ARG", 2: "AA_ERR_UNSUPPORTED", 3: "AA_ERR_CUDA",
+          4: "AA_ERR_NO_MEMORY", 5: "AA_ERR_TIMEOUT"}
+
+# every symbol include/anchorattn.h declares
+EXPORTS = ["aa_plan", "aa_plan_destroy", "aa_plan_metadata", "aa_plan_stats", "aa_plan_work",
+           "aa_rope_apply", "aa_fwd", "aa_bwd_workspace_bytes", "aa_bwd", "aa_check_device_error",
+           "aa_set_wait_limit", "aa_set_bwd_timing_events", "aa_status_string", "aa_last_error"]
+
+
+class AAConfig(ctypes.Structure):
+    _fields_ = [("total_tokens", ctypes.c_int32), ("num_q_heads", ctypes.c_int32),
+                ("num_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32),
+                ("rope_base", ctypes.c_double), ("softmax_scale", ctypes.c_float),
+                ("pos_shift", ctypes.c_int32), ("mask_mode", ctypes.c_int32),
+                ("pos_mode", ctypes.c_int32), ("rope_layout", ctypes.c_int32),
+                ("host_only", ctypes.c_int32)]
+
+
+class AAError(RuntimeError):
+    def __init__(self, status, msg):
+        super().__init__(f"{STATUS.get(status, status)}: {msg}")
+        self.status = status
+
+
+_lib = None
+
+
+def lib():
+    """Load libanchorattn.so (built by __graft_entry__.build())."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is missing: run __graft_entry__.build() first")
+        L = ctypes.CDLL(LIB_PATH)
+        vp, i32, i64p = ctypes.c_void_p, ctypes.c_int32, ctypes.POINTER(ctypes.c_int64)
+        i32p = ctypes.POINTER(ctypes.c_int32)
+        sig = {
+            "aa_plan": ([ctypes.POINTER(AAConfig), i32p, i32, vp, ctypes.POINTER(vp)], ctypes.c_int),
+            "aa_plan_destroy": ([vp], ctypes.c_int),
+            "aa_plan_metadata": ([vp, i32p, i32p], ctypes.c_int),
+            "aa_plan_stats": ([vp, i64p, i64p, i64p], ctypes.c_int),
+            "aa_plan_work": ([vp, i64p, i64p], ctypes.c_int),
+            "aa_rope_apply": ([vp, vp, vp, i32, i32, vp], ctypes.c_int),
+            "aa_fwd": ([vp, vp, vp, vp, vp, vp, vp], ctypes.c_int),
+            "aa_bwd_workspace_bytes": ([vp], ctypes.c_size_t),
+            "aa_bwd": ([vp] + [vp] * 9 + [vp, ctypes.c_size_t, vp], ctypes.c_int),
+            "aa_check_device_error": ([vp, vp], ctypes.c_int),
+            "aa_set_wait_limit": ([vp, ctypes.c_uint64], ctypes.c_int),
+            "aa_set_bwd_timing_events": ([vp, vp, vp], ctypes.c_int),
+            "aa_status_string": ([ctypes.c_int], ctypes.c_char_p),
+            "aa_last_error": ([], ctypes.c_char_p),
+        }
+        for name, (args, res) in sig.items():
+            f = getattr(L, name)
+            f.argtypes, f.restype = args, res
+        _lib = L
+    return _lib
+
+
+def _check(status):
+    if status != 0:
+        raise AAError(status, lib().aa_last_error().decode())
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+class Plan:
+    """aa_plan for one packing; compute methods wrap aa_rope_apply/aa_fwd/aa_bwd."""
+
+    def __init__(self, cu_doclens, total_tokens, num_q_heads, num_kv_heads, head_dim,
+                 rope_base=1e4, mask_mode=MASK_ANCHOR, pos_mode=POS_RESET,
+                 rope_layout=ROPE_ADJACENT, softmax_scale=0.0, pos_shift=0,
+                 host_only=False, stream=None):
+        self.cfg = AAConfig(int(total_tokens), int(num_q_heads), int(num_kv_heads), int(head_dim),
+                            float(rope_base), float(softmax_scale or 0.0), int(pos_shift),
+                            int(mask_mode), int(pos_mode), int(rope_layout), int(bool(host_only)))
+        self.T, self.Hq, self.Hkv, self.D = int(total_tokens), int(num_q_heads), int(num_kv_heads), int(head_dim)
+        self.host_only = bool(host_only)
+        if cu_doclens is None:
+            cu, n = None, 0
+        else:
+            self._cu = np.ascontiguousarray(np.asarray(cu_doclens, dtype=np.int32))
+            cu = self._cu.ctypes.data_as(ctypes.POINTER(ctypes.c_int32))
+            n = int(self._cu.size) - 1
+        h = ctypes.c_void_p()
+        st = ctypes.c_void_p(0) if host_only else _stream(stream)
+        _check(lib().aa_plan(ctypes.byref(self.cfg), cu, n, st, ctypes.byref(h)))
+        self._h = h
+
+    # ---- lifetime
+    def close(self):
+        if getattr(self, "_h", None):
+            lib().aa_plan_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        self.close()
+
+    # ---- host queries
+    def metadata(self):
+        doc = np.zeros(self.T, dtype=np.int32)
+        pos = np.zeros(self.T, dtype=np.int32)
+        _check(lib().aa_plan_metadata(self._h, doc.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)),
+                                      pos.ctypes.data_as(ctypes.POINTER(ctypes.c_int32))))
+        return doc, pos
+
+    def stats(self):
+        a, b, c = ctypes.c_int64(), ctypes.c_int64(), ctypes.c_int64()
+        _check(lib().aa_plan_stats(self._h, ctypes.byref(a), ctypes.byref(b), ctypes.byref(c)))
+        return {"unmasked_pairs": a.value, "live_tiles": b.value, "causal_tiles": c.value}
+
+    def work(self):
+        a, b = ctypes.c_int64(), ctypes.c_int64()
+        _check(lib().aa_plan_work(self._h, ctypes.byref(a), ctypes.byref(b)))
+        return {"fwd_tiles": a.value, "bwd_tiles": b.value}
+
+    def workspace_bytes(self):
+        return int(lib().aa_bwd_workspace_bytes(self._h))
+
+    def set_wait_limit(self, ns):
+        _check(lib().aa_set_wait_limit(self._h, int(ns)))
+
+    def set_bwd_timing_events(self, start=None, stop=None):
+        """torch.cuda.Event pair (enable_timing=True) recorded around the main bwd kernel."""
+        a = ctypes.c_void_p(start.cuda_event) if start is not None else None
+        b = ctypes.c_void_p(stop.cuda_event) if stop is not None else None
+        _check(lib().aa_set_bwd_timing_events(self._h, a, b))
+
+    def check_device_error(self, stream=None):
+        _check(lib().aa_check_device_error(self._h, _stream(stream)))
+
+    # ---- compute (device tensors only)
+    def rope_apply(self, x, inverse=False, out=None, stream=None):
+        import torch
+        assert x.is_cuda and x.dtype == torch.bfloat16 and x.is_contiguous()
+        y = torch.empty_like(x) if out is None else out
+        _check(lib().aa_rope_apply(self._h, _ptr(x), _ptr(y), int(x.shape[1]), int(bool(inverse)),
+                                   _stream(stream)))
+        return y
+
+    def fwd(self, q, k, v, o=None, lse=None, stream=None):
+        import torch
+        for t in (q, k, v):
+            assert t.is_cuda and t.dtype == torch.bfloat16 and t.is_contiguous()
+        o = torch.empty_like(q) if o is None else o
+        lse = torch.empty(self.Hq, self.T, device=q.device, dtype=torch.float32) if lse is None else lse
+        _check(lib().aa_fwd(self._h, _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _stream(stream)))
+        return o, lse
+
+    def alloc_workspace(self, device):
+        import torch
+        return torch.empty(self.workspace_bytes(), device=device, dtype=torch.uint8)
+
+    def bwd(self, q, k, v, o, lse, dout, dq=None, dk=None, dv=None, workspace=None, stream=None):
+        import torch
+        dq = torch.empty_like(q) if dq is None else dq
+        dk = torch.empty_like(k) if dk is None else dk
+        dv = torch.empty_like(v) if dv is None else dv
+        ws = self.alloc_workspace(q.device) if workspace is None else workspace
+        _check(lib().aa_bwd(self._h, _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout),
+                            _ptr(dq), _ptr(dk), _ptr(dv), _ptr(ws), ctypes.c_size_t(ws.numel()),
+                            _stream(stream)))
+        return dq, dk, dv

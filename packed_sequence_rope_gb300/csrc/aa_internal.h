@@ -1,0 +1,62 @@
+// Internal declarations shared by the host planner and the kernel launchers.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <string>
+#include <vector>
+
+#include "../../include/anchorattn.h"
+
+namespace aa {
+
+constexpr int kTile = 128;  // rows of a query tile and of a key tile
+
+// One unit of forward work: query tile `tile` of query head `head`, visiting
+// key tiles [lo, hi] (inclusive). One unit of backward work: key tile `tile`
+// of kv head `head`, visiting query tiles [lo, hi] for every query head of
+// the group.
+struct WorkItem {
+  int32_t tile, head, lo, hi;
+};
+
+struct DevicePlan {
+  int32_t* pos_id = nullptr;   // [T] rotation index (shift included)
+  int32_t* row_lo = nullptr;   // [T] first key of row i's tile-path interval [row_lo, i]
+  int32_t* key_hi = nullptr;   // [T] last query row that sees key j in the tile path
+  WorkItem* fwd_items = nullptr;
+  WorkItem* bwd_items = nullptr;
+  float2* rope_hi = nullptr;   // [n_hi][D/2]  cos/sin((128*h) * theta_p)
+  float2* rope_lo = nullptr;   // [128][D/2]   cos/sin(l * theta_p)
+  int32_t* err = nullptr;      // device error word (0 = ok)
+};
+
+}  // namespace aa
+
+struct aa_plan_s {
+  aa_config cfg;
+  int32_t T = 0, Hq = 0, Hkv = 0, D = 0, n_tiles = 0, group = 1;
+  float scale = 0.f;
+  bool anchor = false;          // anchor column handled outside the tile path
+  bool host_only = false;
+  std::vector<int32_t> cu;      // document boundaries (empty in CAUSAL mode)
+  std::vector<int32_t> doc_id, pos_id, row_lo, key_hi;
+  std::vector<aa::WorkItem> fwd_items, bwd_items;
+  std::vector<float2> rope_hi, rope_lo;
+  int32_t n_hi = 0;
+  int64_t unmasked_pairs = 0, live_tiles = 0, causal_tiles = 0;
+  int64_t fwd_tiles = 0, bwd_tiles = 0;
+  uint64_t wait_limit_ns = 2000000000ull;
+  cudaEvent_t bwd_ev_start = nullptr, bwd_ev_stop = nullptr;
+  int device = 0, num_sms = 0;
+  aa::DevicePlan dev;
+};
+
+namespace aa {
+// Record a failure message for aa_last_error() and return `s`.
+aa_status fail(aa_status s, const std::string& msg);
+aa_status cuda_fail(cudaError_t e, const char* what);
+bool aligned16(const void* p);
+aa_status check_compute_plan(const aa_plan_s* p);
+}  // namespace aa

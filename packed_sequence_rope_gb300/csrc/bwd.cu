@@ -1,0 +1,646 @@
+// Backward pass of fused RoPE + AnchorAttention on sm_103a.
+//
+// Gradients of the forward defined in fwd.cu ("When Precision Meets
+// Position", architecture page §3.4 "AnchorAttention: The Shared Anchor
+// Design" for the mask, Eq. 6 of §3.4 "Rotary Positional Embedding (RoPE)"
+// for the rotation) with respect to the un-rotated q, k, v:
+//   P_ij  = exp(scale * q~_i.k~_j - LSE_i)            (recomputed)
+//   dv_j  = sum_i P_ij dO_i
+//   dS_ij = P_ij (dO_i.v_j - D_i),  D_i = dO_i.O_i
+//   dq~_i = scale sum_j dS_ij k~_j,  dk~_j = scale sum_i dS_ij q~_i
+//   dq = R^T dq~,  dk = R^T dk~
+//
+// Kernels, in stream order:
+//   1. bwd_prep: D_i, and the anchor column for every row (P_i0, dS_i0): the
+//      fp32 dQ accumulator is initialised with scale*dS_i0*k~_0 (so it needs
+//      no separate clearing pass) and per-chunk partial sums of dv_0, dk~_0
+//      are written.
+//   2. attn_bwd: one CTA per (key tile, kv head), K/V stationary in shared
+//      memory (K rotated once), looping over the group's query heads and the
+//      live query tiles. Five tcgen05 MMAs per tile (S^T, dP^T, dV, dK, dQ)
+//      with fp32 TMEM accumulators; dQ goes to the fp32 accumulator with
+//      vector atomics; dK/dV are rotated back and written once.
+//   3. dq_finalize: dq = bf16(R^T dq~).
+//   4. anchor_finalize: dk_0 / dv_0 = fixed-order sums of the partials.
+#include "kcommon.cuh"
+
+namespace aa {
+namespace {
+
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr uint64_t kDrainLimitNs = 1000000000ull;
+constexpr int kPrepChunks = 64;  // row chunks of the anchor partial sums
+
+struct Workspace {
+  float* dq_acc;   // [T, Hq, D] fp32
+  float* dsum;     // [Hq, T] fp32 (D_i)
+  float* part_dv;  // [kPrepChunks, Hq, D]
+  float* part_dk;  // [kPrepChunks, Hq, D]
+};
+
+inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+Workspace carve(void* base, const aa_plan_s* p, size_t* total) {
+  Workspace w;
+  size_t off = 0;
+  uint8_t* b = static_cast<uint8_t*>(base);
+  w.dq_acc = reinterpret_cast<float*>(b + off);
+  off = align256(off + (size_t)p->T * p->Hq * p->D * 4);
+  w.dsum = reinterpret_cast<float*>(b + off);
+  off = align256(off + (size_t)p->Hq * p->T * 4);
+  w.part_dv = reinterpret_cast<float*>(b + off);
+  off = align256(off + (size_t)kPrepChunks * p->Hq * p->D * 4);
+  w.part_dk = reinterpret_cast<float*>(b + off);
+  off = align256(off + (size_t)kPrepChunks * p->Hq * p->D * 4);
+  if (total) *total = off;
+  return w;
+}
+
+// ---------------------------------------------------------------- 1. prep
+// One warp per row; lane l holds channels [l*EPL, (l+1)*EPL).
+template <int HD>
+__global__ void __launch_bounds__(128) bwd_prep_kernel(const __nv_bfloat16* __restrict__ q,
+                                                       const __nv_bfloat16* __restrict__ k,
+                                                       const __nv_bfloat16* __restrict__ v,
+                                                       const __nv_bfloat16* __restrict__ o,
+                                                       const __nv_bfloat16* __restrict__ dout,
+                                                       const float* __restrict__ lse, Workspace ws,
+                                                       const int32_t* __restrict__ pos_id,
+                                                       const float2* __restrict__ hi_tab,
+                                                       const float2* __restrict__ lo_tab, int T, int Hq,
+                                                       int group, int layout, int anchor, float scale) {
+  constexpr int EPL = HD / 32;
+  const int h = blockIdx.y, g = h / group;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int rows_per_chunk = (T + kPrepChunks - 1) / kPrepChunks;
+  const int r_begin = blockIdx.x * rows_per_chunk;
+  const int r_end = min(T, r_begin + rows_per_chunk);
+  __shared__ float red_dv[4][HD], red_dk[4][HD];
+
+  // rotated anchor key for this lane's channels (bf16-rounded, as the forward uses it)
+  float k0[EPL], v0[EPL];
+  auto rotate_lane = [&](float* x, int pos) {
+    if (layout == 2) return;
+    if (layout == 0) {
+#pragma unroll
+      for (int e = 0; e < EPL; e += 2) {
+        const float2 cs = rope_cs(hi_tab, lo_tab, pos, (lane * EPL + e) >> 1, HD / 2);
+        rope_pair(x[e], x[e + 1], cs.x, cs.y);
+      }
+    } else {
+      const bool first = lane < 16;
+#pragma unroll
+      for (int e = 0; e < EPL; ++e) {
+        const float other = __shfl_xor_sync(0xffffffffu, x[e], 16);
+        const int pidx = (lane & 15) * EPL + e;
+        const float2 cs = rope_cs(hi_tab, lo_tab, pos, pidx, HD / 2);
+        float a = first ? x[e] : other, b = first ? other : x[e];
+        rope_pair(a, b, cs.x, cs.y);
+        x[e] = first ? a : b;
+      }
+    }
+  };
+  if (anchor) {
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) {
+      k0[e] = __bfloat162float(k[(size_t)g * HD + lane * EPL + e]);
+      v0[e] = __bfloat162float(v[(size_t)g * HD + lane * EPL + e]);
+    }
+    rotate_lane(k0, __ldg(pos_id));
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) k0[e] = __bfloat162float(__float2bfloat16_rn(k0[e]));
+  }
+  float pdv[EPL], pdk[EPL];
+#pragma unroll
+  for (int e = 0; e < EPL; ++e) pdv[e] = pdk[e] = 0.f;
+
+  for (int i = r_begin + warp; i < r_end; i += 4) {
+    const size_t base = ((size_t)i * Hq + h) * HD + lane * EPL;
+    float ov[EPL], dov[EPL];
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) {
+      ov[e] = __bfloat162float(o[base + e]);
+      dov[e] = __bfloat162float(dout[base + e]);
+    }
+    float dsum = 0.f;
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) dsum = fmaf(ov[e], dov[e], dsum);
+#pragma unroll
+    for (int s = 16; s > 0; s >>= 1) dsum += __shfl_xor_sync(0xffffffffu, dsum, s);
+    if (lane == 0) ws.dsum[(size_t)h * T + i] = dsum;
+    float* acc = ws.dq_acc + base;
+    if (anchor) {
+      float qv[EPL];
+#pragma unroll
+      for (int e = 0; e < EPL; ++e) qv[e] = __bfloat162float(q[base + e]);
+      rotate_lane(qv, __ldg(pos_id + i));
+      float s = 0.f, dp = 0.f;
+#pragma unroll
+      for (int e = 0; e < EPL; ++e) {
+        qv[e] = __bfloat162float(__float2bfloat16_rn(qv[e]));
+        s = fmaf(qv[e], k0[e], s);
+        dp = fmaf(dov[e], v0[e], dp);
+      }
+#pragma unroll
+      for (int sh = 16; sh > 0; sh >>= 1) {
+        s += __shfl_xor_sync(0xffffffffu, s, sh);
+        dp += __shfl_xor_sync(0xffffffffu, dp, sh);
+      }
+      const float p0 = exp2f((s * scale - __ldg(lse + (size_t)h * T + i)) * kLog2e);
+      const float ds0 = p0 * (dp - dsum);
+#pragma unroll
+      for (int e = 0; e < EPL; ++e) {
+        acc[e] = scale * ds0 * k0[e];
+        pdv[e] = fmaf(p0, dov[e], pdv[e]);
+        pdk[e] = fmaf(scale * ds0, qv[e], pdk[e]);
+      }
+    } else {
+#pragma unroll
+      for (int e = 0; e < EPL; ++e) acc[e] = 0.f;
+    }
+  }
+  if (!anchor) return;
+#pragma unroll
+  for (int e = 0; e < EPL; ++e) {
+    red_dv[warp][lane * EPL + e] = pdv[e];
+    red_dk[warp][lane * EPL + e] = pdk[e];
+  }
+  __syncthreads();
+  for (int c = threadIdx.x; c < HD; c += blockDim.x) {
+    const float sdv = ((red_dv[0][c] + red_dv[1][c]) + red_dv[2][c]) + red_dv[3][c];
+    const float sdk = ((red_dk[0][c] + red_dk[1][c]) + red_dk[2][c]) + red_dk[3][c];
+    ws.part_dv[((size_t)blockIdx.x * Hq + h) * HD + c] = sdv;
+    ws.part_dk[((size_t)blockIdx.x * Hq + h) * HD + c] = sdk;
+  }
+}
+
+// ---------------------------------------------------------------- 2. main
+template <int HD>
+struct BwdSmem {
+  static constexpr int kBlocks = HD / 64;
+  alignas(1024) uint8_t k[kBlocks][16384];
+  alignas(1024) uint8_t v[kBlocks][16384];
+  alignas(1024) uint8_t q[kBlocks][16384];
+  alignas(1024) uint8_t dout[kBlocks][16384];
+  alignas(1024) uint8_t pt[2][16384];   // P^T: 128 keys x 128 query rows
+  alignas(1024) uint8_t dst[2][16384];  // dS^T
+  float lse2[128];                      // LSE_i * log2(e) of the current query tile
+  float dsum[128];                      // D_i of the current query tile
+  uint64_t bar_kv, bar_q, bar_mma;
+  uint32_t tmem_base;
+};
+
+struct BwdParams {
+  __nv_bfloat16* dk;
+  __nv_bfloat16* dv;
+  const float* lse;
+  Workspace ws;
+  const int32_t* pos_id;
+  const int32_t* key_hi;
+  const WorkItem* items;
+  const float2* rope_hi;
+  const float2* rope_lo;
+  int32_t* err;
+  uint64_t wait_limit_ns;
+  int T, Hq, Hkv, group, layout;
+  float scale;
+};
+
+template <int HD>
+__global__ void __launch_bounds__(128, 1)
+    attn_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                    const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
+                    const BwdParams P) {
+  extern __shared__ uint8_t smem_raw[];
+  BwdSmem<HD>& sm = *reinterpret_cast<BwdSmem<HD>*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                                    ~uintptr_t(1023));
+  constexpr int kTmemCols = 512;
+  constexpr uint32_t kTileBytes = 128 * HD * 2;
+  const int tid = threadIdx.x, warp = tid >> 5;
+  const WorkItem item = P.items[blockIdx.x];
+  const int kt = item.tile, g = item.head;
+  const int n_qt = item.hi - item.lo + 1;
+  const int n_steps = n_qt * P.group;
+
+  if (tid == 0) {
+    ptx::tma_prefetch_desc(&tmQ);
+    ptx::tma_prefetch_desc(&tmK);
+    ptx::tma_prefetch_desc(&tmV);
+    ptx::tma_prefetch_desc(&tmDO);
+    ptx::mbar_init(&sm.bar_kv, 1);
+    ptx::mbar_init(&sm.bar_q, 1);
+    ptx::mbar_init(&sm.bar_mma, 1);
+    ptx::fence_mbar_init();
+  }
+  if (warp == 0) ptx::tmem_alloc(&sm.tmem_base, kTmemCols);
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = sm.tmem_base;
+  const uint32_t t_s = tmem, t_dp = tmem + 128, t_dv = tmem + 256, t_dk = tmem + 256 + HD, t_dq = tmem;
+  const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+
+  bool kv_pending = false, q_pending = false, mma_pending = false;
+  uint32_t q_phase = 0, mma_phase = 0;
+
+  auto issue_q = [&](int step) {
+    const int h = g * P.group + step / n_qt;
+    const int qt = item.lo + step % n_qt;
+    ptx::mbar_arrive_expect_tx(&sm.bar_q, 2 * kTileBytes);
+    for (int b = 0; b < HD / 64; ++b) {
+      ptx::tma_load_3d(sm.q[b], &tmQ, &sm.bar_q, b * 64, h, qt * kTile);
+      ptx::tma_load_3d(sm.dout[b], &tmDO, &sm.bar_q, b * 64, h, qt * kTile);
+    }
+  };
+
+  if (tid == 0) {
+    ptx::mbar_arrive_expect_tx(&sm.bar_kv, 2 * kTileBytes);
+    for (int b = 0; b < HD / 64; ++b) {
+      ptx::tma_load_3d(sm.k[b], &tmK, &sm.bar_kv, b * 64, g, kt * kTile);
+      ptx::tma_load_3d(sm.v[b], &tmV, &sm.bar_kv, b * 64, g, kt * kTile);
+    }
+    issue_q(0);
+    kv_pending = q_pending = true;
+  }
+
+  const int r = tid;
+  const int j = kt * kTile + r;  // this thread's key (TMEM lane of S^T, dP^T, dV, dK)
+  const bool key_valid = j < P.T;
+  const int jhi = key_valid ? __ldg(P.key_hi + j) : -1;  // rows [j, jhi] see key j
+  const float sl2 = P.scale * kLog2e;
+  constexpr uint32_t idesc_kt = ptx::idesc_bf16_f32(128, 128, 0, 0);   // S^T, dP^T
+  constexpr uint32_t idesc_kd = ptx::idesc_bf16_f32(128, HD, 0, 1);    // dV, dK
+  constexpr uint32_t idesc_qd = ptx::idesc_bf16_f32(128, HD, 1, 1);    // dQ
+
+  bool ok = ptx::mbar_wait(&sm.bar_kv, 0, P.wait_limit_ns, P.err, 201);
+  if (__syncthreads_or(!ok)) goto abort;
+  if (tid == 0) kv_pending = false;
+  if (key_valid) rope_row_smem<HD>(sm.k[0], r, __ldg(P.pos_id + j), P.layout, false, P.rope_hi, P.rope_lo);
+
+  for (int step = 0; step < n_steps; ++step) {
+    const int h = g * P.group + step / n_qt;
+    const int qt = item.lo + step % n_qt;
+    const int i0 = qt * kTile;
+    ok = ptx::mbar_wait(&sm.bar_q, q_phase, P.wait_limit_ns, P.err, 202);
+    if (__syncthreads_or(!ok)) goto abort;
+    if (tid == 0) q_pending = false;
+    q_phase ^= 1;
+    {
+      const int i = i0 + r;  // this thread rotates query row r
+      if (i < P.T) {
+        rope_row_smem<HD>(sm.q[0], r, __ldg(P.pos_id + i), P.layout, false, P.rope_hi, P.rope_lo);
+        sm.lse2[r] = __ldg(P.lse + (size_t)h * P.T + i) * kLog2e;
+        sm.dsum[r] = __ldg(P.ws.dsum + (size_t)h * P.T + i);
+      } else {
+        sm.lse2[r] = INFINITY;
+        sm.dsum[r] = 0.f;
+      }
+    }
+    ptx::fence_proxy_async_smem();
+    ptx::tc_fence_before();
+    __syncthreads();
+    if (tid == 0) {
+      ptx::tc_fence_after();
+#pragma unroll
+      for (int kk = 0; kk < HD / 16; ++kk) {
+        const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+        ptx::mma_bf16(t_s, ptx::smem_desc_sw128(ptx::smem_u32(sm.k[0]) + off, 16, 1024),
+                      ptx::smem_desc_sw128(ptx::smem_u32(sm.q[0]) + off, 16, 1024), idesc_kt, kk > 0);
+      }
+#pragma unroll
+      for (int kk = 0; kk < HD / 16; ++kk) {
+        const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+        ptx::mma_bf16(t_dp, ptx::smem_desc_sw128(ptx::smem_u32(sm.v[0]) + off, 16, 1024),
+                      ptx::smem_desc_sw128(ptx::smem_u32(sm.dout[0]) + off, 16, 1024), idesc_kt, kk > 0);
+      }
+      ptx::mma_commit(&sm.bar_mma);
+      mma_pending = true;
+    }
+    ok = ptx::mbar_wait(&sm.bar_mma, mma_phase, P.wait_limit_ns, P.err, 203);
+    if (__syncthreads_or(!ok)) goto abort;
+    if (tid == 0) mma_pending = false;
+    mma_phase ^= 1;
+    ptx::tc_fence_after();
+
+    // P^T and dS^T for this thread's key row, 32 query columns at a time
+#pragma unroll 1
+    for (int c = 0; c < 4; ++c) {
+      float sv[32], dpv[32];
+      ptx::tmem_ld32(t_s + lane_off + c * 32, sv);
+      ptx::tmem_ld32(t_dp + lane_off + c * 32, dpv);
+      ptx::tmem_wait_ld();
+      uint32_t pw[16], dw[16];
+#pragma unroll
+      for (int e = 0; e < 32; e += 2) {
+        float pp[2], dd[2];
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          const int col = c * 32 + e + u;
+          const int i = i0 + col;
+          const bool vis = (i >= j) && (i <= jhi);
+          const float p = vis ? exp2f(fmaf(sv[e + u], sl2, -sm.lse2[col])) : 0.f;
+          pp[u] = p;
+          dd[u] = p * (dpv[e + u] - sm.dsum[col]);
+        }
+        pw[e / 2] = ptx::pack_bf16x2(pp[0], pp[1]);
+        dw[e / 2] = ptx::pack_bf16x2(dd[0], dd[1]);
+      }
+#pragma unroll
+      for (int q4 = 0; q4 < 4; ++q4) {
+        const int c8 = c * 4 + q4;  // 16-byte chunk index along the 128 query columns
+        const uint32_t off = (c8 >> 3) * 16384 + sw128_chunk(r, c8 & 7);
+        *reinterpret_cast<uint4*>(sm.pt[0] + off) = make_uint4(pw[4 * q4], pw[4 * q4 + 1], pw[4 * q4 + 2], pw[4 * q4 + 3]);
+        *reinterpret_cast<uint4*>(sm.dst[0] + off) = make_uint4(dw[4 * q4], dw[4 * q4 + 1], dw[4 * q4 + 2], dw[4 * q4 + 3]);
+      }
+    }
+    ptx::fence_proxy_async_smem();
+    ptx::tc_fence_before();
+    __syncthreads();
+    if (tid == 0) {
+      ptx::tc_fence_after();
+      const uint32_t first = step == 0 ? 0u : 1u;
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk) {  // K = 128 query rows
+        const uint32_t aoff = (kk >> 2) * 16384 + (kk & 3) * 32;
+        ptx::mma_bf16(t_dv, ptx::smem_desc_sw128(ptx::smem_u32(sm.pt[0]) + aoff, 16, 1024),
+                      ptx::smem_desc_sw128(ptx::smem_u32(sm.dout[0]) + kk * 2048, 16384, 1024), idesc_kd,
+                      (first | (kk > 0)) ? 1u : 0u);
+      }
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk) {
+        const uint32_t aoff = (kk >> 2) * 16384 + (kk & 3) * 32;
+        ptx::mma_bf16(t_dk, ptx::smem_desc_sw128(ptx::smem_u32(sm.dst[0]) + aoff, 16, 1024),
+                      ptx::smem_desc_sw128(ptx::smem_u32(sm.q[0]) + kk * 2048, 16384, 1024), idesc_kd,
+                      (first | (kk > 0)) ? 1u : 0u);
+      }
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk) {  // K = 128 keys
+        ptx::mma_bf16(t_dq, ptx::smem_desc_sw128(ptx::smem_u32(sm.dst[0]) + kk * 2048, 16384, 1024),
+                      ptx::smem_desc_sw128(ptx::smem_u32(sm.k[0]) + kk * 2048, 16384, 1024), idesc_qd,
+                      kk > 0 ? 1u : 0u);
+      }
+      ptx::mma_commit(&sm.bar_mma);
+      mma_pending = true;
+    }
+    ok = ptx::mbar_wait(&sm.bar_mma, mma_phase, P.wait_limit_ns, P.err, 204);
+    if (__syncthreads_or(!ok)) goto abort;
+    mma_phase ^= 1;
+    if (tid == 0) {
+      mma_pending = false;
+      if (step + 1 < n_steps) {
+        issue_q(step + 1);
+        q_pending = true;
+      }
+    }
+    ptx::tc_fence_after();
+    {
+      // dQ~ rows of this tile: TMEM lane r = query row i0 + r
+      const int i = i0 + r;
+      float* dst = P.ws.dq_acc + ((size_t)(i < P.T ? i : 0) * P.Hq + h) * HD;
+#pragma unroll 1
+      for (int c = 0; c < HD / 32; ++c) {
+        float dq[32];
+        ptx::tmem_ld32(t_dq + lane_off + c * 32, dq);
+        ptx::tmem_wait_ld();
+        if (i < P.T) {
+#pragma unroll
+          for (int e = 0; e < 32; e += 4)
+            ptx::red_add_v4(dst + c * 32 + e, P.scale * dq[e], P.scale * dq[e + 1], P.scale * dq[e + 2],
+                            P.scale * dq[e + 3]);
+        }
+      }
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+  }
+
+  {
+    // ---- epilogue: dV and dK~ for this thread's key row; dk = R^T (scale dK~)
+    float acc[HD];
+#pragma unroll
+    for (int c = 0; c < HD / 32; ++c) ptx::tmem_ld32(t_dv + lane_off + c * 32, acc + c * 32);
+    ptx::tmem_wait_ld();
+    if (key_valid) {
+      uint4* dst = reinterpret_cast<uint4*>(P.dv + ((size_t)j * P.Hkv + g) * HD);
+#pragma unroll
+      for (int c = 0; c < HD / 8; ++c)
+        dst[c] = make_uint4(ptx::pack_bf16x2(acc[8 * c], acc[8 * c + 1]), ptx::pack_bf16x2(acc[8 * c + 2], acc[8 * c + 3]),
+                            ptx::pack_bf16x2(acc[8 * c + 4], acc[8 * c + 5]), ptx::pack_bf16x2(acc[8 * c + 6], acc[8 * c + 7]));
+    }
+#pragma unroll
+    for (int c = 0; c < HD / 32; ++c) ptx::tmem_ld32(t_dk + lane_off + c * 32, acc + c * 32);
+    ptx::tmem_wait_ld();
+    if (key_valid) {
+#pragma unroll
+      for (int c = 0; c < HD; ++c) acc[c] *= P.scale;
+      const int pos = __ldg(P.pos_id + j);
+      if (P.layout == 0) {
+#pragma unroll
+        for (int p = 0; p < HD / 2; ++p) {
+          const float2 cs = rope_cs(P.rope_hi, P.rope_lo, pos, p, HD / 2);
+          rope_pair(acc[2 * p], acc[2 * p + 1], cs.x, -cs.y);
+        }
+      } else if (P.layout == 1) {
+#pragma unroll
+        for (int p = 0; p < HD / 2; ++p) {
+          const float2 cs = rope_cs(P.rope_hi, P.rope_lo, pos, p, HD / 2);
+          rope_pair(acc[p], acc[p + HD / 2], cs.x, -cs.y);
+        }
+      }
+      uint4* dst = reinterpret_cast<uint4*>(P.dk + ((size_t)j * P.Hkv + g) * HD);
+#pragma unroll
+      for (int c = 0; c < HD / 8; ++c)
+        dst[c] = make_uint4(ptx::pack_bf16x2(acc[8 * c], acc[8 * c + 1]), ptx::pack_bf16x2(acc[8 * c + 2], acc[8 * c + 3]),
+                            ptx::pack_bf16x2(acc[8 * c + 4], acc[8 * c + 5]), ptx::pack_bf16x2(acc[8 * c + 6], acc[8 * c + 7]));
+    }
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == 0) ptx::tmem_dealloc(tmem, kTmemCols);
+  return;
+
+abort:
+  if (tid == 0) {
+    if (kv_pending) ptx::mbar_wait(&sm.bar_kv, 0, kDrainLimitNs, P.err, 299);
+    if (q_pending) ptx::mbar_wait(&sm.bar_q, q_phase, kDrainLimitNs, P.err, 299);
+    if (mma_pending) ptx::mbar_wait(&sm.bar_mma, mma_phase, kDrainLimitNs, P.err, 299);
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == 0) ptx::tmem_dealloc(tmem, kTmemCols);
+}
+
+// ---------------------------------------------------------------- 3. dq
+__global__ void __launch_bounds__(256) dq_finalize_kernel(const float* __restrict__ acc, __nv_bfloat16* __restrict__ dq,
+                                                          const int32_t* __restrict__ pos_id,
+                                                          const float2* __restrict__ hi_tab,
+                                                          const float2* __restrict__ lo_tab, int64_t T, int H,
+                                                          int D, int layout) {
+  const int half = D / 2, quads = half / 4;
+  const int64_t n = T * H * quads;
+  for (int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; idx < n; idx += (int64_t)gridDim.x * blockDim.x) {
+    const int qd = (int)(idx % quads);
+    const int64_t row = idx / quads;
+    const int pos = __ldg(pos_id + row / H);
+    const float* a = acc + row * D;
+    __nv_bfloat16* y = dq + row * D;
+    float x0[4], x1[4];
+    int i0[4], i1[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int p = qd * 4 + e;
+      i0[e] = layout == 1 ? p : 2 * p;
+      i1[e] = layout == 1 ? p + half : 2 * p + 1;
+    }
+    if (layout == 1) {
+      const float4 u = *reinterpret_cast<const float4*>(a + qd * 4);
+      const float4 w = *reinterpret_cast<const float4*>(a + half + qd * 4);
+      x0[0] = u.x; x0[1] = u.y; x0[2] = u.z; x0[3] = u.w;
+      x1[0] = w.x; x1[1] = w.y; x1[2] = w.z; x1[3] = w.w;
+    } else {
+      const float4 u = *reinterpret_cast<const float4*>(a + qd * 8);
+      const float4 w = *reinterpret_cast<const float4*>(a + qd * 8 + 4);
+      x0[0] = u.x; x1[0] = u.y; x0[1] = u.z; x1[1] = u.w;
+      x0[2] = w.x; x1[2] = w.y; x0[3] = w.z; x1[3] = w.w;
+    }
+    if (layout != 2) {
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float2 cs = rope_cs(hi_tab, lo_tab, pos, qd * 4 + e, half);
+        rope_pair(x0[e], x1[e], cs.x, -cs.y);
+      }
+    }
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      y[i0[e]] = __float2bfloat16_rn(x0[e]);
+      y[i1[e]] = __float2bfloat16_rn(x1[e]);
+    }
+  }
+}
+
+// ---------------------------------------------------------------- 4. anchor
+__global__ void anchor_finalize_kernel(Workspace ws, __nv_bfloat16* __restrict__ dk, __nv_bfloat16* __restrict__ dv,
+                                       const int32_t* __restrict__ pos_id, const float2* __restrict__ hi_tab,
+                                       const float2* __restrict__ lo_tab, int Hq, int Hkv, int D, int layout) {
+  const int g = blockIdx.x, group = Hq / Hkv;
+  extern __shared__ float sh[];  // [2][D]
+  for (int c = threadIdx.x; c < D; c += blockDim.x) {
+    float sdv = 0.f, sdk = 0.f;
+    for (int hh = 0; hh < group; ++hh) {
+      const int h = g * group + hh;
+      for (int b = 0; b < kPrepChunks; ++b) {
+        sdv += ws.part_dv[((size_t)b * Hq + h) * D + c];
+        sdk += ws.part_dk[((size_t)b * Hq + h) * D + c];
+      }
+    }
+    sh[c] = sdv;
+    sh[D + c] = sdk;
+  }
+  __syncthreads();
+  const int pos = __ldg(pos_id);
+  for (int p = threadIdx.x; p < D / 2; p += blockDim.x) {
+    const int ia = layout == 1 ? p : 2 * p, ib = layout == 1 ? p + D / 2 : 2 * p + 1;
+    float a = sh[D + ia], b = sh[D + ib];
+    if (layout != 2) {
+      const float2 cs = rope_cs(hi_tab, lo_tab, pos, p, D / 2);
+      rope_pair(a, b, cs.x, -cs.y);
+    }
+    dk[(size_t)g * D + ia] = __float2bfloat16_rn(a);
+    dk[(size_t)g * D + ib] = __float2bfloat16_rn(b);
+    dv[(size_t)g * D + ia] = __float2bfloat16_rn(sh[ia]);
+    dv[(size_t)g * D + ib] = __float2bfloat16_rn(sh[ib]);
+  }
+}
+
+template <int HD>
+aa_status launch_bwd(aa_plan_s* p, const void* q, const void* k, const void* v, const void* o, const float* lse,
+                     const void* dout, void* dq, void* dk, void* dv, void* workspace, cudaStream_t s) {
+  size_t need = 0;
+  Workspace ws = carve(workspace, p, &need);
+  cudaError_t e;
+  const int rope_layout = p->cfg.rope_layout;
+  bwd_prep_kernel<HD><<<dim3(kPrepChunks, p->Hq), 128, 0, s>>>(
+      static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(k),
+      static_cast<const __nv_bfloat16*>(v), static_cast<const __nv_bfloat16*>(o),
+      static_cast<const __nv_bfloat16*>(dout), lse, ws, p->dev.pos_id, p->dev.rope_hi, p->dev.rope_lo, p->T, p->Hq,
+      p->group, rope_layout, p->anchor ? 1 : 0, p->scale);
+  if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(e, "bwd_prep_kernel launch");
+
+  CUtensorMap tq, tk, tv, tdo;
+  aa_status st;
+  if ((st = make_tile_map(&tq, q, p->T, p->Hq, HD)) != AA_OK) return st;
+  if ((st = make_tile_map(&tk, k, p->T, p->Hkv, HD)) != AA_OK) return st;
+  if ((st = make_tile_map(&tv, v, p->T, p->Hkv, HD)) != AA_OK) return st;
+  if ((st = make_tile_map(&tdo, dout, p->T, p->Hq, HD)) != AA_OK) return st;
+  BwdParams P;
+  P.dk = static_cast<__nv_bfloat16*>(dk);
+  P.dv = static_cast<__nv_bfloat16*>(dv);
+  P.lse = lse;
+  P.ws = ws;
+  P.pos_id = p->dev.pos_id;
+  P.key_hi = p->dev.key_hi;
+  P.items = p->dev.bwd_items;
+  P.rope_hi = p->dev.rope_hi;
+  P.rope_lo = p->dev.rope_lo;
+  P.err = p->dev.err;
+  P.wait_limit_ns = p->wait_limit_ns;
+  P.T = p->T;
+  P.Hq = p->Hq;
+  P.Hkv = p->Hkv;
+  P.group = p->group;
+  P.layout = rope_layout;
+  P.scale = p->scale;
+  const size_t smem = sizeof(BwdSmem<HD>) + 1024;
+  e = cudaFuncSetAttribute(attn_bwd_kernel<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return cuda_fail(e, "attn_bwd_kernel smem attribute");
+  if (p->bwd_ev_start && (e = cudaEventRecord(p->bwd_ev_start, s)) != cudaSuccess)
+    return cuda_fail(e, "recording the bwd start event");
+  attn_bwd_kernel<HD><<<(unsigned)p->bwd_items.size(), 128, smem, s>>>(tq, tk, tv, tdo, P);
+  if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(e, "attn_bwd_kernel launch");
+  if (p->bwd_ev_stop && (e = cudaEventRecord(p->bwd_ev_stop, s)) != cudaSuccess)
+    return cuda_fail(e, "recording the bwd stop event");
+
+  const int64_t n = (int64_t)p->T * p->Hq * (HD / 8);
+  int64_t blocks = std::min<int64_t>((n + 255) / 256, (int64_t)p->num_sms * 8);
+  dq_finalize_kernel<<<(unsigned)blocks, 256, 0, s>>>(ws.dq_acc, static_cast<__nv_bfloat16*>(dq), p->dev.pos_id,
+                                                      p->dev.rope_hi, p->dev.rope_lo, p->T, p->Hq, HD, rope_layout);
+  if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(e, "dq_finalize_kernel launch");
+  if (p->anchor) {
+    anchor_finalize_kernel<<<p->Hkv, 128, 2 * HD * sizeof(float), s>>>(
+        ws, static_cast<__nv_bfloat16*>(dk), static_cast<__nv_bfloat16*>(dv), p->dev.pos_id, p->dev.rope_hi,
+        p->dev.rope_lo, p->Hq, p->Hkv, HD, rope_layout);
+    if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(e, "anchor_finalize_kernel launch");
+  }
+  return AA_OK;
+}
+
+}  // namespace
+}  // namespace aa
+
+using namespace aa;
+
+extern "C" size_t aa_bwd_workspace_bytes(aa_plan_t p) {
+  if (!p) return 0;
+  size_t total = 0;
+  carve(nullptr, p, &total);
+  return total;
+}
+
+extern "C" aa_status aa_bwd(aa_plan_t p, const void* q, const void* k, const void* v, const void* o,
+                            const float* lse, const void* dout, void* dq, void* dk, void* dv, void* workspace,
+                            size_t workspace_bytes, aa_stream_t stream) {
+  aa_status st = check_compute_plan(p);
+  if (st != AA_OK) return st;
+  const void* ptrs[] = {q, k, v, o, lse, dout, dq, dk, dv};
+  for (const void* x : ptrs) {
+    if (!x) return fail(AA_ERR_INVALID_ARG, "NULL tensor pointer");
+    if (!aligned16(x)) return fail(AA_ERR_INVALID_ARG, "tensors must be 16-byte aligned");
+  }
+  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+    return fail(AA_ERR_INVALID_ARG, "workspace must be a 256-byte aligned device pointer");
+  if (workspace_bytes < aa_bwd_workspace_bytes(p))
+    return fail(AA_ERR_INVALID_ARG, "workspace is smaller than aa_bwd_workspace_bytes()");
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  return p->D == 128 ? launch_bwd<128>(p, q, k, v, o, lse, dout, dq, dk, dv, workspace, s)
+                     : launch_bwd<64>(p, q, k, v, o, lse, dout, dq, dk, dv, workspace, s);
+}

@@ -1,0 +1,355 @@
+// Host planner: turns cu_doclens into per-token metadata, tile work lists and
+// RoPE tables, and owns their device copies.
+//
+// Method: "When Precision Meets Position: BFloat16 Breaks Down RoPE in
+// Long-Context Training", architecture page, §3.4 "AnchorAttention: The Shared
+// Anchor Design" ("Mask construction": anchor column visible to every row,
+// intra-document causal attention, cross-document pairs masked) and §3.4
+// "Document Token Indexing" (continuous vs reset position IDs). The pages fix
+// the mask; the tiling and the work order are this library's.
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+#include <algorithm>
+#include <new>
+#include <string>
+
+#include "aa_internal.h"
+
+namespace aa {
+
+static thread_local std::string g_last_error;
+
+aa_status fail(aa_status s, const std::string& msg) {
+  g_last_error = msg;
+  return s;
+}
+
+aa_status cuda_fail(cudaError_t e, const char* what) {
+  g_last_error = std::string(what) + ": " + cudaGetErrorString(e);
+  return AA_ERR_CUDA;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+aa_status check_compute_plan(const aa_plan_s* p) {
+  if (!p) return fail(AA_ERR_INVALID_ARG, "plan is NULL");
+  if (p->host_only) return fail(AA_ERR_INVALID_ARG, "plan was built with host_only = 1");
+  return AA_OK;
+}
+
+// Visible-interval metadata. Row i sees keys [row_lo[i], i] through the tile
+// path; key j is seen by rows [j, key_hi[j]]. With the anchor handled
+// separately (ANCHOR mode) key 0 is removed from both: row_lo >= 1, the anchor
+// row's interval is empty, and key_hi[0] = -1.
+static void build_token_metadata(aa_plan_s* p) {
+  const int T = p->T;
+  p->doc_id.assign(T, 0);
+  p->pos_id.assign(T, 0);
+  p->row_lo.assign(T, 0);
+  p->key_hi.assign(T, T - 1);
+  const int mode = p->cfg.mask_mode;
+  const bool continuous = mode == AA_MASK_CAUSAL || p->cfg.pos_mode == AA_POS_CONTINUOUS;
+  if (mode == AA_MASK_CAUSAL) {
+    for (int i = 0; i < T; ++i) p->pos_id[i] = i + p->cfg.pos_shift;
+    return;
+  }
+  // anchor token
+  p->doc_id[0] = 0;
+  p->pos_id[0] = p->cfg.pos_shift;
+  p->row_lo[0] = p->anchor ? 1 : 0;   // ANCHOR: empty tile interval [1, 0]
+  p->key_hi[0] = p->anchor ? -1 : 0;  // INTRA_DOC: the anchor sees only itself
+  const int K = (int)p->cu.size() - 1;
+  for (int k = 1; k <= K; ++k) {
+    const int a = p->cu[k - 1], b = p->cu[k];
+    for (int i = a; i < b; ++i) {
+      p->doc_id[i] = k;
+      p->pos_id[i] = (continuous ? i : (i - a + 1)) + p->cfg.pos_shift;
+      p->row_lo[i] = a;
+      p->key_hi[i] = b - 1;
+    }
+  }
+}
+
+static void build_stats_and_work(aa_plan_s* p) {
+  const int T = p->T, nt = p->n_tiles;
+  // pair count: closed form per mode
+  if (p->cfg.mask_mode == AA_MASK_CAUSAL) {
+    p->unmasked_pairs = (int64_t)T * (T + 1) / 2;
+  } else {
+    int64_t s = 1;  // the anchor's own pair
+    for (size_t k = 1; k < p->cu.size(); ++k) {
+      const int64_t n = p->cu[k] - p->cu[k - 1];
+      s += n * (n + 1) / 2;
+      if (p->anchor) s += n;  // one anchor edge per document token
+    }
+    p->unmasked_pairs = s;
+  }
+  p->causal_tiles = (int64_t)nt * (nt + 1) / 2;
+  p->live_tiles = 0;
+  p->fwd_items.clear();
+  p->bwd_items.clear();
+  std::vector<WorkItem> q_ranges(nt);
+  for (int a = 0; a < nt; ++a) {
+    const int r0 = a * kTile, r1 = std::min(T, r0 + kTile) - 1;
+    int lo = -1;
+    for (int i = r0; i <= r1; ++i)
+      if (p->row_lo[i] <= i) { lo = p->row_lo[i]; break; }  // row_lo is non-decreasing
+    // every tile holds at least one row that sees itself
+    const int kt_lo = lo / kTile;
+    q_ranges[a] = WorkItem{a, 0, kt_lo, a};
+    int64_t live = a - kt_lo + 1;
+    if (p->anchor && kt_lo > 0) live += 1;  // the anchor column's block
+    p->live_tiles += live;
+  }
+  for (int h = 0; h < p->Hq; ++h)
+    for (int a = 0; a < nt; ++a) {
+      WorkItem w = q_ranges[a];
+      w.head = h;
+      p->fwd_items.push_back(w);
+    }
+  for (int g = 0; g < p->Hkv; ++g)
+    for (int b = 0; b < nt; ++b) {
+      const int j0 = b * kTile, j1 = std::min(T, j0 + kTile) - 1;
+      int hi = -1;
+      for (int j = j0; j <= j1; ++j) hi = std::max(hi, p->key_hi[j]);
+      if (hi < j0) continue;  // no key of this tile is seen through the tile path
+      p->bwd_items.push_back(WorkItem{b, g, b, hi / kTile});
+    }
+  // longest first (LPT); ties in a fixed order so plans are reproducible
+  auto by_cost = [](const WorkItem& x, const WorkItem& y) {
+    const int cx = x.hi - x.lo, cy = y.hi - y.lo;
+    if (cx != cy) return cx > cy;
+    if (x.tile != y.tile) return x.tile < y.tile;
+    return x.head < y.head;
+  };
+  std::stable_sort(p->fwd_items.begin(), p->fwd_items.end(), by_cost);
+  std::stable_sort(p->bwd_items.begin(), p->bwd_items.end(), by_cost);
+  p->fwd_tiles = 0;
+  for (auto& w : p->fwd_items) p->fwd_tiles += w.hi - w.lo + 1;
+  p->bwd_tiles = 0;
+  for (auto& w : p->bwd_items) p->bwd_tiles += (int64_t)(w.hi - w.lo + 1) * p->group;
+}
+
+// Two-level cos/sin tables for Eq. 6: pos = 128*h + l, so
+// (cos, sin)(pos*theta) is the complex product of rope_hi[h] and rope_lo[l].
+// Entries are computed in fp64 and rounded once to fp32.
+static void build_rope_tables(aa_plan_s* p) {
+  const int half = p->D / 2;
+  int max_pos = 0;
+  for (int v : p->pos_id) max_pos = std::max(max_pos, v);
+  p->n_hi = max_pos / kTile + 1;
+  std::vector<double> theta(half);
+  for (int i = 0; i < half; ++i)
+    theta[i] = std::pow(p->cfg.rope_base, -2.0 * (double)i / (double)p->D);
+  p->rope_hi.resize((size_t)p->n_hi * half);
+  p->rope_lo.resize((size_t)kTile * half);
+  for (int h = 0; h < p->n_hi; ++h)
+    for (int i = 0; i < half; ++i) {
+      const double ang = (double)h * kTile * theta[i];
+      p->rope_hi[(size_t)h * half + i] = make_float2((float)std::cos(ang), (float)std::sin(ang));
+    }
+  for (int l = 0; l < kTile; ++l)
+    for (int i = 0; i < half; ++i) {
+      const double ang = (double)l * theta[i];
+      p->rope_lo[(size_t)l * half + i] = make_float2((float)std::cos(ang), (float)std::sin(ang));
+    }
+}
+
+template <class T>
+static aa_status upload(T** dst, const std::vector<T>& src, cudaStream_t s, const char* what) {
+  const size_t bytes = std::max<size_t>(src.size(), 1) * sizeof(T);
+  cudaError_t e = cudaMalloc((void**)dst, bytes);
+  if (e != cudaSuccess) {
+    *dst = nullptr;
+    return e == cudaErrorMemoryAllocation ? fail(AA_ERR_NO_MEMORY, std::string("cudaMalloc ") + what)
+                                          : cuda_fail(e, what);
+  }
+  if (!src.empty()) {
+    e = cudaMemcpyAsync(*dst, src.data(), src.size() * sizeof(T), cudaMemcpyHostToDevice, s);
+    if (e != cudaSuccess) return cuda_fail(e, what);
+  }
+  return AA_OK;
+}
+
+static void free_device(aa_plan_s* p) {
+  DevicePlan& d = p->dev;
+  void* ptrs[] = {d.pos_id, d.row_lo, d.key_hi, d.fwd_items, d.bwd_items, d.rope_hi, d.rope_lo, d.err};
+  for (void* q : ptrs)
+    if (q) cudaFree(q);
+  d = DevicePlan{};
+}
+
+static aa_status validate(const aa_config* c, const int32_t* cu, int32_t num_docs) {
+  if (!c) return fail(AA_ERR_INVALID_ARG, "config is NULL");
+  if (c->total_tokens < 2 || c->total_tokens >= (1 << 30))
+    return fail(AA_ERR_INVALID_ARG, "total_tokens must be in [2, 2^30)");
+  if (c->num_q_heads < 1 || c->num_kv_heads < 1 || c->num_q_heads % c->num_kv_heads)
+    return fail(AA_ERR_INVALID_ARG, "need Hq >= 1, Hkv >= 1 and Hq % Hkv == 0");
+  if ((int64_t)c->num_q_heads * c->total_tokens >= (1ll << 31))
+    return fail(AA_ERR_INVALID_ARG, "Hq * T must stay below 2^31");
+  if (c->head_dim != 64 && c->head_dim != 128)
+    return fail(AA_ERR_UNSUPPORTED, "head_dim must be 64 or 128");
+  if (c->mask_mode < AA_MASK_CAUSAL || c->mask_mode > AA_MASK_ANCHOR)
+    return fail(AA_ERR_INVALID_ARG, "unknown mask_mode");
+  if (c->pos_mode != AA_POS_RESET && c->pos_mode != AA_POS_CONTINUOUS)
+    return fail(AA_ERR_INVALID_ARG, "unknown pos_mode");
+  if (c->rope_layout < AA_ROPE_ADJACENT || c->rope_layout > AA_ROPE_NONE)
+    return fail(AA_ERR_INVALID_ARG, "unknown rope_layout");
+  if (c->rope_layout != AA_ROPE_NONE && !(c->rope_base > 1.0 && std::isfinite(c->rope_base)))
+    return fail(AA_ERR_INVALID_ARG, "rope_base must be finite and > 1");
+  if (c->pos_shift < 0 || (int64_t)c->pos_shift + c->total_tokens >= (1ll << 30))
+    return fail(AA_ERR_INVALID_ARG, "pos_shift must be >= 0 and keep positions below 2^30");
+  if (!std::isfinite(c->softmax_scale)) return fail(AA_ERR_INVALID_ARG, "softmax_scale is not finite");
+  if (c->mask_mode != AA_MASK_CAUSAL) {
+    if (!cu || num_docs < 1) return fail(AA_ERR_INVALID_ARG, "cu_doclens with >= 1 document required");
+    if (cu[0] != 1) return fail(AA_ERR_INVALID_ARG, "cu_doclens[0] must be 1 (token 0 is the anchor)");
+    if (cu[num_docs] != c->total_tokens) return fail(AA_ERR_INVALID_ARG, "cu_doclens[num_docs] must equal T");
+    for (int k = 1; k <= num_docs; ++k)
+      if (cu[k] <= cu[k - 1]) return fail(AA_ERR_INVALID_ARG, "cu_doclens must increase strictly");
+  }
+  return AA_OK;
+}
+
+}  // namespace aa
+
+using namespace aa;
+
+extern "C" aa_status aa_plan(const aa_config* cfg, const int32_t* cu_doclens_host, int32_t num_docs,
+                             aa_stream_t stream, aa_plan_t* out) {
+  if (!out) return fail(AA_ERR_INVALID_ARG, "out is NULL");
+  *out = nullptr;
+  aa_status st = validate(cfg, cu_doclens_host, num_docs);
+  if (st != AA_OK) return st;
+  aa_plan_s* p = new (std::nothrow) aa_plan_s();
+  if (!p) return fail(AA_ERR_NO_MEMORY, "plan allocation");
+  p->cfg = *cfg;
+  p->T = cfg->total_tokens;
+  p->Hq = cfg->num_q_heads;
+  p->Hkv = cfg->num_kv_heads;
+  p->group = p->Hq / p->Hkv;
+  p->D = cfg->head_dim;
+  p->n_tiles = (p->T + kTile - 1) / kTile;
+  p->scale = cfg->softmax_scale > 0.f ? cfg->softmax_scale : (float)(1.0 / std::sqrt((double)p->D));
+  p->anchor = cfg->mask_mode == AA_MASK_ANCHOR;
+  p->host_only = cfg->host_only != 0;
+  if (cfg->mask_mode != AA_MASK_CAUSAL) p->cu.assign(cu_doclens_host, cu_doclens_host + num_docs + 1);
+  build_token_metadata(p);
+  build_stats_and_work(p);
+  build_rope_tables(p);
+  if (p->host_only) {
+    *out = p;
+    return AA_OK;
+  }
+  cudaError_t e = cudaGetDevice(&p->device);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&p->num_sms, cudaDevAttrMultiProcessorCount, p->device);
+  if (e != cudaSuccess) {
+    delete p;
+    return cuda_fail(e, "device query");
+  }
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  std::vector<int32_t> zero(1, 0);
+  DevicePlan& d = p->dev;
+  if ((st = upload(&d.pos_id, p->pos_id, s, "pos_id")) != AA_OK ||
+      (st = upload(&d.row_lo, p->row_lo, s, "row_lo")) != AA_OK ||
+      (st = upload(&d.key_hi, p->key_hi, s, "key_hi")) != AA_OK ||
+      (st = upload(&d.fwd_items, p->fwd_items, s, "fwd work list")) != AA_OK ||
+      (st = upload(&d.bwd_items, p->bwd_items, s, "bwd work list")) != AA_OK ||
+      (st = upload(&d.rope_hi, p->rope_hi, s, "rope table (hi)")) != AA_OK ||
+      (st = upload(&d.rope_lo, p->rope_lo, s, "rope table (lo)")) != AA_OK ||
+      (st = upload(&d.err, zero, s, "error word")) != AA_OK) {
+    cudaStreamSynchronize(s);
+    free_device(p);
+    delete p;
+    return st;
+  }
+  // the host vectors must outlive the asynchronous copies
+  e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) {
+    free_device(p);
+    delete p;
+    return cuda_fail(e, "plan upload");
+  }
+  *out = p;
+  return AA_OK;
+}
+
+extern "C" aa_status aa_plan_destroy(aa_plan_t p) {
+  if (!p) return AA_OK;
+  if (!p->host_only) {
+    cudaDeviceSynchronize();
+    free_device(p);
+  }
+  delete p;
+  return AA_OK;
+}
+
+extern "C" aa_status aa_plan_metadata(aa_plan_t p, int32_t* doc_id_host, int32_t* pos_id_host) {
+  if (!p) return fail(AA_ERR_INVALID_ARG, "plan is NULL");
+  if (doc_id_host) std::memcpy(doc_id_host, p->doc_id.data(), sizeof(int32_t) * p->T);
+  if (pos_id_host) std::memcpy(pos_id_host, p->pos_id.data(), sizeof(int32_t) * p->T);
+  return AA_OK;
+}
+
+extern "C" aa_status aa_plan_stats(aa_plan_t p, int64_t* pairs, int64_t* live, int64_t* causal) {
+  if (!p) return fail(AA_ERR_INVALID_ARG, "plan is NULL");
+  if (pairs) *pairs = p->unmasked_pairs;
+  if (live) *live = p->live_tiles;
+  if (causal) *causal = p->causal_tiles;
+  return AA_OK;
+}
+
+extern "C" aa_status aa_plan_work(aa_plan_t p, int64_t* fwd_tiles, int64_t* bwd_tiles) {
+  if (!p) return fail(AA_ERR_INVALID_ARG, "plan is NULL");
+  if (fwd_tiles) *fwd_tiles = p->fwd_tiles;
+  if (bwd_tiles) *bwd_tiles = p->bwd_tiles;
+  return AA_OK;
+}
+
+extern "C" aa_status aa_set_wait_limit(aa_plan_t p, uint64_t ns) {
+  if (!p) return fail(AA_ERR_INVALID_ARG, "plan is NULL");
+  p->wait_limit_ns = ns;
+  return AA_OK;
+}
+
+extern "C" aa_status aa_set_bwd_timing_events(aa_plan_t p, void* start, void* stop) {
+  if (!p) return fail(AA_ERR_INVALID_ARG, "plan is NULL");
+  if ((start == nullptr) != (stop == nullptr))
+    return fail(AA_ERR_INVALID_ARG, "give both timing events or neither");
+  p->bwd_ev_start = static_cast<cudaEvent_t>(start);
+  p->bwd_ev_stop = static_cast<cudaEvent_t>(stop);
+  return AA_OK;
+}
+
+extern "C" aa_status aa_check_device_error(aa_plan_t p, aa_stream_t stream) {
+  aa_status st = check_compute_plan(p);
+  if (st != AA_OK) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  int32_t word = 0;
+  cudaError_t e = cudaMemcpyAsync(&word, p->dev.err, sizeof(word), cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return cuda_fail(e, "reading the device error word");
+  if (word != 0) {
+    e = cudaMemsetAsync(p->dev.err, 0, sizeof(int32_t), s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return cuda_fail(e, "clearing the device error word");
+    char buf[96];
+    std::snprintf(buf, sizeof buf, "device wait timed out (site code %d)", (int)word);
+    return fail(AA_ERR_TIMEOUT, buf);
+  }
+  return AA_OK;
+}
+
+extern "C" const char* aa_status_string(aa_status s) {
+  switch (s) {
+    case AA_OK: return "AA_OK";
+    case AA_ERR_INVALID_ARG: return "AA_ERR_INVALID_ARG";
+    case AA_ERR_UNSUPPORTED: return "AA_ERR_UNSUPPORTED";
+    case AA_ERR_CUDA: return "AA_ERR_CUDA";
+    case AA_ERR_NO_MEMORY: return "AA_ERR_NO_MEMORY";
+    case AA_ERR_TIMEOUT: return "AA_ERR_TIMEOUT";
+  }
+  return "AA_ERR_UNKNOWN";
+}
+
+extern "C" const char* aa_last_error(void) { return g_last_error.c_str(); }

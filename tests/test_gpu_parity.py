@@ -1,0 +1,171 @@
+"""GPU parity: the CUDA path through the C ABI against the fp64 oracle.
+
+Element-wise at sizes the oracle finishes in seconds (several tiles, ragged
+tails, documents shorter than a tile, GQA, every mask/position/RoPE mode),
+sampled at the full workload sizes, plus run-to-run determinism and
+fused-vs-unfused RoPE bit identity.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle as orc
+from aa_synth import WORKLOADS, make_qkv, workload_cu_doclens
+from gpu_common import (REL_L2, check_forward, f64, inputs, problem, rel_l2)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def aa():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import __graft_entry__
+    __graft_entry__.build()
+    import packed_sequence_rope_gb300 as pkg
+    return pkg
+
+
+def _bf16_ulp(x):
+    ax = np.maximum(np.abs(x), 1e-30)
+    return 2.0 ** (np.floor(np.log2(ax)) - 7)
+
+
+# --------------------------------------------------------------------------- RoPE
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("layout", [orc.ROPE_ADJACENT, orc.ROPE_HALF])
+@pytest.mark.parametrize("shift", [0, 120000])
+def test_rope_apply_matches_oracle(aa, D, layout, shift):
+    T, H = 777, 3
+    cu = [1, 200, 201, 777]
+    x = torch.randn(T, H, D, device="cuda").to(torch.bfloat16)
+    with aa.Plan(cu, T, H, H, D, 5e5, orc.MASK_ANCHOR, orc.POS_CONTINUOUS, layout, pos_shift=shift) as p:
+        y = p.rope_apply(x)
+        back = p.rope_apply(y, inverse=True)
+        torch.cuda.synchronize()
+    pos = orc.position_ids(cu, T, orc.MASK_ANCHOR, orc.POS_CONTINUOUS, shift)
+    ref = orc.rotate(f64(x), pos, 5e5, layout)
+    # fp32 rotation rounded once to bf16: within one bf16 ulp of the exact value
+    assert (np.abs(f64(y) - ref) <= _bf16_ulp(ref) + 1e-6).all()
+    ref_back = orc.rotate(f64(y), pos, 5e5, layout, inverse=True)
+    assert (np.abs(f64(back) - ref_back) <= _bf16_ulp(ref_back) + 1e-6).all()
+
+
+def test_rope_none_is_copy(aa):
+    x = torch.randn(300, 2, 64, device="cuda").to(torch.bfloat16)
+    with aa.Plan([1, 300], 300, 2, 2, 64, 1e4, rope_layout=orc.ROPE_NONE) as p:
+        assert torch.equal(p.rope_apply(x), x)
+
+
+# --------------------------------------------------------------------------- fwd/bwd small
+CASES = [
+    # name, cu, T, Hq, Hkv, D, base, mode, pos, layout
+    ("tiny", [1, 32, 96, 192, 256], 256, 1, 1, 64, 1e4, orc.MASK_ANCHOR, orc.POS_RESET, orc.ROPE_ADJACENT),
+    ("ragged_gqa", [1, 5, 140, 141, 400, 1000, 1301], 1301, 4, 2, 128, 5e6, orc.MASK_ANCHOR, orc.POS_RESET,
+     orc.ROPE_ADJACENT),
+    ("continuous", [1, 300, 301, 700, 1100], 1100, 2, 2, 128, 1e4, orc.MASK_ANCHOR, orc.POS_CONTINUOUS,
+     orc.ROPE_ADJACENT),
+    ("intra_doc", [1, 129, 500, 900], 900, 2, 1, 128, 1e4, orc.MASK_INTRA_DOC, orc.POS_RESET, orc.ROPE_ADJACENT),
+    ("causal", None, 700, 2, 2, 128, 1e4, orc.MASK_CAUSAL, orc.POS_RESET, orc.ROPE_ADJACENT),
+    ("half_d64", [1, 64, 65, 333, 640], 640, 2, 2, 64, 1e4, orc.MASK_ANCHOR, orc.POS_RESET, orc.ROPE_HALF),
+    ("no_rope", [1, 50, 600], 600, 2, 1, 128, 1e4, orc.MASK_ANCHOR, orc.POS_RESET, orc.ROPE_NONE),
+    ("single_doc", [1, 513], 513, 2, 2, 128, 1e4, orc.MASK_ANCHOR, orc.POS_RESET, orc.ROPE_ADJACENT),
+    ("two_tokens", [1, 2], 2, 1, 1, 128, 1e4, orc.MASK_ANCHOR, orc.POS_RESET, orc.ROPE_ADJACENT),
+]
+
+
+@pytest.mark.parametrize("case", CASES, ids=[c[0] for c in CASES])
+def test_fwd_bwd_elementwise(aa, case):
+    name, cu, T, Hq, Hkv, D, base, mode, pos, layout = case
+    q, k, v, do = inputs(T, Hq, Hkv, D, seed=len(name))
+    with aa.Plan(cu, T, Hq, Hkv, D, base, mode, pos, layout) as p:
+        o, lse = p.fwd(q, k, v)
+        dq, dk, dv = p.bwd(q, k, v, o, lse, do)
+        torch.cuda.synchronize()
+        p.check_device_error()
+    prob = problem(cu, T, Hq, Hkv, D, base, mode, pos, layout)
+    O, L = orc.forward(prob, q.cpu(), k.cpu(), v.cpu())
+    check_forward(o, lse, O, L, tag=name)
+    gq, gk, gv = orc.backward(prob, q.cpu(), k.cpu(), v.cpu(), do.cpu())
+    for nm, got, ref in (("dq", dq, gq), ("dk", dk, gk), ("dv", dv, gv)):
+        e = rel_l2(got, ref)
+        assert e <= REL_L2, f"{name} {nm} rel-L2 {e:.3e}"
+
+
+def test_anchor_row_and_gradients_of_anchor(aa):
+    # the anchor row returns v_0 exactly (up to bf16 rounding of a copy)
+    T, H, D = 1000, 2, 128
+    cu = [1, 100, 450, 1000]
+    q, k, v, do = inputs(T, H, H, D, seed=7)
+    with aa.Plan(cu, T, H, H, D, 1e4) as p:
+        o, lse = p.fwd(q, k, v)
+        dq, dk, dv = p.bwd(q, k, v, o, lse, do)
+        torch.cuda.synchronize()
+    assert torch.equal(o[0], v[0])
+    gq, gk, gv = orc.backward(problem(cu, T, H, H, D, 1e4), q.cpu(), k.cpu(), v.cpu(), do.cpu())
+    assert rel_l2(dk[0], gk[0]) <= REL_L2 and rel_l2(dv[0], gv[0]) <= REL_L2
+
+
+def test_determinism_and_fused_equals_unfused(aa):
+    T, Hq, Hkv, D = 1500, 4, 2, 128
+    cu = [1, 90, 600, 1100, 1500]
+    q, k, v, do = inputs(T, Hq, Hkv, D, seed=3)
+    with aa.Plan(cu, T, Hq, Hkv, D, 5e6) as p, \
+            aa.Plan(cu, T, Hq, Hkv, D, 5e6, rope_layout=orc.ROPE_NONE) as pn:
+        o1, l1 = p.fwd(q, k, v)
+        o2, l2 = p.fwd(q, k, v)
+        _, dk1, dv1 = p.bwd(q, k, v, o1, l1, do)
+        _, dk2, dv2 = p.bwd(q, k, v, o1, l1, do)
+        # unfused: rotate with aa_rope_apply, then attention with RoPE disabled
+        o3, l3 = pn.fwd(p.rope_apply(q), p.rope_apply(k), v)
+        torch.cuda.synchronize()
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+    assert torch.equal(dk1, dk2) and torch.equal(dv1, dv2)
+    assert torch.equal(o1, o3) and torch.equal(l1, l3)
+
+
+# --------------------------------------------------------------------------- full sizes, sampled
+def _sample_rows(cu, T, n, seed):
+    rng = np.random.default_rng(seed)
+    starts = np.asarray(cu[:-1], dtype=np.int64)
+    rows = np.unique(np.concatenate([[0, 1, T - 1], starts, rng.integers(0, T, n)]))
+    return rows
+
+
+@pytest.mark.parametrize("name", ["llama7b_8k", "llama7b_64k"])
+def test_full_size_forward_sampled(aa, name):
+    w = WORKLOADS[name]
+    cu = workload_cu_doclens(w)
+    q, k, v, do = make_qkv(w, device="cuda", with_grad_out=False)
+    with aa.Plan(cu, w.total_tokens, w.num_q_heads, w.num_kv_heads, w.head_dim, w.rope_base) as p:
+        o, lse = p.fwd(q, k, v)
+        torch.cuda.synchronize()
+        p.check_device_error()
+    rows = _sample_rows(cu, w.total_tokens, 96, 0)
+    prob = problem(cu, w.total_tokens, w.num_q_heads, w.num_kv_heads, w.head_dim, w.rope_base)
+    O, L = orc.forward(prob, q.cpu(), k.cpu(), v.cpu(), rows=rows)
+    check_forward(o, lse, O, L, rows=rows, tag=name)
+
+
+def test_full_size_backward_documents(aa):
+    # documents are independent apart from the anchor: the oracle restricted
+    # to one document's rows gives that document's complete dq, dk, dv
+    w = WORKLOADS["llama7b_8k"]
+    cu = workload_cu_doclens(w)
+    T = w.total_tokens
+    q, k, v, do = make_qkv(w, device="cuda")
+    with aa.Plan(cu, T, w.num_q_heads, w.num_kv_heads, w.head_dim, w.rope_base) as p:
+        o, lse = p.fwd(q, k, v)
+        dq, dk, dv = p.bwd(q, k, v, o, lse, do)
+        torch.cuda.synchronize()
+        p.check_device_error()
+    prob = problem(cu, T, w.num_q_heads, w.num_kv_heads, w.head_dim, w.rope_base)
+    lens = np.diff(cu)
+    picks = [int(np.argmin(lens)), int(np.argmax(lens)), len(lens) - 1]
+    for d in sorted(set(picks)):
+        a, b = int(cu[d]), int(cu[d + 1])
+        rows = np.arange(a, b)
+        gq, gk, gv = orc.backward(prob, q.cpu(), k.cpu(), v.cpu(), do.cpu(), rows=rows)
+        for nm, got, ref in (("dq", dq[a:b], gq[a:b]), ("dk", dk[a:b], gk[a:b]), ("dv", dv[a:b], gv[a:b])):
+            e = rel_l2(got, ref)
+            assert e <= REL_L2, f"doc {d} {nm} rel-L2 {e:.3e}"

@@ -1,0 +1,128 @@
+"""Host-side tests of the C-ABI library: exports, planner metadata bit-exact
+against the oracle, statistics, and synchronous argument validation.
+No GPU needed: plans are built with host_only = 1."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+import oracle as orc
+from aa_synth import WORKLOADS, doc_lengths, pack, workload_cu_doclens
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def aa():
+    import __graft_entry__
+    __graft_entry__.build()
+    import packed_sequence_rope_gb300 as pkg
+    return pkg
+
+
+def test_library_exports_every_declared_symbol(aa):
+    header = open(os.path.join(ROOT, "include", "anchorattn.h")).read()
+    declared = set(re.findall(r"^\s*(?:aa_status|size_t|const char\*)\s+(aa_\w+)\s*\(", header, re.M))
+    assert declared == set(aa.EXPORTS)
+    L = ctypes.CDLL(aa.binding.LIB_PATH)
+    for name in declared:
+        assert hasattr(L, name), name
+
+
+def _plan(aa, cu, T, mode=orc.MASK_ANCHOR, pos=orc.POS_RESET, shift=0, Hq=2, Hkv=1, D=128):
+    return aa.Plan(cu, T, Hq, Hkv, D, 1e4, mode, pos, pos_shift=shift, host_only=True)
+
+
+@pytest.mark.parametrize("mode", [orc.MASK_ANCHOR, orc.MASK_INTRA_DOC, orc.MASK_CAUSAL])
+@pytest.mark.parametrize("pos", [orc.POS_RESET, orc.POS_CONTINUOUS])
+@pytest.mark.parametrize("seed", [0, 1])
+def test_metadata_bit_exact_vs_oracle(aa, mode, pos, seed):
+    rng = np.random.default_rng(seed)
+    T = 700 + 291 * seed
+    cu = pack(doc_lengths("loguniform", T - 1, rng, lo=3, hi=400), T)
+    shift = 17 * seed
+    with _plan(aa, cu, T, mode, pos, shift) as p:
+        doc, posv = p.metadata()
+        assert np.array_equal(doc, orc.document_ids(cu, T, mode))
+        assert np.array_equal(posv, orc.position_ids(cu, T, mode, pos, shift))
+        st = p.stats()
+        assert st["unmasked_pairs"] == orc.unmasked_pairs(cu, T, mode)
+        live, causal = orc.tile_counts(cu, T, mode)
+        assert (st["live_tiles"], st["causal_tiles"]) == (live, causal)
+
+
+def test_metadata_tiny_workload(aa):
+    w = WORKLOADS["tiny_256"]
+    cu = workload_cu_doclens(w)
+    assert list(cu) == [1, 32, 96, 192, 256]
+    with aa.Plan(cu, 256, 1, 1, 64, 1e4, host_only=True) as p:
+        doc, pos = p.metadata()
+        assert pos[0] == 0 and pos[1] == 1 and pos[31] == 31 and pos[32] == 1 and pos[255] == 64
+        assert p.stats()["unmasked_pairs"] == orc.unmasked_pairs(cu, 256, orc.MASK_ANCHOR)
+
+
+def test_work_counts(aa):
+    # a single document: the forward visits every causal tile per head;
+    # the backward the same count per kv head and group member
+    T = 1000
+    with aa.Plan([1, T], T, 4, 2, 128, 1e4, host_only=True) as p:
+        nt = (T + 127) // 128
+        w = p.work()
+        assert w["fwd_tiles"] == 4 * nt * (nt + 1) // 2
+        assert w["bwd_tiles"] == 4 * nt * (nt + 1) // 2
+
+
+@pytest.mark.parametrize("kwargs,cu,msg", [
+    (dict(total_tokens=1), [1], "total_tokens"),
+    (dict(num_q_heads=3, num_kv_heads=2), [1, 64], "Hq % Hkv"),
+    (dict(head_dim=96), [1, 64], "head_dim"),
+    (dict(), [0, 64], "cu_doclens\\[0\\]"),
+    (dict(), [1, 63], "must equal T"),
+    (dict(), [1, 30, 30, 64], "increase strictly"),
+    (dict(rope_base=1.0), [1, 64], "rope_base"),
+    (dict(pos_shift=-1), [1, 64], "pos_shift"),
+    (dict(mask_mode=7), [1, 64], "mask_mode"),
+])
+def test_invalid_arguments_rejected(aa, kwargs, cu, msg):
+    args = dict(total_tokens=64, num_q_heads=2, num_kv_heads=1, head_dim=128, rope_base=1e4,
+                mask_mode=orc.MASK_ANCHOR, pos_shift=0)
+    args.update(kwargs)
+    with pytest.raises(aa.AAError, match=msg) as ei:
+        aa.Plan(cu, args["total_tokens"], args["num_q_heads"], args["num_kv_heads"], args["head_dim"],
+                args["rope_base"], args["mask_mode"], pos_shift=args["pos_shift"], host_only=True)
+    assert ei.value.status in (1, 2)
+
+
+def test_compute_on_host_only_plan_is_refused(aa):
+    with _plan(aa, [1, 64], 64) as p:
+        L = aa.lib()
+        assert L.aa_fwd(p._h, None, None, None, None, None, None) == 1
+        assert "host_only" in L.aa_last_error().decode()
+        assert L.aa_check_device_error(p._h, None) == 1
+
+
+def test_status_strings(aa):
+    L = aa.lib()
+    assert [L.aa_status_string(i).decode() for i in range(6)] == [
+        "AA_OK", "AA_ERR_INVALID_ARG", "AA_ERR_UNSUPPORTED", "AA_ERR_CUDA", "AA_ERR_NO_MEMORY", "AA_ERR_TIMEOUT"]
+
+
+def test_causal_mode_ignores_cu_doclens(aa):
+    with aa.Plan(None, 300, 1, 1, 64, 1e4, orc.MASK_CAUSAL, host_only=True) as p:
+        doc, pos = p.metadata()
+        assert not doc.any() and np.array_equal(pos, np.arange(300))
+        assert p.stats()["unmasked_pairs"] == 300 * 301 // 2
+
+
+@pytest.mark.parametrize("name", ["llama7b_8k", "llama7b_64k"])
+def test_workload_stats_vs_oracle(aa, name):
+    w = WORKLOADS[name]
+    cu = workload_cu_doclens(w)
+    T = w.total_tokens
+    with aa.Plan(cu, T, w.num_q_heads, w.num_kv_heads, w.head_dim, w.rope_base, host_only=True) as p:
+        st = p.stats()
+        assert st["unmasked_pairs"] == orc.unmasked_pairs(cu, T, orc.MASK_ANCHOR)
+        if T <= 8192:
+            assert st["live_tiles"] == orc.tile_counts(cu, T, orc.MASK_ANCHOR)[0]
