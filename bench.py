@@ -161,6 +161,12 @@ def run_ours(args):
         step()
     plan.check_device_error()
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    # torch creates events lazily and only times events it has recorded: record
+    # the hook's pair once here so the library re-records existing handles
+    for e in ev:
+        e[2].record(stream)
+        e[3].record(stream)
+    torch.cuda.synchronize()
     clocks = ClockSampler(local)
     _barrier(world)
     clocks.start()

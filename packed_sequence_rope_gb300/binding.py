@@ -159,6 +159,8 @@ class Plan:
 
     def set_bwd_timing_events(self, start=None, stop=None):
         """torch.cuda.Event pair (enable_timing=True) recorded around the main bwd kernel."""
+        if start is not None and (not start.cuda_event or not stop.cuda_event):
+            raise ValueError("record the events once with torch first so that they exist")
         a = ctypes.c_void_p(start.cuda_event) if start is not None else None
         b = ctypes.c_void_p(stop.cuda_event) if stop is not None else None
         _check(lib().aa_set_bwd_timing_events(self._h, a, b))
