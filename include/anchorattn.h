@@ -153,6 +153,31 @@ aa_status aa_bwd(aa_plan_t plan, const void* q, const void* k, const void* v, co
                  const float* lse, const void* dout, void* dq, void* dk, void* dv,
                  void* workspace, size_t workspace_bytes, aa_stream_t stream);
 
+/* aa_bwd without a caller-provided workspace (no counterpart in the paper:
+ * an interface addition of this library).
+ * Some callers cannot call cudaMalloc at the point where they run the
+ * backward pass: a plugin inside a host framework whose memory planner owns
+ * every device allocation, a latency-critical loop where an allocation would
+ * stall or synchronise the device, or a deployment that must stay inside a
+ * memory budget fixed at start-up. This entry point takes its scratch from a
+ * 64 MiB array that the library reserves statically on every GPU that loads
+ * it (held until the process exits) and allocates nothing itself.
+ *  - Arguments and results are those of aa_bwd minus the workspace pair.
+ *  - Plans whose aa_bwd_workspace_bytes() exceeds 64 MiB are rejected with
+ *    AA_ERR_INVALID_ARG and a message giving both sizes (roughly T * Hq up to
+ *    120K query rows at D = 128); nothing is launched.
+ *  - The plan's device must be current. The first call on a device looks up
+ *    the array's device address (cudaGetSymbolAddress) once; make that first
+ *    call before any stream capture on that device.
+ *  - Every call on a device shares the one array, and the array keeps the
+ *    last call's contents; the call overwrites all the scratch it reads, so
+ *    nothing needs clearing. Calls whose executions overlap on the GPU (for
+ *    instance on two streams) race on the array and give wrong results:
+ *    order them on one stream or with events. */
+aa_status aa_bwd_static_workspace(aa_plan_t plan, const void* q, const void* k, const void* v,
+                                  const void* o, const float* lse, const void* dout, void* dq, void* dk,
+                                  void* dv, aa_stream_t stream);
+
 /* Synchronise `stream`, read and clear the plan's device error word.
  * Returns AA_ERR_TIMEOUT if a bounded device wait ran out since the last
  * check, AA_OK otherwise. */

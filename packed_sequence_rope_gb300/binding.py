@@ -22,7 +22,7 @@ STATUS = {0: "AA_OK", 1: "AA_ERR_INVALID_ARG", 2: "AA_ERR_UNSUPPORTED", 3: "AA_E
 
 # every symbol include/anchorattn.h declares
 EXPORTS = ["aa_plan", "aa_plan_destroy", "aa_plan_metadata", "aa_plan_stats", "aa_plan_work",
-           "aa_rope_apply", "aa_fwd", "aa_bwd_workspace_bytes", "aa_bwd", "aa_check_device_error",
+           "aa_rope_apply", "aa_fwd", "aa_bwd_workspace_bytes", "aa_bwd", "aa_bwd_static_workspace", "aa_check_device_error",
            "aa_set_wait_limit", "aa_set_bwd_timing_events", "aa_status_string", "aa_last_error"]
 
 
@@ -63,6 +63,7 @@ def lib():
             "aa_fwd": ([vp, vp, vp, vp, vp, vp, vp], ctypes.c_int),
             "aa_bwd_workspace_bytes": ([vp], ctypes.c_size_t),
             "aa_bwd": ([vp] + [vp] * 9 + [vp, ctypes.c_size_t, vp], ctypes.c_int),
+            "aa_bwd_static_workspace": ([vp] + [vp] * 9 + [vp], ctypes.c_int),
             "aa_check_device_error": ([vp, vp], ctypes.c_int),
             "aa_set_wait_limit": ([vp, ctypes.c_uint64], ctypes.c_int),
             "aa_set_bwd_timing_events": ([vp, vp, vp], ctypes.c_int),
@@ -199,4 +200,16 @@ class Plan:
         _check(lib().aa_bwd(self._h, _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout),
                             _ptr(dq), _ptr(dk), _ptr(dv), _ptr(ws), ctypes.c_size_t(ws.numel()),
                             _stream(stream)))
+        return dq, dk, dv
+
+    def bwd_static_workspace(self, q, k, v, o, lse, dout, dq=None, dk=None, dv=None, stream=None):
+        """aa_bwd_static_workspace: the backward pass with the library's static
+        64 MiB scratch instead of a caller-provided workspace (for callers that
+        must not allocate device memory; outputs may still come from torch)."""
+        import torch
+        dq = torch.empty_like(q) if dq is None else dq
+        dk = torch.empty_like(k) if dk is None else dk
+        dv = torch.empty_like(v) if dv is None else dv
+        _check(lib().aa_bwd_static_workspace(self._h, _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse),
+                                             _ptr(dout), _ptr(dq), _ptr(dk), _ptr(dv), _stream(stream)))
         return dq, dk, dv

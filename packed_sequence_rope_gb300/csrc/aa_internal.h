@@ -59,4 +59,8 @@ aa_status fail(aa_status s, const std::string& msg);
 aa_status cuda_fail(cudaError_t e, const char* what);
 bool aligned16(const void* p);
 aa_status check_compute_plan(const aa_plan_s* p);
+// Launch the backward kernels with an already-validated workspace pointer.
+aa_status launch_bwd_with_workspace(aa_plan_s* p, const void* q, const void* k, const void* v, const void* o,
+                                    const float* lse, const void* dout, void* dq, void* dk, void* dv,
+                                    void* workspace, cudaStream_t s);
 }  // namespace aa

@@ -615,6 +615,14 @@ aa_status launch_bwd(aa_plan_s* p, const void* q, const void* k, const void* v, 
 }
 
 }  // namespace
+
+aa_status launch_bwd_with_workspace(aa_plan_s* p, const void* q, const void* k, const void* v, const void* o,
+                                    const float* lse, const void* dout, void* dq, void* dk, void* dv,
+                                    void* workspace, cudaStream_t s) {
+  return p->D == 128 ? launch_bwd<128>(p, q, k, v, o, lse, dout, dq, dk, dv, workspace, s)
+                     : launch_bwd<64>(p, q, k, v, o, lse, dout, dq, dk, dv, workspace, s);
+}
+
 }  // namespace aa
 
 using namespace aa;
