@@ -27,8 +27,9 @@ struct DevicePlan {
   int32_t* key_hi = nullptr;   // [T] last query row that sees key j in the tile path
   WorkItem* fwd_items = nullptr;
   WorkItem* bwd_items = nullptr;
+  int32_t* qtile_klo = nullptr;  // [n_tiles] first live key tile of each query tile
   float2* rope_hi = nullptr;   // [n_hi][D/2]  cos/sin((128*h) * theta_p)
-  float2* rope_lo = nullptr;   // [128][D/2]   cos/sin(l * theta_p)
+  float2* rope_lo = nullptr;   // [D/2][128]   cos/sin(l * theta_p), p-major
   int32_t* err = nullptr;      // device error word (0 = ok)
 };
 
@@ -42,7 +43,8 @@ struct aa_plan_s {
   bool host_only = false;
   std::vector<int32_t> cu;      // document boundaries (empty in CAUSAL mode)
   std::vector<int32_t> doc_id, pos_id, row_lo, key_hi;
-  std::vector<aa::WorkItem> fwd_items, bwd_items;
+  std::vector<aa::WorkItem> fwd_items, bwd_items;  // fwd: one item per (query-tile pair, head)
+  std::vector<int32_t> qtile_klo;
   std::vector<float2> rope_hi, rope_lo;
   int32_t n_hi = 0;
   int64_t unmasked_pairs = 0, live_tiles = 0, causal_tiles = 0;

@@ -8,34 +8,46 @@
 //   LSE_i = ln sum_{j visible} exp(scale * (R_i q_i).(R_j k_j))
 // with the visible set {0} U [row_lo_i, i] (ANCHOR) or [row_lo_i, i].
 //
-// How: one CTA per (query tile of 128 rows, head) work item, items in
-// longest-first order. Q and K/V tiles arrive by TMA (128-byte swizzle), are
-// rotated in shared memory in fp32 and rounded to bf16 (RoPE fused into the
-// tile load), S = Q~ K~^T and O += P V run on the tcgen05 tensor cores with
-// fp32 accumulators in TMEM, and the online softmax runs one query row per
-// thread straight from TMEM. Only the key tiles that overlap the row
-// intervals of the tile are visited; the anchor column is folded into the
-// softmax's starting state on the CUDA cores (m = s_i0, l = 1, weight of v_0),
-// so fully cross-document tiles are never touched.
+// How. One CTA per (pair of 128-row query tiles, head), longest work first.
+// Warp roles (512 threads):
+//   warp 0      TMA producer: Q0/Q1 once, then K/V tiles through a 2-stage ring
+//   warp 1      TMEM owner and MMA issuer (one thread)
+//   warps 4-7   softmax for query tile 0 (thread = query row = TMEM lane)
+//   warps 8-11  softmax for query tile 1
+//   warps 12-15 RoPE: rotate Q0/Q1 once and every K tile once (fp32, rounded
+//               to bf16 in place), shared by both query tiles
+// Tensor-memory columns: S0 [0,128) S1 [128,256) O0, O1 (D columns each). The
+// softmax writes P as packed bf16 over the first 64 columns of its S, and the
+// PV product reads it straight from TMEM (tcgen05.mma with A in TMEM).
+// The MMA issue order S0(j), PV1(j-1), S1(j), PV0(j) lets each softmax group
+// work while the tensor core runs the other group's products. Only the key
+// tiles that overlap a query tile's row intervals are visited; the anchor
+// column enters as the online softmax's start state (m = s_i0, l = 1) and its
+// value row is added in the epilogue.
 #include "kcommon.cuh"
 
 namespace aa {
 namespace {
 
 constexpr float kLog2e = 1.4426950408889634f;
-constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale O only when the max grows by > 2^8
+constexpr float kRescaleThreshold = 8.0f;  // log2 units: O is rescaled only when the max grows by > 2^8
+constexpr uint64_t kDrainLimitNs = 1000000000ull;
+constexpr int kStages = 2;
+constexpr int kThreads = 512;
 
 template <int HD>
 struct FwdSmem {
-  static constexpr int kBlocks = HD / 64;
-  alignas(1024) uint8_t q[kBlocks][16384];
-  alignas(1024) uint8_t k[kBlocks][16384];
-  alignas(1024) uint8_t v[kBlocks][16384];
-  alignas(1024) uint8_t p[2][16384];  // P tile: 128 query rows x 128 keys, bf16
-  float k0[HD];                       // rotated anchor key (bf16-rounded)
-  float v0[HD];                       // anchor value
-  uint64_t bar_q, bar_kv, bar_mma;
+  static constexpr int kB = HD / 64;
+  alignas(1024) uint8_t q[2][kB][16384];
+  alignas(1024) uint8_t k[kStages][kB][16384];
+  alignas(1024) uint8_t v[kStages][kB][16384];
+  float k0[HD];  // rotated anchor key (bf16-rounded)
+  float v0[HD];  // anchor value
+  uint64_t q_full, q_ready;
+  uint64_t kv_full[kStages], k_ready[kStages], kv_empty[kStages];
+  uint64_t s_full[2], p_full[2], o_full, drain;
   uint32_t tmem_base;
+  int abort_flag;
 };
 
 struct FwdParams {
@@ -45,259 +57,319 @@ struct FwdParams {
   float* lse;
   const int32_t* pos_id;
   const int32_t* row_lo;
+  const int32_t* qtile_klo;
   const WorkItem* items;
   const float2* rope_hi;
   const float2* rope_lo;
   int32_t* err;
   uint64_t wait_limit_ns;
-  int T, Hq, Hkv, group, layout, anchor;
+  int T, Hq, Hkv, group, layout, anchor, n_tiles;
   float scale;
 };
 
-constexpr uint64_t kDrainLimitNs = 1000000000ull;
+// Bounded wait that also gives up as soon as another role of the CTA aborted.
+__device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, const FwdParams& P,
+                                              volatile int* abort_flag, int site) {
+  if (ptx::mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = ptx::global_timer_ns();
+  while (true) {
+    if (ptx::mbar_try_wait(bar, parity)) return true;
+    if (*abort_flag) return false;
+    if (ptx::global_timer_ns() - t0 >= P.wait_limit_ns) {
+      atomicCAS(P.err, 0, site);
+      *abort_flag = 1;
+      return false;
+    }
+  }
+}
 
 template <int HD>
-__global__ void __launch_bounds__(128, 1)
+__global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const FwdParams P) {
   extern __shared__ uint8_t smem_raw[];
   FwdSmem<HD>& sm = *reinterpret_cast<FwdSmem<HD>*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                     ~uintptr_t(1023));
-  constexpr int kTmemCols = 256;  // S: 128 columns, O: HD columns
   constexpr uint32_t kTileBytes = 128 * HD * 2;
-  const int tid = threadIdx.x, warp = tid >> 5;
+  constexpr int kTmemCols = 512;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const WorkItem item = P.items[blockIdx.x];
-  const int qt = item.tile, h = item.head, g = h / P.group;
-  const int row0 = qt * kTile;
+  const int h = item.head, g = h / P.group;
+  const int qt0 = 2 * item.tile;
+  const bool has1 = qt0 + 1 < P.n_tiles;
+  // key-tile range of each query tile (empty for a missing second tile)
+  const int lo0 = __ldg(P.qtile_klo + qt0), hi0 = qt0;
+  const int lo1 = has1 ? __ldg(P.qtile_klo + qt0 + 1) : 1, hi1 = has1 ? qt0 + 1 : 0;
+  const int kt_lo = item.lo, kt_hi = item.hi;
+  volatile int* abort_flag = &sm.abort_flag;
 
   if (tid == 0) {
     ptx::tma_prefetch_desc(&tmQ);
     ptx::tma_prefetch_desc(&tmK);
     ptx::tma_prefetch_desc(&tmV);
-    ptx::mbar_init(&sm.bar_q, 1);
-    ptx::mbar_init(&sm.bar_kv, 1);
-    ptx::mbar_init(&sm.bar_mma, 1);
+    ptx::mbar_init(&sm.q_full, 1);
+    ptx::mbar_init(&sm.q_ready, 128);
+    for (int s = 0; s < kStages; ++s) {
+      ptx::mbar_init(&sm.kv_full[s], 1);
+      ptx::mbar_init(&sm.k_ready[s], 128);
+      ptx::mbar_init(&sm.kv_empty[s], 1);
+    }
+    for (int t = 0; t < 2; ++t) {
+      ptx::mbar_init(&sm.s_full[t], 1);
+      ptx::mbar_init(&sm.p_full[t], 128);
+    }
+    ptx::mbar_init(&sm.o_full, 1);
+    ptx::mbar_init(&sm.drain, 1);
+    sm.abort_flag = 0;
     ptx::fence_mbar_init();
   }
-  if (warp == 0) ptx::tmem_alloc(&sm.tmem_base, kTmemCols);
+  if (warp == 1) ptx::tmem_alloc(&sm.tmem_base, kTmemCols);
   ptx::tc_fence_before();
   __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem = sm.tmem_base;
-  const uint32_t tmem_s = tmem, tmem_o = tmem + 128;
-  const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
 
-  // thread 0 tracks what is in flight so an aborted CTA can drain it
-  bool kv_pending = false, mma_pending = false, q_pending = false;
-  uint32_t kv_phase = 0, mma_phase = 0;
-
-  if (tid == 0) {
-    ptx::mbar_arrive_expect_tx(&sm.bar_q, kTileBytes);
-    for (int b = 0; b < HD / 64; ++b) ptx::tma_load_3d(sm.q[b], &tmQ, &sm.bar_q, b * 64, h, row0);
-    ptx::mbar_arrive_expect_tx(&sm.bar_kv, 2 * kTileBytes);
-    for (int b = 0; b < HD / 64; ++b) {
-      ptx::tma_load_3d(sm.k[b], &tmK, &sm.bar_kv, b * 64, g, item.lo * kTile);
-      ptx::tma_load_3d(sm.v[b], &tmV, &sm.bar_kv, b * 64, g, item.lo * kTile);
-    }
-    q_pending = kv_pending = true;
-  }
-
-  // anchor key (rotated like any key, rounded to bf16) and value
-  if (P.anchor) {
-    const int pos0 = __ldg(P.pos_id);
-    const __nv_bfloat16* k0 = P.k + (size_t)g * HD;
-    const __nv_bfloat16* v0 = P.v + (size_t)g * HD;
-    for (int c = tid; c < HD; c += 128) sm.v0[c] = __bfloat162float(v0[c]);
-    if (tid < HD / 2) {
-      int ia, ib;
-      if (P.layout == 1) { ia = tid; ib = tid + HD / 2; } else { ia = 2 * tid; ib = 2 * tid + 1; }
-      float x = __bfloat162float(k0[ia]), y = __bfloat162float(k0[ib]);
-      if (P.layout != 2) {
-        const float2 cs = rope_cs(P.rope_hi, P.rope_lo, pos0, tid, HD / 2);
-        rope_pair(x, y, cs.x, cs.y);
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      ptx::mbar_arrive_expect_tx(&sm.q_full, (has1 ? 2 : 1) * kTileBytes);
+      for (int b = 0; b < HD / 64; ++b) {
+        ptx::tma_load_3d(sm.q[0][b], &tmQ, &sm.q_full, b * 64, h, qt0 * kTile);
+        if (has1) ptx::tma_load_3d(sm.q[1][b], &tmQ, &sm.q_full, b * 64, h, (qt0 + 1) * kTile);
       }
-      sm.k0[ia] = __bfloat162float(__float2bfloat16_rn(x));
-      sm.k0[ib] = __bfloat162float(__float2bfloat16_rn(y));
+      int n_issued = 0;
+      bool ok = true;
+      for (int kt = kt_lo; kt <= kt_hi && ok; ++kt, ++n_issued) {
+        const int s = n_issued % kStages;
+        if (n_issued >= kStages) ok = wait_or_abort(&sm.kv_empty[s], ((n_issued / kStages) - 1) & 1, P, abort_flag, 301);
+        if (!ok) break;
+        ptx::mbar_arrive_expect_tx(&sm.kv_full[s], 2 * kTileBytes);
+        for (int b = 0; b < HD / 64; ++b) {
+          ptx::tma_load_3d(sm.k[s][b], &tmK, &sm.kv_full[s], b * 64, g, kt * kTile);
+          ptx::tma_load_3d(sm.v[s][b], &tmV, &sm.kv_full[s], b * 64, g, kt * kTile);
+        }
+      }
+      // let every issued copy land before the CTA can exit
+      ptx::mbar_wait(&sm.q_full, 0, kDrainLimitNs, P.err, 309);
+      for (int u = (n_issued > kStages ? n_issued - kStages : 0); u < n_issued; ++u)
+        ptx::mbar_wait(&sm.kv_full[u % kStages], (u / kStages) & 1, kDrainLimitNs, P.err, 309);
     }
-  }
-
-  const int r = tid;  // this thread's query row within the tile == TMEM lane
-  const int i = row0 + r;
-  const bool row_valid = i < P.T;
-  const int lo = row_valid ? __ldg(P.row_lo + i) : 1;
-  const int hi = row_valid ? i : 0;
-  const float sl2 = P.scale * kLog2e;
-
-  bool ok = ptx::mbar_wait(&sm.bar_q, 0, P.wait_limit_ns, P.err, 101);
-  if (__syncthreads_or(!ok)) goto abort;
-  if (tid == 0) q_pending = false;
-  if (row_valid) rope_row_smem<HD>(sm.q[0], r, __ldg(P.pos_id + i), P.layout, false, P.rope_hi, P.rope_lo);
-  ptx::fence_proxy_async_smem();
-  __syncthreads();
-
-  {
-    // online-softmax state in log2 units
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc_s = ptx::idesc_bf16_f32(128, 128, 0, 0);
+      constexpr uint32_t idesc_pv = ptx::idesc_bf16_f32(128, HD, 0, 1);
+      const uint32_t t_s[2] = {tmem, tmem + 128};
+      const uint32_t t_o[2] = {tmem + 256, tmem + 256 + HD};
+      uint32_t ph_p[2] = {0, 0};
+      bool first_pv[2] = {true, true};
+      auto issue_s = [&](int t, int s) {
+        for (int kk = 0; kk < HD / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+          ptx::mma_bf16(t_s[t], ptx::smem_desc_sw128(ptx::smem_u32(sm.q[t][0]) + off, 16, 1024),
+                        ptx::smem_desc_sw128(ptx::smem_u32(sm.k[s][0]) + off, 16, 1024), idesc_s, kk > 0);
+        }
+        ptx::mma_commit(&sm.s_full[t]);
+      };
+      auto issue_pv = [&](int t, int s) -> bool {
+        if (!wait_or_abort(&sm.p_full[t], ph_p[t], P, abort_flag, 311)) return false;
+        ph_p[t] ^= 1;
+        ptx::tc_fence_after();
+        for (int kk = 0; kk < 8; ++kk)
+          ptx::mma_bf16_ts(t_o[t], t_s[t] + kk * 8,
+                           ptx::smem_desc_sw128(ptx::smem_u32(sm.v[s][0]) + kk * 2048, 16384, 1024), idesc_pv,
+                           (!first_pv[t] || kk > 0) ? 1u : 0u);
+        first_pv[t] = false;
+        return true;
+      };
+      bool ok = wait_or_abort(&sm.q_ready, 0, P, abort_flag, 312);
+      int pend1 = -1;  // stage whose PV1 is still to be issued
+      int it = 0;
+      for (int kt = kt_lo; kt <= kt_hi && ok; ++kt, ++it) {
+        const int s = it % kStages;
+        ok = wait_or_abort(&sm.k_ready[s], (it / kStages) & 1, P, abort_flag, 313);
+        if (!ok) break;
+        ptx::tc_fence_after();
+        const bool in0 = kt >= lo0 && kt <= hi0, in1 = kt >= lo1 && kt <= hi1;
+        if (in0) issue_s(0, s);
+        if (pend1 >= 0) {
+          ok = issue_pv(1, pend1);
+          if (!ok) break;
+          pend1 = -1;
+        }
+        if (it > 0) ptx::mma_commit(&sm.kv_empty[(it - 1) % kStages]);
+        if (in1) issue_s(1, s);
+        if (in0) {
+          ok = issue_pv(0, s);
+          if (!ok) break;
+        }
+        if (in1) pend1 = s;
+      }
+      if (ok && pend1 >= 0) ok = issue_pv(1, pend1);
+      if (ok) {
+        ptx::mma_commit(&sm.kv_empty[(it - 1) % kStages]);
+        ptx::mma_commit(&sm.o_full);
+      }
+      // every issued MMA must finish before TMEM is released
+      ptx::mma_commit(&sm.drain);
+      ptx::mbar_wait(&sm.drain, 0, kDrainLimitNs, P.err, 319);
+    }
+  } else if (warp >= 4 && warp < 12) {
+    // ------------------------------------------------------------ softmax
+    const int t = (warp - 4) >> 2;
+    const int r = tid & 127;
+    const int lo_t = t ? lo1 : lo0, hi_t = t ? hi1 : hi0;
+    const bool tile_exists = t == 0 || has1;
+    const int i = (qt0 + t) * kTile + r;
+    const bool row_valid = tile_exists && i < P.T;
+    const int lo = row_valid ? __ldg(P.row_lo + i) : 1;
+    const int hi = row_valid ? i : 0;
+    const float sl2 = P.scale * kLog2e;
+    const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
+    const uint32_t t_s = tmem + 128 * t + lane_off, t_o = tmem + 256 + HD * t + lane_off;
     float m = -INFINITY, l = 0.f, s0 = 0.f;
-    if (P.anchor) {
+    bool ok = tile_exists;
+    if (ok) ok = wait_or_abort(&sm.q_ready, 0, P, abort_flag, 321);
+    if (ok && P.anchor) {
       float acc = 0.f;
-      for (int c = 0; c < HD; ++c) acc = fmaf(tile_elem(sm.q[0], r, c), sm.k0[c], acc);
+      for (int c = 0; c < HD; ++c) acc = fmaf(tile_elem(sm.q[t][0], r, c), sm.k0[c], acc);
       s0 = acc * sl2;
       m = s0;
       l = 1.f;
     }
-    constexpr uint32_t idesc_s = ptx::idesc_bf16_f32(128, 128, 0, 0);
-    constexpr uint32_t idesc_pv = ptx::idesc_bf16_f32(128, HD, 0, 1);
-    const int n_iter = item.hi - item.lo + 1;
-    for (int it = 0; it < n_iter; ++it) {
-      const int kt = item.lo + it;
-      ok = ptx::mbar_wait(&sm.bar_kv, kv_phase, P.wait_limit_ns, P.err, 102);
-      if (__syncthreads_or(!ok)) goto abort;
-      if (tid == 0) kv_pending = false;
-      kv_phase ^= 1;
-      {
-        const int j = kt * kTile + r;
-        if (j < P.T) rope_row_smem<HD>(sm.k[0], r, __ldg(P.pos_id + j), P.layout, false, P.rope_hi, P.rope_lo);
-      }
-      ptx::fence_proxy_async_smem();
-      __syncthreads();
-      if (tid == 0) {
-        ptx::tc_fence_after();
-#pragma unroll
-        for (int kk = 0; kk < HD / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-          const uint64_t a = ptx::smem_desc_sw128(ptx::smem_u32(sm.q[0]) + off, 16, 1024);
-          const uint64_t b = ptx::smem_desc_sw128(ptx::smem_u32(sm.k[0]) + off, 16, 1024);
-          ptx::mma_bf16(tmem_s, a, b, idesc_s, kk > 0);
-        }
-        ptx::mma_commit(&sm.bar_mma);
-        mma_pending = true;
-      }
-      ok = ptx::mbar_wait(&sm.bar_mma, mma_phase, P.wait_limit_ns, P.err, 103);
-      if (__syncthreads_or(!ok)) goto abort;
-      if (tid == 0) mma_pending = false;
-      mma_phase ^= 1;
+    uint32_t ph_s = 0;
+    for (int kt = lo_t; kt <= hi_t && ok; ++kt) {
+      ok = wait_or_abort(&sm.s_full[t], ph_s, P, abort_flag, 322);
+      if (!ok) break;
+      ph_s ^= 1;
       ptx::tc_fence_after();
-
-      // ---- softmax on this thread's row
-      float sv[128];
-#pragma unroll
-      for (int c = 0; c < 4; ++c) ptx::tmem_ld32(tmem_s + lane_off + c * 32, sv + c * 32);
-      ptx::tmem_wait_ld();
       const int j0 = kt * kTile;
+      // pass 1: row max of the visible scaled logits
       float mt = -INFINITY;
 #pragma unroll
-      for (int c = 0; c < 128; ++c) {
-        const int j = j0 + c;
-        const bool vis = (j >= lo) && (j <= hi);
-        sv[c] = vis ? sv[c] * sl2 : -INFINITY;
-        mt = fmaxf(mt, sv[c]);
+      for (int c = 0; c < 4; ++c) {
+        float sv[32];
+        ptx::tmem_ld32(t_s + c * 32, sv);
+        ptx::tmem_wait_ld();
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+          const int j = j0 + c * 32 + e;
+          if (j >= lo && j <= hi) mt = fmaxf(mt, sv[e] * sl2);
+        }
       }
-      // TMEM loads/stores are warp-collective, so the rescale decision is
-      // taken per warp: if any row of the warp needs it, every row of the
-      // warp moves to max(m, mt) (a factor of 1 where the max did not grow)
+      // TMEM access is warp-collective, so a rescale of O is decided per warp
       const bool need = (mt > m + kRescaleThreshold) || (m == -INFINITY && mt > -INFINITY);
       if (__any_sync(0xffffffffu, need)) {
         const float mn = fmaxf(m, mt);
         const float f = (m == -INFINITY) ? 0.f : exp2f(m - mn);
         l *= f;
-        if (it > 0) {
-#pragma unroll
+        if (kt > lo_t) {  // O holds earlier tiles: S(kt) done implies their PV is done
+#pragma unroll 1
           for (int c = 0; c < HD / 32; ++c) {
             float ov[32];
-            ptx::tmem_ld32(tmem_o + lane_off + c * 32, ov);
+            ptx::tmem_ld32(t_o + c * 32, ov);
             ptx::tmem_wait_ld();
 #pragma unroll
             for (int e = 0; e < 32; ++e) ov[e] *= f;
-            ptx::tmem_st32(tmem_o + lane_off + c * 32, ov);
+            ptx::tmem_st32(t_o + c * 32, ov);
           }
-          ptx::tmem_wait_st();
         }
         m = mn;
       }
+      // pass 2: P = exp2(s - m) as packed bf16 over the first 64 columns of S
       float rs = 0.f;
+      const float mm = (m == -INFINITY) ? 0.f : m;
 #pragma unroll
-      for (int c8 = 0; c8 < 16; ++c8) {
-        uint32_t w[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float p0 = (m == -INFINITY) ? 0.f : exp2f(sv[c8 * 8 + 2 * e] - m);
-          const float p1 = (m == -INFINITY) ? 0.f : exp2f(sv[c8 * 8 + 2 * e + 1] - m);
-          rs += p0 + p1;
-          w[e] = ptx::pack_bf16x2(p0, p1);
-        }
-        *reinterpret_cast<uint4*>(sm.p[c8 >> 3] + sw128_chunk(r, c8 & 7)) = make_uint4(w[0], w[1], w[2], w[3]);
-      }
-      l += rs;
-      ptx::fence_proxy_async_smem();
-      ptx::tc_fence_before();
-      __syncthreads();
-      if (tid == 0) {
-        ptx::tc_fence_after();
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          const uint64_t a = ptx::smem_desc_sw128(ptx::smem_u32(sm.p[0]) + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024);
-          const uint64_t b = ptx::smem_desc_sw128(ptx::smem_u32(sm.v[0]) + kk * 2048, 16384, 1024);
-          ptx::mma_bf16(tmem_o, a, b, idesc_pv, (it > 0 || kk > 0) ? 1u : 0u);
-        }
-        ptx::mma_commit(&sm.bar_mma);
-        mma_pending = true;
-      }
-      ok = ptx::mbar_wait(&sm.bar_mma, mma_phase, P.wait_limit_ns, P.err, 104);
-      if (__syncthreads_or(!ok)) goto abort;
-      mma_phase ^= 1;
-      if (tid == 0) {
-        mma_pending = false;
-        if (it + 1 < n_iter) {
-          ptx::mbar_arrive_expect_tx(&sm.bar_kv, 2 * kTileBytes);
-          for (int b = 0; b < HD / 64; ++b) {
-            ptx::tma_load_3d(sm.k[b], &tmK, &sm.bar_kv, b * 64, g, (kt + 1) * kTile);
-            ptx::tma_load_3d(sm.v[b], &tmV, &sm.bar_kv, b * 64, g, (kt + 1) * kTile);
-          }
-          kv_pending = true;
-        }
-      }
-      ptx::tc_fence_after();
-    }
-
-    // ---- epilogue: O = (O_tiles + w0 * v0) / l, LSE = ln(l) + m ln 2
-    const float w0 = P.anchor ? exp2f(s0 - m) : 0.f;
-    const float inv_l = 1.f / l;
-    __nv_bfloat16* orow = P.o + ((size_t)(row_valid ? i : 0) * P.Hq + h) * HD;
-#pragma unroll
-    for (int c = 0; c < HD / 32; ++c) {
-      float ov[32];
-      ptx::tmem_ld32(tmem_o + lane_off + c * 32, ov);  // warp-collective: every lane loads
-      ptx::tmem_wait_ld();
-      if (row_valid) {
+      for (int c = 0; c < 4; ++c) {
+        float sv[32];
+        ptx::tmem_ld32(t_s + c * 32, sv);
+        ptx::tmem_wait_ld();
         uint32_t w[16];
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
-          const float a = (ov[2 * e] + w0 * sm.v0[c * 32 + 2 * e]) * inv_l;
-          const float b = (ov[2 * e + 1] + w0 * sm.v0[c * 32 + 2 * e + 1]) * inv_l;
-          w[e] = ptx::pack_bf16x2(a, b);
+          const int j = j0 + c * 32 + 2 * e;
+          const float p0 = (j >= lo && j <= hi) ? exp2f(fmaf(sv[2 * e], sl2, -mm)) : 0.f;
+          const float p1 = (j + 1 >= lo && j + 1 <= hi) ? exp2f(fmaf(sv[2 * e + 1], sl2, -mm)) : 0.f;
+          rs += p0 + p1;
+          w[e] = ptx::pack_bf16x2(p0, p1);
         }
-        uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
-#pragma unroll
-        for (int e = 0; e < 4; ++e) dst[e] = make_uint4(w[4 * e], w[4 * e + 1], w[4 * e + 2], w[4 * e + 3]);
+        ptx::tmem_st16(t_s + c * 16, w);
       }
+      l += rs;
+      ptx::tmem_wait_st();
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(&sm.p_full[t]);
     }
-    if (row_valid) P.lse[(size_t)h * P.T + i] = (m + log2f(l)) * 0.69314718055994531f;
+    if (ok) ok = wait_or_abort(&sm.o_full, 0, P, abort_flag, 323);
+    if (ok) {
+      ptx::tc_fence_after();
+      const float w0 = P.anchor ? exp2f(s0 - m) : 0.f;
+      const float inv_l = 1.f / l;
+      __nv_bfloat16* orow = P.o + ((size_t)(row_valid ? i : 0) * P.Hq + h) * HD;
+#pragma unroll 1
+      for (int c = 0; c < HD / 32; ++c) {
+        float ov[32];
+        ptx::tmem_ld32(t_o + c * 32, ov);
+        ptx::tmem_wait_ld();
+        if (row_valid) {
+          uint32_t w[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            const float a = (ov[2 * e] + w0 * sm.v0[c * 32 + 2 * e]) * inv_l;
+            const float b = (ov[2 * e + 1] + w0 * sm.v0[c * 32 + 2 * e + 1]) * inv_l;
+            w[e] = ptx::pack_bf16x2(a, b);
+          }
+          uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) dst[e] = make_uint4(w[4 * e], w[4 * e + 1], w[4 * e + 2], w[4 * e + 3]);
+        }
+      }
+      if (row_valid) P.lse[(size_t)h * P.T + i] = (m + log2f(l)) * 0.69314718055994531f;
+    }
+  } else if (warp >= 12) {
+    // ------------------------------------------------------------ RoPE
+    const int r = tid & 127;
+    if (P.anchor && r < HD / 2) {
+      const int pos0 = __ldg(P.pos_id);
+      const __nv_bfloat16* k0 = P.k + (size_t)g * HD;
+      const __nv_bfloat16* v0 = P.v + (size_t)g * HD;
+      int ia, ib;
+      if (P.layout == 1) { ia = r; ib = r + HD / 2; } else { ia = 2 * r; ib = 2 * r + 1; }
+      float x = __bfloat162float(k0[ia]), y = __bfloat162float(k0[ib]);
+      if (P.layout != 2) {
+        const float2 cs = rope_cs(P.rope_hi, P.rope_lo, pos0, r, HD / 2);
+        rope_pair(x, y, cs.x, cs.y);
+      }
+      sm.k0[ia] = __bfloat162float(__float2bfloat16_rn(x));
+      sm.k0[ib] = __bfloat162float(__float2bfloat16_rn(y));
+      sm.v0[ia] = __bfloat162float(v0[ia]);
+      sm.v0[ib] = __bfloat162float(v0[ib]);
+    }
+    bool ok = wait_or_abort(&sm.q_full, 0, P, abort_flag, 331);
+    if (ok) {
+      for (int t = 0; t < (has1 ? 2 : 1); ++t) {
+        const int i = (qt0 + t) * kTile + r;
+        if (i < P.T) rope_row_smem<HD>(sm.q[t][0], r, __ldg(P.pos_id + i), P.layout, false, P.rope_hi, P.rope_lo);
+      }
+      // q_ready also publishes the anchor key/value rows written above
+      ptx::fence_proxy_async_smem();
+      ptx::mbar_arrive(&sm.q_ready);
+    }
+    int it = 0;
+    for (int kt = kt_lo; kt <= kt_hi && ok; ++kt, ++it) {
+      const int s = it % kStages;
+      ok = wait_or_abort(&sm.kv_full[s], (it / kStages) & 1, P, abort_flag, 332);
+      if (!ok) break;
+      const int j = kt * kTile + r;
+      if (j < P.T) rope_row_smem<HD>(sm.k[s][0], r, __ldg(P.pos_id + j), P.layout, false, P.rope_hi, P.rope_lo);
+      ptx::fence_proxy_async_smem();
+      ptx::mbar_arrive(&sm.k_ready[s]);
+    }
   }
-  ptx::tc_fence_before();
-  __syncthreads();
-  if (warp == 0) ptx::tmem_dealloc(tmem, kTmemCols);
-  return;
 
-abort:
-  // a bounded wait ran out: let in-flight copies and MMAs land, free TMEM, return
-  if (tid == 0) {
-    if (q_pending) ptx::mbar_wait(&sm.bar_q, 0, kDrainLimitNs, P.err, 199);
-    if (kv_pending) ptx::mbar_wait(&sm.bar_kv, kv_phase, kDrainLimitNs, P.err, 199);
-    if (mma_pending) ptx::mbar_wait(&sm.bar_mma, mma_phase, kDrainLimitNs, P.err, 199);
-  }
   ptx::tc_fence_before();
   __syncthreads();
-  if (warp == 0) ptx::tmem_dealloc(tmem, kTmemCols);
+  if (warp == 1) ptx::tmem_dealloc(tmem, kTmemCols);
 }
 
 template <int HD>
@@ -315,6 +387,7 @@ aa_status launch_fwd(aa_plan_s* p, const void* q, const void* k, const void* v, 
   P.lse = lse;
   P.pos_id = p->dev.pos_id;
   P.row_lo = p->dev.row_lo;
+  P.qtile_klo = p->dev.qtile_klo;
   P.items = p->dev.fwd_items;
   P.rope_hi = p->dev.rope_hi;
   P.rope_lo = p->dev.rope_lo;
@@ -326,12 +399,13 @@ aa_status launch_fwd(aa_plan_s* p, const void* q, const void* k, const void* v, 
   P.group = p->group;
   P.layout = p->cfg.rope_layout;
   P.anchor = p->anchor ? 1 : 0;
+  P.n_tiles = p->n_tiles;
   P.scale = p->scale;
   const size_t smem = sizeof(FwdSmem<HD>) + 1024;
   cudaError_t e = cudaFuncSetAttribute(attn_fwd_kernel<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return cuda_fail(e, "attn_fwd_kernel smem attribute");
   const unsigned n_items = (unsigned)p->fwd_items.size();
-  attn_fwd_kernel<HD><<<n_items, 128, smem, s>>>(tq, tk, tv, P);
+  attn_fwd_kernel<HD><<<n_items, kThreads, smem, s>>>(tq, tk, tv, P);
   e = cudaGetLastError();
   return e == cudaSuccess ? AA_OK : cuda_fail(e, "attn_fwd_kernel launch");
 }

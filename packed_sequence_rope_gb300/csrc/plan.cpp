@@ -102,11 +102,14 @@ static void build_stats_and_work(aa_plan_s* p) {
     if (p->anchor && kt_lo > 0) live += 1;  // the anchor column's block
     p->live_tiles += live;
   }
+  // forward: one item per pair of query tiles (2a, 2a+1) and head, visiting
+  // the union of the two tiles' key ranges
+  p->qtile_klo.assign(nt, 0);
+  for (int a = 0; a < nt; ++a) p->qtile_klo[a] = q_ranges[a].lo;
   for (int h = 0; h < p->Hq; ++h)
-    for (int a = 0; a < nt; ++a) {
-      WorkItem w = q_ranges[a];
-      w.head = h;
-      p->fwd_items.push_back(w);
+    for (int a = 0; 2 * a < nt; ++a) {
+      const int t0 = 2 * a, t1 = std::min(nt - 1, 2 * a + 1);
+      p->fwd_items.push_back(WorkItem{a, h, std::min(q_ranges[t0].lo, q_ranges[t1].lo), t1});
     }
   for (int g = 0; g < p->Hkv; ++g)
     for (int b = 0; b < nt; ++b) {
@@ -126,14 +129,15 @@ static void build_stats_and_work(aa_plan_s* p) {
   std::stable_sort(p->fwd_items.begin(), p->fwd_items.end(), by_cost);
   std::stable_sort(p->bwd_items.begin(), p->bwd_items.end(), by_cost);
   p->fwd_tiles = 0;
-  for (auto& w : p->fwd_items) p->fwd_tiles += w.hi - w.lo + 1;
+  for (int a = 0; a < nt; ++a) p->fwd_tiles += (int64_t)(q_ranges[a].hi - q_ranges[a].lo + 1) * p->Hq;
   p->bwd_tiles = 0;
   for (auto& w : p->bwd_items) p->bwd_tiles += (int64_t)(w.hi - w.lo + 1) * p->group;
 }
 
 // Two-level cos/sin tables for Eq. 6: pos = 128*h + l, so
-// (cos, sin)(pos*theta) is the complex product of rope_hi[h] and rope_lo[l].
-// Entries are computed in fp64 and rounded once to fp32.
+// (cos, sin)(pos*theta_p) is the complex product of rope_hi[h][p] and
+// rope_lo[p][l]. Entries are computed in fp64 and rounded once to fp32.
+// rope_lo is p-major so that consecutive positions read consecutive entries.
 static void build_rope_tables(aa_plan_s* p) {
   const int half = p->D / 2;
   int max_pos = 0;
@@ -149,10 +153,10 @@ static void build_rope_tables(aa_plan_s* p) {
       const double ang = (double)h * kTile * theta[i];
       p->rope_hi[(size_t)h * half + i] = make_float2((float)std::cos(ang), (float)std::sin(ang));
     }
-  for (int l = 0; l < kTile; ++l)
-    for (int i = 0; i < half; ++i) {
+  for (int i = 0; i < half; ++i)
+    for (int l = 0; l < kTile; ++l) {
       const double ang = (double)l * theta[i];
-      p->rope_lo[(size_t)l * half + i] = make_float2((float)std::cos(ang), (float)std::sin(ang));
+      p->rope_lo[(size_t)i * kTile + l] = make_float2((float)std::cos(ang), (float)std::sin(ang));
     }
 }
 
@@ -174,7 +178,7 @@ static aa_status upload(T** dst, const std::vector<T>& src, cudaStream_t s, cons
 
 static void free_device(aa_plan_s* p) {
   DevicePlan& d = p->dev;
-  void* ptrs[] = {d.pos_id, d.row_lo, d.key_hi, d.fwd_items, d.bwd_items, d.rope_hi, d.rope_lo, d.err};
+  void* ptrs[] = {d.pos_id, d.row_lo, d.key_hi, d.fwd_items, d.bwd_items, d.qtile_klo, d.rope_hi, d.rope_lo, d.err};
   for (void* q : ptrs)
     if (q) cudaFree(q);
   d = DevicePlan{};
@@ -255,6 +259,7 @@ extern "C" aa_status aa_plan(const aa_config* cfg, const int32_t* cu_doclens_hos
       (st = upload(&d.key_hi, p->key_hi, s, "key_hi")) != AA_OK ||
       (st = upload(&d.fwd_items, p->fwd_items, s, "fwd work list")) != AA_OK ||
       (st = upload(&d.bwd_items, p->bwd_items, s, "bwd work list")) != AA_OK ||
+      (st = upload(&d.qtile_klo, p->qtile_klo, s, "query-tile key ranges")) != AA_OK ||
       (st = upload(&d.rope_hi, p->rope_hi, s, "rope table (hi)")) != AA_OK ||
       (st = upload(&d.rope_lo, p->rope_lo, s, "rope table (lo)")) != AA_OK ||
       (st = upload(&d.err, zero, s, "error word")) != AA_OK) {
