@@ -175,19 +175,32 @@ __global__ void __launch_bounds__(128) bwd_prep_kernel(const __nv_bfloat16* __re
 }
 
 // ---------------------------------------------------------------- 2. main
+// One CTA per (key tile, kv head), 512 threads:
+//   warp 0      TMA producer: K, V once; Q_i, dO_i through a 2-stage ring
+//   warp 1      TMEM owner and MMA issuer (one thread)
+//   warps 4-7   P/dS group (thread = key row = TMEM lane): P^T packed bf16 into
+//               TMEM for the dV product, dS^T bf16 into shared memory
+//   warps 8-11  dQ group (thread = query row): drains dQ~ from TMEM into the
+//               fp32 accumulator with vector atomics, concurrently with the
+//               next tile's products
+//   warps 12-15 RoPE: K once, every Q tile as it lands
+// TMEM columns: S^T [0,128) (P^T over [0,64)), dP^T [128,256) (dQ~ reuses
+// [128,128+D) once dS is formed), dV [256,256+D), dK~ [256+D,256+2D).
+constexpr int kBwdThreads = 512;
+
 template <int HD>
 struct BwdSmem {
-  static constexpr int kBlocks = HD / 64;
-  alignas(1024) uint8_t k[kBlocks][16384];
-  alignas(1024) uint8_t v[kBlocks][16384];
-  alignas(1024) uint8_t q[kBlocks][16384];
-  alignas(1024) uint8_t dout[kBlocks][16384];
-  alignas(1024) uint8_t pt[2][16384];   // P^T: 128 keys x 128 query rows
-  alignas(1024) uint8_t dst[2][16384];  // dS^T
-  float lse2[128];                      // LSE_i * log2(e) of the current query tile
-  float dsum[128];                      // D_i of the current query tile
-  uint64_t bar_kv, bar_q, bar_mma;
+  static constexpr int kB = HD / 64;
+  alignas(1024) uint8_t k[kB][16384];
+  alignas(1024) uint8_t v[kB][16384];
+  alignas(1024) uint8_t q[2][kB][16384];
+  alignas(1024) uint8_t dout[2][kB][16384];
+  alignas(1024) uint8_t dst[2][16384];  // dS^T: 128 keys x 128 query rows, bf16
+  uint64_t kv_full, k_ready;
+  uint64_t qd_full[2], q_ready[2], qd_empty[2];
+  uint64_t st_full, p_full, dq_full, dq_free, o_full, drain;
   uint32_t tmem_base;
+  int abort_flag;
 };
 
 struct BwdParams {
@@ -206,8 +219,29 @@ struct BwdParams {
   float scale;
 };
 
+__device__ __forceinline__ bool bwd_wait(uint64_t* bar, uint32_t parity, const BwdParams& P,
+                                         volatile int* abort_flag, int site) {
+  if (ptx::mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = ptx::global_timer_ns();
+  while (true) {
+    if (ptx::mbar_try_wait(bar, parity)) return true;
+    if (*abort_flag) return false;
+    if (ptx::global_timer_ns() - t0 >= P.wait_limit_ns) {
+      atomicCAS(P.err, 0, site);
+      *abort_flag = 1;
+      return false;
+    }
+  }
+}
+
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 template <int HD>
-__global__ void __launch_bounds__(128, 1)
+__global__ void __launch_bounds__(kBwdThreads, 1)
     attn_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
                     const BwdParams P) {
@@ -216,186 +250,265 @@ __global__ void __launch_bounds__(128, 1)
                                                     ~uintptr_t(1023));
   constexpr int kTmemCols = 512;
   constexpr uint32_t kTileBytes = 128 * HD * 2;
-  const int tid = threadIdx.x, warp = tid >> 5;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const WorkItem item = P.items[blockIdx.x];
   const int kt = item.tile, g = item.head;
   const int n_qt = item.hi - item.lo + 1;
   const int n_steps = n_qt * P.group;
+  volatile int* abort_flag = &sm.abort_flag;
 
   if (tid == 0) {
     ptx::tma_prefetch_desc(&tmQ);
     ptx::tma_prefetch_desc(&tmK);
     ptx::tma_prefetch_desc(&tmV);
     ptx::tma_prefetch_desc(&tmDO);
-    ptx::mbar_init(&sm.bar_kv, 1);
-    ptx::mbar_init(&sm.bar_q, 1);
-    ptx::mbar_init(&sm.bar_mma, 1);
+    ptx::mbar_init(&sm.kv_full, 1);
+    ptx::mbar_init(&sm.k_ready, 128);
+    for (int s = 0; s < 2; ++s) {
+      ptx::mbar_init(&sm.qd_full[s], 1);
+      ptx::mbar_init(&sm.q_ready[s], 128);
+      ptx::mbar_init(&sm.qd_empty[s], 1);
+    }
+    ptx::mbar_init(&sm.st_full, 1);
+    ptx::mbar_init(&sm.p_full, 128);
+    ptx::mbar_init(&sm.dq_full, 1);
+    ptx::mbar_init(&sm.dq_free, 128);
+    ptx::mbar_init(&sm.o_full, 1);
+    ptx::mbar_init(&sm.drain, 1);
+    sm.abort_flag = 0;
     ptx::fence_mbar_init();
   }
-  if (warp == 0) ptx::tmem_alloc(&sm.tmem_base, kTmemCols);
+  if (warp == 1) ptx::tmem_alloc(&sm.tmem_base, kTmemCols);
   ptx::tc_fence_before();
   __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem = sm.tmem_base;
-  const uint32_t t_s = tmem, t_dp = tmem + 128, t_dv = tmem + 256, t_dk = tmem + 256 + HD, t_dq = tmem;
-  const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+  const uint32_t t_s = tmem, t_dp = tmem + 128, t_dq = tmem + 128, t_dv = tmem + 256, t_dk = tmem + 256 + HD;
 
-  bool kv_pending = false, q_pending = false, mma_pending = false;
-  uint32_t q_phase = 0, mma_phase = 0;
+  auto step_head = [&](int step) { return g * P.group + step / n_qt; };
+  auto step_qt = [&](int step) { return item.lo + step % n_qt; };
 
-  auto issue_q = [&](int step) {
-    const int h = g * P.group + step / n_qt;
-    const int qt = item.lo + step % n_qt;
-    ptx::mbar_arrive_expect_tx(&sm.bar_q, 2 * kTileBytes);
-    for (int b = 0; b < HD / 64; ++b) {
-      ptx::tma_load_3d(sm.q[b], &tmQ, &sm.bar_q, b * 64, h, qt * kTile);
-      ptx::tma_load_3d(sm.dout[b], &tmDO, &sm.bar_q, b * 64, h, qt * kTile);
-    }
-  };
-
-  if (tid == 0) {
-    ptx::mbar_arrive_expect_tx(&sm.bar_kv, 2 * kTileBytes);
-    for (int b = 0; b < HD / 64; ++b) {
-      ptx::tma_load_3d(sm.k[b], &tmK, &sm.bar_kv, b * 64, g, kt * kTile);
-      ptx::tma_load_3d(sm.v[b], &tmV, &sm.bar_kv, b * 64, g, kt * kTile);
-    }
-    issue_q(0);
-    kv_pending = q_pending = true;
-  }
-
-  const int r = tid;
-  const int j = kt * kTile + r;  // this thread's key (TMEM lane of S^T, dP^T, dV, dK)
-  const bool key_valid = j < P.T;
-  const int jhi = key_valid ? __ldg(P.key_hi + j) : -1;  // rows [j, jhi] see key j
-  const float sl2 = P.scale * kLog2e;
-  constexpr uint32_t idesc_kt = ptx::idesc_bf16_f32(128, 128, 0, 0);   // S^T, dP^T
-  constexpr uint32_t idesc_kd = ptx::idesc_bf16_f32(128, HD, 0, 1);    // dV, dK
-  constexpr uint32_t idesc_qd = ptx::idesc_bf16_f32(128, HD, 1, 1);    // dQ
-
-  bool ok = ptx::mbar_wait(&sm.bar_kv, 0, P.wait_limit_ns, P.err, 201);
-  if (__syncthreads_or(!ok)) goto abort;
-  if (tid == 0) kv_pending = false;
-  if (key_valid) rope_row_smem<HD>(sm.k[0], r, __ldg(P.pos_id + j), P.layout, false, P.rope_hi, P.rope_lo);
-
-  for (int step = 0; step < n_steps; ++step) {
-    const int h = g * P.group + step / n_qt;
-    const int qt = item.lo + step % n_qt;
-    const int i0 = qt * kTile;
-    ok = ptx::mbar_wait(&sm.bar_q, q_phase, P.wait_limit_ns, P.err, 202);
-    if (__syncthreads_or(!ok)) goto abort;
-    if (tid == 0) q_pending = false;
-    q_phase ^= 1;
-    {
-      const int i = i0 + r;  // this thread rotates query row r
-      if (i < P.T) {
-        rope_row_smem<HD>(sm.q[0], r, __ldg(P.pos_id + i), P.layout, false, P.rope_hi, P.rope_lo);
-        sm.lse2[r] = __ldg(P.lse + (size_t)h * P.T + i) * kLog2e;
-        sm.dsum[r] = __ldg(P.ws.dsum + (size_t)h * P.T + i);
-      } else {
-        sm.lse2[r] = INFINITY;
-        sm.dsum[r] = 0.f;
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      ptx::mbar_arrive_expect_tx(&sm.kv_full, 2 * kTileBytes);
+      for (int b = 0; b < HD / 64; ++b) {
+        ptx::tma_load_3d(sm.k[b], &tmK, &sm.kv_full, b * 64, g, kt * kTile);
+        ptx::tma_load_3d(sm.v[b], &tmV, &sm.kv_full, b * 64, g, kt * kTile);
       }
-    }
-    ptx::fence_proxy_async_smem();
-    ptx::tc_fence_before();
-    __syncthreads();
-    if (tid == 0) {
-      ptx::tc_fence_after();
-#pragma unroll
-      for (int kk = 0; kk < HD / 16; ++kk) {
-        const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-        ptx::mma_bf16(t_s, ptx::smem_desc_sw128(ptx::smem_u32(sm.k[0]) + off, 16, 1024),
-                      ptx::smem_desc_sw128(ptx::smem_u32(sm.q[0]) + off, 16, 1024), idesc_kt, kk > 0);
-      }
-#pragma unroll
-      for (int kk = 0; kk < HD / 16; ++kk) {
-        const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-        ptx::mma_bf16(t_dp, ptx::smem_desc_sw128(ptx::smem_u32(sm.v[0]) + off, 16, 1024),
-                      ptx::smem_desc_sw128(ptx::smem_u32(sm.dout[0]) + off, 16, 1024), idesc_kt, kk > 0);
-      }
-      ptx::mma_commit(&sm.bar_mma);
-      mma_pending = true;
-    }
-    ok = ptx::mbar_wait(&sm.bar_mma, mma_phase, P.wait_limit_ns, P.err, 203);
-    if (__syncthreads_or(!ok)) goto abort;
-    if (tid == 0) mma_pending = false;
-    mma_phase ^= 1;
-    ptx::tc_fence_after();
-
-    // P^T and dS^T for this thread's key row, 32 query columns at a time
-#pragma unroll 1
-    for (int c = 0; c < 4; ++c) {
-      float sv[32], dpv[32];
-      ptx::tmem_ld32(t_s + lane_off + c * 32, sv);
-      ptx::tmem_ld32(t_dp + lane_off + c * 32, dpv);
-      ptx::tmem_wait_ld();
-      uint32_t pw[16], dw[16];
-#pragma unroll
-      for (int e = 0; e < 32; e += 2) {
-        float pp[2], dd[2];
-#pragma unroll
-        for (int u = 0; u < 2; ++u) {
-          const int col = c * 32 + e + u;
-          const int i = i0 + col;
-          const bool vis = (i >= j) && (i <= jhi);
-          const float p = vis ? exp2f(fmaf(sv[e + u], sl2, -sm.lse2[col])) : 0.f;
-          pp[u] = p;
-          dd[u] = p * (dpv[e + u] - sm.dsum[col]);
+      int n_issued = 0;
+      bool ok = true;
+      for (int step = 0; step < n_steps; ++step, ++n_issued) {
+        const int s = step & 1;
+        if (step >= 2) ok = bwd_wait(&sm.qd_empty[s], ((step >> 1) - 1) & 1, P, abort_flag, 401);
+        if (!ok) break;
+        const int h = step_head(step), qt = step_qt(step);
+        ptx::mbar_arrive_expect_tx(&sm.qd_full[s], 2 * kTileBytes);
+        for (int b = 0; b < HD / 64; ++b) {
+          ptx::tma_load_3d(sm.q[s][b], &tmQ, &sm.qd_full[s], b * 64, h, qt * kTile);
+          ptx::tma_load_3d(sm.dout[s][b], &tmDO, &sm.qd_full[s], b * 64, h, qt * kTile);
         }
-        pw[e / 2] = ptx::pack_bf16x2(pp[0], pp[1]);
-        dw[e / 2] = ptx::pack_bf16x2(dd[0], dd[1]);
       }
-#pragma unroll
-      for (int q4 = 0; q4 < 4; ++q4) {
-        const int c8 = c * 4 + q4;  // 16-byte chunk index along the 128 query columns
-        const uint32_t off = (c8 >> 3) * 16384 + sw128_chunk(r, c8 & 7);
-        *reinterpret_cast<uint4*>(sm.pt[0] + off) = make_uint4(pw[4 * q4], pw[4 * q4 + 1], pw[4 * q4 + 2], pw[4 * q4 + 3]);
-        *reinterpret_cast<uint4*>(sm.dst[0] + off) = make_uint4(dw[4 * q4], dw[4 * q4 + 1], dw[4 * q4 + 2], dw[4 * q4 + 3]);
-      }
+      ptx::mbar_wait(&sm.kv_full, 0, kDrainLimitNs, P.err, 409);
+      for (int u = (n_issued > 2 ? n_issued - 2 : 0); u < n_issued; ++u)
+        ptx::mbar_wait(&sm.qd_full[u & 1], (u >> 1) & 1, kDrainLimitNs, P.err, 409);
     }
-    ptx::fence_proxy_async_smem();
-    ptx::tc_fence_before();
-    __syncthreads();
-    if (tid == 0) {
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc_kt = ptx::idesc_bf16_f32(128, 128, 0, 0);  // S^T, dP^T
+      constexpr uint32_t idesc_kd = ptx::idesc_bf16_f32(128, HD, 0, 1);   // dV, dK
+      constexpr uint32_t idesc_qd = ptx::idesc_bf16_f32(128, HD, 1, 1);   // dQ
+      const uint32_t sk = ptx::smem_u32(sm.k[0]), sv = ptx::smem_u32(sm.v[0]);
+      const uint32_t sds = ptx::smem_u32(sm.dst[0]);
+      bool ok = bwd_wait(&sm.k_ready, 0, P, abort_flag, 411);
+      for (int step = 0; step < n_steps && ok; ++step) {
+        const int s = step & 1;
+        const uint32_t sq = ptx::smem_u32(sm.q[s][0]), sdo = ptx::smem_u32(sm.dout[s][0]);
+        ok = bwd_wait(&sm.q_ready[s], (step >> 1) & 1, P, abort_flag, 412);
+        if (!ok) break;
+        ptx::tc_fence_after();
+        for (int kk = 0; kk < HD / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+          ptx::mma_bf16(t_s, ptx::smem_desc_sw128(sk + off, 16, 1024), ptx::smem_desc_sw128(sq + off, 16, 1024),
+                        idesc_kt, kk > 0);
+        }
+        if (step > 0) {
+          // dQ~ of the previous tile must be drained before dP^T overwrites it
+          ok = bwd_wait(&sm.dq_free, (step - 1) & 1, P, abort_flag, 413);
+          if (!ok) break;
+          ptx::tc_fence_after();
+        }
+        for (int kk = 0; kk < HD / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+          ptx::mma_bf16(t_dp, ptx::smem_desc_sw128(sv + off, 16, 1024), ptx::smem_desc_sw128(sdo + off, 16, 1024),
+                        idesc_kt, kk > 0);
+        }
+        ptx::mma_commit(&sm.st_full);
+        ok = bwd_wait(&sm.p_full, step & 1, P, abort_flag, 414);
+        if (!ok) break;
+        ptx::tc_fence_after();
+        for (int kk = 0; kk < 8; ++kk)  // dV += P^T dO (P^T from TMEM)
+          ptx::mma_bf16_ts(t_dv, t_s + kk * 8, ptx::smem_desc_sw128(sdo + kk * 2048, 16384, 1024), idesc_kd,
+                           (step > 0 || kk > 0) ? 1u : 0u);
+        for (int kk = 0; kk < 8; ++kk) {  // dK~ += dS^T Q~
+          const uint32_t aoff = (kk >> 2) * 16384 + (kk & 3) * 32;
+          ptx::mma_bf16(t_dk, ptx::smem_desc_sw128(sds + aoff, 16, 1024),
+                        ptx::smem_desc_sw128(sq + kk * 2048, 16384, 1024), idesc_kd, (step > 0 || kk > 0) ? 1u : 0u);
+        }
+        for (int kk = 0; kk < 8; ++kk)  // dQ~ = dS K~
+          ptx::mma_bf16(t_dq, ptx::smem_desc_sw128(sds + kk * 2048, 16384, 1024),
+                        ptx::smem_desc_sw128(sk + kk * 2048, 16384, 1024), idesc_qd, kk > 0 ? 1u : 0u);
+        ptx::mma_commit(&sm.dq_full);
+        ptx::mma_commit(&sm.qd_empty[s]);
+      }
+      if (ok) ptx::mma_commit(&sm.o_full);
+      ptx::mma_commit(&sm.drain);
+      ptx::mbar_wait(&sm.drain, 0, kDrainLimitNs, P.err, 419);
+    }
+  } else if (warp >= 4 && warp < 8) {
+    // ------------------------------------------------------------ P / dS
+    const int r = tid & 127;
+    const int j = kt * kTile + r;
+    const bool key_valid = j < P.T;
+    const int jhi = key_valid ? __ldg(P.key_hi + j) : -1;  // rows [j, jhi] see key j
+    const float sl2 = P.scale * kLog2e;
+    const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
+    bool ok = true;
+    for (int step = 0; step < n_steps && ok; ++step) {
+      const int h = step_head(step), i0 = step_qt(step) * kTile;
+      const float* lse_row = P.lse + (size_t)h * P.T;
+      const float* d_row = P.ws.dsum + (size_t)h * P.T;
+      // vector loads need 16-byte aligned rows: T % 4 == 0, and no tail tile
+      const bool tail = i0 + kTile > P.T || (P.T & 3) != 0;
+      const bool full = __all_sync(0xffffffffu, j <= i0 && i0 + kTile - 1 <= jhi);
+      ok = bwd_wait(&sm.st_full, step & 1, P, abort_flag, 421);
+      if (!ok) break;
       ptx::tc_fence_after();
-      const uint32_t first = step == 0 ? 0u : 1u;
+#pragma unroll 1
+      for (int c = 0; c < 4; ++c) {
+        float sv[32], dpv[32];
+        ptx::tmem_ld32(t_s + lane_off + c * 32, sv);
+        ptx::tmem_ld32(t_dp + lane_off + c * 32, dpv);
+        ptx::tmem_wait_ld();
 #pragma unroll
-      for (int kk = 0; kk < 8; ++kk) {  // K = 128 query rows
-        const uint32_t aoff = (kk >> 2) * 16384 + (kk & 3) * 32;
-        ptx::mma_bf16(t_dv, ptx::smem_desc_sw128(ptx::smem_u32(sm.pt[0]) + aoff, 16, 1024),
-                      ptx::smem_desc_sw128(ptx::smem_u32(sm.dout[0]) + kk * 2048, 16384, 1024), idesc_kd,
-                      (first | (kk > 0)) ? 1u : 0u);
-      }
+        for (int gq = 0; gq < 4; ++gq) {  // 8 query columns at a time
+          const int cb = c * 32 + gq * 8;
+          float lse2[8], dd[8];
+          if (!tail) {
 #pragma unroll
-      for (int kk = 0; kk < 8; ++kk) {
-        const uint32_t aoff = (kk >> 2) * 16384 + (kk & 3) * 32;
-        ptx::mma_bf16(t_dk, ptx::smem_desc_sw128(ptx::smem_u32(sm.dst[0]) + aoff, 16, 1024),
-                      ptx::smem_desc_sw128(ptx::smem_u32(sm.q[0]) + kk * 2048, 16384, 1024), idesc_kd,
-                      (first | (kk > 0)) ? 1u : 0u);
-      }
+            for (int e = 0; e < 8; e += 4) {
+              const float4 a4 = __ldg(reinterpret_cast<const float4*>(lse_row + i0 + cb + e));
+              const float4 b4 = __ldg(reinterpret_cast<const float4*>(d_row + i0 + cb + e));
+              lse2[e] = a4.x * kLog2e; lse2[e + 1] = a4.y * kLog2e; lse2[e + 2] = a4.z * kLog2e; lse2[e + 3] = a4.w * kLog2e;
+              dd[e] = b4.x; dd[e + 1] = b4.y; dd[e + 2] = b4.z; dd[e + 3] = b4.w;
+            }
+          } else {
 #pragma unroll
-      for (int kk = 0; kk < 8; ++kk) {  // K = 128 keys
-        ptx::mma_bf16(t_dq, ptx::smem_desc_sw128(ptx::smem_u32(sm.dst[0]) + kk * 2048, 16384, 1024),
-                      ptx::smem_desc_sw128(ptx::smem_u32(sm.k[0]) + kk * 2048, 16384, 1024), idesc_qd,
-                      kk > 0 ? 1u : 0u);
+            for (int e = 0; e < 8; ++e) {
+              const int i = i0 + cb + e;
+              lse2[e] = i < P.T ? __ldg(lse_row + i) * kLog2e : INFINITY;
+              dd[e] = i < P.T ? __ldg(d_row + i) : 0.f;
+            }
+          }
+          uint32_t pw[4], dw[4];
+#pragma unroll
+          for (int e = 0; e < 8; e += 2) {
+            const int x = gq * 8 + e;
+            float p0, p1;
+            if (full) {
+              p0 = ex2(fmaf(sv[x], sl2, -lse2[e]));
+              p1 = ex2(fmaf(sv[x + 1], sl2, -lse2[e + 1]));
+            } else {
+              const int i = i0 + cb + e;
+              p0 = (i >= j && i <= jhi) ? ex2(fmaf(sv[x], sl2, -lse2[e])) : 0.f;
+              p1 = (i + 1 >= j && i + 1 <= jhi) ? ex2(fmaf(sv[x + 1], sl2, -lse2[e + 1])) : 0.f;
+            }
+            pw[e / 2] = ptx::pack_bf16x2(p0, p1);
+            dw[e / 2] = ptx::pack_bf16x2(p0 * (dpv[x] - dd[e]), p1 * (dpv[x + 1] - dd[e + 1]));
+          }
+          ptx::tmem_st4(t_s + lane_off + c * 16 + gq * 4, pw);
+          const int c8 = c * 4 + gq;  // 16-byte chunk along the 128 query columns
+          *reinterpret_cast<uint4*>(sm.dst[c8 >> 3] + sw128_chunk(r, c8 & 7)) = make_uint4(dw[0], dw[1], dw[2], dw[3]);
+        }
       }
-      ptx::mma_commit(&sm.bar_mma);
-      mma_pending = true;
+      ptx::tmem_wait_st();
+      ptx::fence_proxy_async_smem();
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(&sm.p_full);
     }
-    ok = ptx::mbar_wait(&sm.bar_mma, mma_phase, P.wait_limit_ns, P.err, 204);
-    if (__syncthreads_or(!ok)) goto abort;
-    mma_phase ^= 1;
-    if (tid == 0) {
-      mma_pending = false;
-      if (step + 1 < n_steps) {
-        issue_q(step + 1);
-        q_pending = true;
+    if (ok) ok = bwd_wait(&sm.o_full, 0, P, abort_flag, 423);
+    if (ok) {
+      // ---- epilogue: dV and dk = R^T (scale dK~) for this thread's key row
+      ptx::tc_fence_after();
+      __nv_bfloat16* dvrow = P.dv + ((size_t)(key_valid ? j : 0) * P.Hkv + g) * HD;
+      __nv_bfloat16* dkrow = P.dk + ((size_t)(key_valid ? j : 0) * P.Hkv + g) * HD;
+      const int pos = key_valid ? __ldg(P.pos_id + j) : 0;
+      auto store32 = [&](__nv_bfloat16* row, int c0, const float* x) {
+        uint4* dst = reinterpret_cast<uint4*>(row + c0);
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+          dst[c] = make_uint4(ptx::pack_bf16x2(x[8 * c], x[8 * c + 1]), ptx::pack_bf16x2(x[8 * c + 2], x[8 * c + 3]),
+                              ptx::pack_bf16x2(x[8 * c + 4], x[8 * c + 5]), ptx::pack_bf16x2(x[8 * c + 6], x[8 * c + 7]));
+      };
+#pragma unroll 1
+      for (int c = 0; c < HD / 32; ++c) {
+        float x[32];
+        ptx::tmem_ld32(t_dv + lane_off + c * 32, x);
+        ptx::tmem_wait_ld();
+        if (key_valid) store32(dvrow, c * 32, x);
+      }
+      if (P.layout != 1) {
+#pragma unroll 1
+        for (int c = 0; c < HD / 32; ++c) {
+          float x[32];
+          ptx::tmem_ld32(t_dk + lane_off + c * 32, x);
+          ptx::tmem_wait_ld();
+          if (key_valid) {
+#pragma unroll
+            for (int e = 0; e < 32; ++e) x[e] *= P.scale;
+            if (P.layout == 0) {
+#pragma unroll
+              for (int e = 0; e < 32; e += 2) {
+                const float2 cs = rope_cs(P.rope_hi, P.rope_lo, pos, (c * 32 + e) >> 1, HD / 2);
+                rope_pair(x[e], x[e + 1], cs.x, -cs.y);
+              }
+            }
+            store32(dkrow, c * 32, x);
+          }
+        }
+      } else {
+        // pairs (p, p + D/2): columns c*32.. meet columns D/2 + c*32..
+#pragma unroll 1
+        for (int c = 0; c < HD / 64; ++c) {
+          float x[32], y[32];
+          ptx::tmem_ld32(t_dk + lane_off + c * 32, x);
+          ptx::tmem_ld32(t_dk + lane_off + HD / 2 + c * 32, y);
+          ptx::tmem_wait_ld();
+          if (key_valid) {
+#pragma unroll
+            for (int e = 0; e < 32; ++e) {
+              x[e] *= P.scale;
+              y[e] *= P.scale;
+              const float2 cs = rope_cs(P.rope_hi, P.rope_lo, pos, c * 32 + e, HD / 2);
+              rope_pair(x[e], y[e], cs.x, -cs.y);
+            }
+            store32(dkrow, c * 32, x);
+            store32(dkrow, HD / 2 + c * 32, y);
+          }
+        }
       }
     }
-    ptx::tc_fence_after();
-    {
-      // dQ~ rows of this tile: TMEM lane r = query row i0 + r
-      const int i = i0 + r;
+  } else if (warp >= 8 && warp < 12) {
+    // ------------------------------------------------------------ dQ drain
+    const int r = tid & 127;
+    const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
+    bool ok = true;
+    for (int step = 0; step < n_steps && ok; ++step) {
+      const int h = step_head(step), i = step_qt(step) * kTile + r;
+      ok = bwd_wait(&sm.dq_full, step & 1, P, abort_flag, 431);
+      if (!ok) break;
+      ptx::tc_fence_after();
       float* dst = P.ws.dq_acc + ((size_t)(i < P.T ? i : 0) * P.Hq + h) * HD;
 #pragma unroll 1
       for (int c = 0; c < HD / 32; ++c) {
@@ -409,65 +522,33 @@ __global__ void __launch_bounds__(128, 1)
                             P.scale * dq[e + 3]);
         }
       }
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(&sm.dq_free);
     }
-    ptx::tc_fence_before();
-    __syncthreads();
+  } else if (warp >= 12) {
+    // ------------------------------------------------------------ RoPE
+    const int r = tid & 127;
+    bool ok = bwd_wait(&sm.kv_full, 0, P, abort_flag, 441);
+    if (ok) {
+      const int j = kt * kTile + r;
+      if (j < P.T) rope_row_smem<HD>(sm.k[0], r, __ldg(P.pos_id + j), P.layout, false, P.rope_hi, P.rope_lo);
+      ptx::fence_proxy_async_smem();
+      ptx::mbar_arrive(&sm.k_ready);
+    }
+    for (int step = 0; step < n_steps && ok; ++step) {
+      const int s = step & 1;
+      ok = bwd_wait(&sm.qd_full[s], (step >> 1) & 1, P, abort_flag, 442);
+      if (!ok) break;
+      const int i = step_qt(step) * kTile + r;
+      if (i < P.T) rope_row_smem<HD>(sm.q[s][0], r, __ldg(P.pos_id + i), P.layout, false, P.rope_hi, P.rope_lo);
+      ptx::fence_proxy_async_smem();
+      ptx::mbar_arrive(&sm.q_ready[s]);
+    }
   }
 
-  {
-    // ---- epilogue: dV and dK~ for this thread's key row; dk = R^T (scale dK~)
-    float acc[HD];
-#pragma unroll
-    for (int c = 0; c < HD / 32; ++c) ptx::tmem_ld32(t_dv + lane_off + c * 32, acc + c * 32);
-    ptx::tmem_wait_ld();
-    if (key_valid) {
-      uint4* dst = reinterpret_cast<uint4*>(P.dv + ((size_t)j * P.Hkv + g) * HD);
-#pragma unroll
-      for (int c = 0; c < HD / 8; ++c)
-        dst[c] = make_uint4(ptx::pack_bf16x2(acc[8 * c], acc[8 * c + 1]), ptx::pack_bf16x2(acc[8 * c + 2], acc[8 * c + 3]),
-                            ptx::pack_bf16x2(acc[8 * c + 4], acc[8 * c + 5]), ptx::pack_bf16x2(acc[8 * c + 6], acc[8 * c + 7]));
-    }
-#pragma unroll
-    for (int c = 0; c < HD / 32; ++c) ptx::tmem_ld32(t_dk + lane_off + c * 32, acc + c * 32);
-    ptx::tmem_wait_ld();
-    if (key_valid) {
-#pragma unroll
-      for (int c = 0; c < HD; ++c) acc[c] *= P.scale;
-      const int pos = __ldg(P.pos_id + j);
-      if (P.layout == 0) {
-#pragma unroll
-        for (int p = 0; p < HD / 2; ++p) {
-          const float2 cs = rope_cs(P.rope_hi, P.rope_lo, pos, p, HD / 2);
-          rope_pair(acc[2 * p], acc[2 * p + 1], cs.x, -cs.y);
-        }
-      } else if (P.layout == 1) {
-#pragma unroll
-        for (int p = 0; p < HD / 2; ++p) {
-          const float2 cs = rope_cs(P.rope_hi, P.rope_lo, pos, p, HD / 2);
-          rope_pair(acc[p], acc[p + HD / 2], cs.x, -cs.y);
-        }
-      }
-      uint4* dst = reinterpret_cast<uint4*>(P.dk + ((size_t)j * P.Hkv + g) * HD);
-#pragma unroll
-      for (int c = 0; c < HD / 8; ++c)
-        dst[c] = make_uint4(ptx::pack_bf16x2(acc[8 * c], acc[8 * c + 1]), ptx::pack_bf16x2(acc[8 * c + 2], acc[8 * c + 3]),
-                            ptx::pack_bf16x2(acc[8 * c + 4], acc[8 * c + 5]), ptx::pack_bf16x2(acc[8 * c + 6], acc[8 * c + 7]));
-    }
-  }
   ptx::tc_fence_before();
   __syncthreads();
-  if (warp == 0) ptx::tmem_dealloc(tmem, kTmemCols);
-  return;
-
-abort:
-  if (tid == 0) {
-    if (kv_pending) ptx::mbar_wait(&sm.bar_kv, 0, kDrainLimitNs, P.err, 299);
-    if (q_pending) ptx::mbar_wait(&sm.bar_q, q_phase, kDrainLimitNs, P.err, 299);
-    if (mma_pending) ptx::mbar_wait(&sm.bar_mma, mma_phase, kDrainLimitNs, P.err, 299);
-  }
-  ptx::tc_fence_before();
-  __syncthreads();
-  if (warp == 0) ptx::tmem_dealloc(tmem, kTmemCols);
+  if (warp == 1) ptx::tmem_dealloc(tmem, kTmemCols);
 }
 
 // ---------------------------------------------------------------- 3. dq
@@ -595,7 +676,7 @@ aa_status launch_bwd(aa_plan_s* p, const void* q, const void* k, const void* v, 
   if (e != cudaSuccess) return cuda_fail(e, "attn_bwd_kernel smem attribute");
   if (p->bwd_ev_start && (e = cudaEventRecord(p->bwd_ev_start, s)) != cudaSuccess)
     return cuda_fail(e, "recording the bwd start event");
-  attn_bwd_kernel<HD><<<(unsigned)p->bwd_items.size(), 128, smem, s>>>(tq, tk, tv, tdo, P);
+  attn_bwd_kernel<HD><<<(unsigned)p->bwd_items.size(), kBwdThreads, smem, s>>>(tq, tk, tv, tdo, P);
   if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(e, "attn_bwd_kernel launch");
   if (p->bwd_ev_stop && (e = cudaEventRecord(p->bwd_ev_stop, s)) != cudaSuccess)
     return cuda_fail(e, "recording the bwd stop event");

@@ -172,6 +172,13 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float* v) {
       : "memory");
 }
 
+// Each thread of the warp writes 4 consecutive 32-bit columns of its own lane.
+__device__ __forceinline__ void tmem_st4(uint32_t taddr, const uint32_t* w) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1,%2,%3,%4};" ::"r"(taddr), "r"(w[0]), "r"(w[1]),
+               "r"(w[2]), "r"(w[3])
+               : "memory");
+}
+
 // Each thread of the warp writes 16 consecutive 32-bit columns of its own lane.
 __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t* w) {
   asm volatile(
