@@ -11,7 +11,8 @@
 
 namespace aa {
 
-constexpr int kTile = 128;  // rows of a query tile and of a key tile
+constexpr int kTile = 128;      // rows of a query tile and of a key tile
+constexpr int kRopeSplit = 32;  // position split of the two-level cos/sin tables
 
 // One unit of forward work: query tile `tile` of query head `head`, visiting
 // key tiles [lo, hi] (inclusive). One unit of backward work: key tile `tile`
@@ -28,8 +29,8 @@ struct DevicePlan {
   WorkItem* fwd_items = nullptr;
   WorkItem* bwd_items = nullptr;
   int32_t* qtile_klo = nullptr;  // [n_tiles] first live key tile of each query tile
-  float2* rope_hi = nullptr;   // [n_hi][D/2]  cos/sin((128*h) * theta_p)
-  float2* rope_lo = nullptr;   // [D/2][128]   cos/sin(l * theta_p), p-major
+  float2* rope_hi = nullptr;   // [n_hi][D/2]  cos/sin((32*h) * theta_p)
+  float2* rope_lo = nullptr;   // [D/2][32]    cos/sin(l * theta_p), p-major
   int32_t* err = nullptr;      // device error word (0 = ok)
 };
 

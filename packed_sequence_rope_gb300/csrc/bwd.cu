@@ -196,6 +196,8 @@ struct BwdSmem {
   alignas(1024) uint8_t q[2][kB][16384];
   alignas(1024) uint8_t dout[2][kB][16384];
   alignas(1024) uint8_t dst[2][16384];  // dS^T: 128 keys x 128 query rows, bf16
+  float lse2[2][128];                   // LSE * log2(e) of each stage's query rows
+  float dsum[2][128];                   // D of each stage's query rows
   uint64_t kv_full, k_ready;
   uint64_t qd_full[2], q_ready[2], qd_empty[2];
   uint64_t st_full, p_full, dq_full, dq_free, o_full, drain;
@@ -234,20 +236,20 @@ __device__ __forceinline__ bool bwd_wait(uint64_t* bar, uint32_t parity, const B
   }
 }
 
-__device__ __forceinline__ float ex2(float x) {
-  float y;
-  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-  return y;
-}
 
 template <int HD>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     attn_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
                     const BwdParams P) {
-  extern __shared__ uint8_t smem_raw[];
-  BwdSmem<HD>& sm = *reinterpret_cast<BwdSmem<HD>*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                                    ~uintptr_t(1023));
+  // the layout fills the 227 KB limit exactly, so it relies on a 1 KB aligned
+  // dynamic shared-memory base (checked: swizzled tiles need it)
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  if (ptx::smem_u32(smem_raw) & 1023u) {
+    if (threadIdx.x == 0) atomicCAS(P.err, 0, 498);
+    return;
+  }
+  BwdSmem<HD>& sm = *reinterpret_cast<BwdSmem<HD>*>(smem_raw);
   constexpr int kTmemCols = 512;
   constexpr uint32_t kTileBytes = 128 * HD * 2;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -376,15 +378,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
     bool ok = true;
     for (int step = 0; step < n_steps && ok; ++step) {
-      const int h = step_head(step), i0 = step_qt(step) * kTile;
-      const float* lse_row = P.lse + (size_t)h * P.T;
-      const float* d_row = P.ws.dsum + (size_t)h * P.T;
-      // vector loads need 16-byte aligned rows: T % 4 == 0, and no tail tile
-      const bool tail = i0 + kTile > P.T || (P.T & 3) != 0;
+      const int s = step & 1, i0 = step_qt(step) * kTile;
       const bool full = __all_sync(0xffffffffu, j <= i0 && i0 + kTile - 1 <= jhi);
-      ok = bwd_wait(&sm.st_full, step & 1, P, abort_flag, 421);
+      ok = bwd_wait(&sm.q_ready[s], (step >> 1) & 1, P, abort_flag, 420);  // LSE/D staged
+      if (ok) ok = bwd_wait(&sm.st_full, step & 1, P, abort_flag, 421);
       if (!ok) break;
       ptx::tc_fence_after();
+      const float4* lse_s = reinterpret_cast<const float4*>(sm.lse2[s]);
+      const float4* d_s = reinterpret_cast<const float4*>(sm.dsum[s]);
 #pragma unroll 1
       for (int c = 0; c < 4; ++c) {
         float sv[32], dpv[32];
@@ -395,21 +396,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         for (int gq = 0; gq < 4; ++gq) {  // 8 query columns at a time
           const int cb = c * 32 + gq * 8;
           float lse2[8], dd[8];
-          if (!tail) {
 #pragma unroll
-            for (int e = 0; e < 8; e += 4) {
-              const float4 a4 = __ldg(reinterpret_cast<const float4*>(lse_row + i0 + cb + e));
-              const float4 b4 = __ldg(reinterpret_cast<const float4*>(d_row + i0 + cb + e));
-              lse2[e] = a4.x * kLog2e; lse2[e + 1] = a4.y * kLog2e; lse2[e + 2] = a4.z * kLog2e; lse2[e + 3] = a4.w * kLog2e;
-              dd[e] = b4.x; dd[e + 1] = b4.y; dd[e + 2] = b4.z; dd[e + 3] = b4.w;
-            }
-          } else {
-#pragma unroll
-            for (int e = 0; e < 8; ++e) {
-              const int i = i0 + cb + e;
-              lse2[e] = i < P.T ? __ldg(lse_row + i) * kLog2e : INFINITY;
-              dd[e] = i < P.T ? __ldg(d_row + i) : 0.f;
-            }
+          for (int e = 0; e < 8; e += 4) {
+            const float4 a4 = lse_s[(cb + e) >> 2], b4 = d_s[(cb + e) >> 2];
+            lse2[e] = a4.x; lse2[e + 1] = a4.y; lse2[e + 2] = a4.z; lse2[e + 3] = a4.w;
+            dd[e] = b4.x; dd[e + 1] = b4.y; dd[e + 2] = b4.z; dd[e + 3] = b4.w;
           }
           uint32_t pw[4], dw[4];
 #pragma unroll
@@ -417,12 +408,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             const int x = gq * 8 + e;
             float p0, p1;
             if (full) {
-              p0 = ex2(fmaf(sv[x], sl2, -lse2[e]));
-              p1 = ex2(fmaf(sv[x + 1], sl2, -lse2[e + 1]));
+              p0 = ptx::ex2(fmaf(sv[x], sl2, -lse2[e]));
+              p1 = ptx::ex2(fmaf(sv[x + 1], sl2, -lse2[e + 1]));
             } else {
               const int i = i0 + cb + e;
-              p0 = (i >= j && i <= jhi) ? ex2(fmaf(sv[x], sl2, -lse2[e])) : 0.f;
-              p1 = (i + 1 >= j && i + 1 <= jhi) ? ex2(fmaf(sv[x + 1], sl2, -lse2[e + 1])) : 0.f;
+              p0 = (i >= j && i <= jhi) ? ptx::ex2(fmaf(sv[x], sl2, -lse2[e])) : 0.f;
+              p1 = (i + 1 >= j && i + 1 <= jhi) ? ptx::ex2(fmaf(sv[x + 1], sl2, -lse2[e + 1])) : 0.f;
             }
             pw[e / 2] = ptx::pack_bf16x2(p0, p1);
             dw[e / 2] = ptx::pack_bf16x2(p0 * (dpv[x] - dd[e]), p1 * (dpv[x + 1] - dd[e + 1]));
@@ -540,6 +531,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       ok = bwd_wait(&sm.qd_full[s], (step >> 1) & 1, P, abort_flag, 442);
       if (!ok) break;
       const int i = step_qt(step) * kTile + r;
+      const size_t hrow = (size_t)step_head(step) * P.T;
+      sm.lse2[s][r] = i < P.T ? __ldg(P.lse + hrow + i) * kLog2e : INFINITY;
+      sm.dsum[s][r] = i < P.T ? __ldg(P.ws.dsum + hrow + i) : 0.f;
       if (i < P.T) rope_row_smem<HD>(sm.q[s][0], r, __ldg(P.pos_id + i), P.layout, false, P.rope_hi, P.rope_lo);
       ptx::fence_proxy_async_smem();
       ptx::mbar_arrive(&sm.q_ready[s]);
@@ -671,7 +665,7 @@ aa_status launch_bwd(aa_plan_s* p, const void* q, const void* k, const void* v, 
   P.group = p->group;
   P.layout = rope_layout;
   P.scale = p->scale;
-  const size_t smem = sizeof(BwdSmem<HD>) + 1024;
+  const size_t smem = sizeof(BwdSmem<HD>);
   e = cudaFuncSetAttribute(attn_bwd_kernel<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return cuda_fail(e, "attn_bwd_kernel smem attribute");
   if (p->bwd_ev_start && (e = cudaEventRecord(p->bwd_ev_start, s)) != cudaSuccess)

@@ -87,9 +87,12 @@ template <int HD>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const FwdParams P) {
-  extern __shared__ uint8_t smem_raw[];
-  FwdSmem<HD>& sm = *reinterpret_cast<FwdSmem<HD>*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                                    ~uintptr_t(1023));
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  if (ptx::smem_u32(smem_raw) & 1023u) {  // swizzled tiles need a 1 KB aligned base
+    if (threadIdx.x == 0) atomicCAS(P.err, 0, 398);
+    return;
+  }
+  FwdSmem<HD>& sm = *reinterpret_cast<FwdSmem<HD>*>(smem_raw);
   constexpr uint32_t kTileBytes = 128 * HD * 2;
   constexpr int kTmemCols = 512;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -244,19 +247,27 @@ __global__ void __launch_bounds__(kThreads, 1)
       ph_s ^= 1;
       ptx::tc_fence_after();
       const int j0 = kt * kTile;
-      // pass 1: row max of the visible scaled logits
+      // tiles every row of the warp sees entirely skip the per-element mask
+      const bool full = __all_sync(0xffffffffu, lo <= j0 && j0 + kTile - 1 <= hi);
+      // pass 1: row max of the visible logits (scaled once at the end)
       float mt = -INFINITY;
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         float sv[32];
         ptx::tmem_ld32(t_s + c * 32, sv);
         ptx::tmem_wait_ld();
+        if (full) {
 #pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          const int j = j0 + c * 32 + e;
-          if (j >= lo && j <= hi) mt = fmaxf(mt, sv[e] * sl2);
+          for (int e = 0; e < 32; e += 2) mt = fmaxf(mt, fmaxf(sv[e], sv[e + 1]));
+        } else {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) {
+            const int j = j0 + c * 32 + e;
+            if (j >= lo && j <= hi) mt = fmaxf(mt, sv[e]);
+          }
         }
       }
+      mt *= sl2;
       // TMEM access is warp-collective, so a rescale of O is decided per warp
       const bool need = (mt > m + kRescaleThreshold) || (m == -INFINITY && mt > -INFINITY);
       if (__any_sync(0xffffffffu, need)) {
@@ -285,13 +296,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::tmem_ld32(t_s + c * 32, sv);
         ptx::tmem_wait_ld();
         uint32_t w[16];
+        if (full) {
 #pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          const int j = j0 + c * 32 + 2 * e;
-          const float p0 = (j >= lo && j <= hi) ? exp2f(fmaf(sv[2 * e], sl2, -mm)) : 0.f;
-          const float p1 = (j + 1 >= lo && j + 1 <= hi) ? exp2f(fmaf(sv[2 * e + 1], sl2, -mm)) : 0.f;
-          rs += p0 + p1;
-          w[e] = ptx::pack_bf16x2(p0, p1);
+          for (int e = 0; e < 16; ++e) {
+            const float p0 = ptx::ex2(fmaf(sv[2 * e], sl2, -mm));
+            const float p1 = ptx::ex2(fmaf(sv[2 * e + 1], sl2, -mm));
+            rs += p0 + p1;
+            w[e] = ptx::pack_bf16x2(p0, p1);
+          }
+        } else {
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            const int j = j0 + c * 32 + 2 * e;
+            const float p0 = (j >= lo && j <= hi) ? ptx::ex2(fmaf(sv[2 * e], sl2, -mm)) : 0.f;
+            const float p1 = (j + 1 >= lo && j + 1 <= hi) ? ptx::ex2(fmaf(sv[2 * e + 1], sl2, -mm)) : 0.f;
+            rs += p0 + p1;
+            w[e] = ptx::pack_bf16x2(p0, p1);
+          }
         }
         ptx::tmem_st16(t_s + c * 16, w);
       }
@@ -401,7 +422,7 @@ aa_status launch_fwd(aa_plan_s* p, const void* q, const void* k, const void* v, 
   P.anchor = p->anchor ? 1 : 0;
   P.n_tiles = p->n_tiles;
   P.scale = p->scale;
-  const size_t smem = sizeof(FwdSmem<HD>) + 1024;
+  const size_t smem = sizeof(FwdSmem<HD>);
   cudaError_t e = cudaFuncSetAttribute(attn_fwd_kernel<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return cuda_fail(e, "attn_fwd_kernel smem attribute");
   const unsigned n_items = (unsigned)p->fwd_items.size();

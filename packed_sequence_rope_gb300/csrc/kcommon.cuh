@@ -12,13 +12,13 @@
 
 namespace aa {
 
-// (cos, sin)(pos * theta_p) from the two-level tables: pos = 128*h + l and the
+// (cos, sin)(pos * theta_p) from the two-level tables: pos = 32*h + l and the
 // angle-addition identity, evaluated with explicitly rounded fp32 operations
 // so every kernel produces identical bits for the same (pos, p).
 __device__ __forceinline__ float2 rope_cs(const float2* __restrict__ hi_tab, const float2* __restrict__ lo_tab,
                                           int pos, int p, int half) {
-  const float2 a = __ldg(hi_tab + (size_t)(pos >> 7) * half + p);
-  const float2 b = __ldg(lo_tab + (size_t)p * 128 + (pos & 127));
+  const float2 a = __ldg(hi_tab + (size_t)(pos >> 5) * half + p);
+  const float2 b = __ldg(lo_tab + (size_t)p * kRopeSplit + (pos & (kRopeSplit - 1)));
   const float c = __fmaf_rn(a.x, b.x, -__fmul_rn(a.y, b.y));
   const float s = __fmaf_rn(a.y, b.x, __fmul_rn(a.x, b.y));
   return make_float2(c, s);

@@ -134,29 +134,31 @@ static void build_stats_and_work(aa_plan_s* p) {
   for (auto& w : p->bwd_items) p->bwd_tiles += (int64_t)(w.hi - w.lo + 1) * p->group;
 }
 
-// Two-level cos/sin tables for Eq. 6: pos = 128*h + l, so
+// Two-level cos/sin tables for Eq. 6: pos = 32*h + l, so
 // (cos, sin)(pos*theta_p) is the complex product of rope_hi[h][p] and
 // rope_lo[p][l]. Entries are computed in fp64 and rounded once to fp32.
-// rope_lo is p-major so that consecutive positions read consecutive entries.
+// rope_lo (16 KB at D = 128) stays in L1; a 128-row tile touches only a few
+// rope_hi rows, and rope_lo is p-major so consecutive positions read
+// consecutive entries.
 static void build_rope_tables(aa_plan_s* p) {
   const int half = p->D / 2;
   int max_pos = 0;
   for (int v : p->pos_id) max_pos = std::max(max_pos, v);
-  p->n_hi = max_pos / kTile + 1;
+  p->n_hi = max_pos / kRopeSplit + 1;
   std::vector<double> theta(half);
   for (int i = 0; i < half; ++i)
     theta[i] = std::pow(p->cfg.rope_base, -2.0 * (double)i / (double)p->D);
   p->rope_hi.resize((size_t)p->n_hi * half);
-  p->rope_lo.resize((size_t)kTile * half);
+  p->rope_lo.resize((size_t)kRopeSplit * half);
   for (int h = 0; h < p->n_hi; ++h)
     for (int i = 0; i < half; ++i) {
-      const double ang = (double)h * kTile * theta[i];
+      const double ang = (double)h * kRopeSplit * theta[i];
       p->rope_hi[(size_t)h * half + i] = make_float2((float)std::cos(ang), (float)std::sin(ang));
     }
   for (int i = 0; i < half; ++i)
-    for (int l = 0; l < kTile; ++l) {
+    for (int l = 0; l < kRopeSplit; ++l) {
       const double ang = (double)l * theta[i];
-      p->rope_lo[(size_t)i * kTile + l] = make_float2((float)std::cos(ang), (float)std::sin(ang));
+      p->rope_lo[(size_t)i * kRopeSplit + l] = make_float2((float)std::cos(ang), (float)std::sin(ang));
     }
 }
 
@@ -339,7 +341,7 @@ extern "C" aa_status aa_check_device_error(aa_plan_t p, aa_stream_t stream) {
     if (e == cudaSuccess) e = cudaStreamSynchronize(s);
     if (e != cudaSuccess) return cuda_fail(e, "clearing the device error word");
     char buf[96];
-    std::snprintf(buf, sizeof buf, "device wait timed out (site code %d)", (int)word);
+    std::snprintf(buf, sizeof buf, "device-side wait timed out or launch check failed (site code %d)", (int)word);
     return fail(AA_ERR_TIMEOUT, buf);
   }
   return AA_OK;
