@@ -150,11 +150,13 @@ def run_ours(args):
     lse = torch.empty(Hq, T, device=dev, dtype=torch.float32)
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
     ws = plan.alloc_workspace(dev)
+    fws = plan.alloc_fwd_workspace(dev)
     stream = torch.cuda.current_stream()
-    n_launch_per_step = 1 + 3 + (1 if mask == aa.MASK_ANCHOR else 0)
+    # fwd: K rotation + attention; bwd: Q rotation, prep, tile kernel, dq finalize (+ anchor)
+    n_launch_per_step = 2 + 4 + (1 if mask == aa.MASK_ANCHOR else 0)
 
     def step():
-        plan.fwd(q, k, v, o, lse)
+        plan.fwd(q, k, v, o, lse, fws)
         plan.bwd(q, k, v, o, lse, do, dq, dk, dv, ws)
 
     for _ in range(args.warmup):
@@ -176,7 +178,7 @@ def run_ours(args):
     for s in range(args.steps):
         e = ev[s]
         e[0].record(stream)
-        plan.fwd(q, k, v, o, lse)
+        plan.fwd(q, k, v, o, lse, fws)
         e[1].record(stream)
         plan.set_bwd_timing_events(e[2], e[3])
         plan.bwd(q, k, v, o, lse, do, dq, dk, dv, ws)
@@ -265,15 +267,16 @@ def _causal_speedup(aa, w, q, k, v, do, dev, ms_anchor, args):
         lse = torch.empty(Hq, T, device=dev, dtype=torch.float32)
         dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
         ws = pc.alloc_workspace(dev)
+        fws = pc.alloc_fwd_workspace(dev)
         for _ in range(1):
-            pc.fwd(q, k, v, o, lse)
+            pc.fwd(q, k, v, o, lse, fws)
             pc.bwd(q, k, v, o, lse, do, dq, dk, dv, ws)
         torch.cuda.synchronize()
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         n = 2
         a.record()
         for _ in range(n):
-            pc.fwd(q, k, v, o, lse)
+            pc.fwd(q, k, v, o, lse, fws)
             pc.bwd(q, k, v, o, lse, do, dq, dk, dv, ws)
         b.record()
         torch.cuda.synchronize()
@@ -297,13 +300,14 @@ def _e2e(aa, plan, w, dev, args, flops, world):
     lse = torch.empty(Hq, T, device=dev, dtype=torch.float32)
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
     ws = plan.alloc_workspace(dev)
+    fws = plan.alloc_fwd_workspace(dev)
     h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hdo))
     d2h = sum(t.numel() * t.element_size() for t in (out_o, out_l, out_dq, out_dk, out_dv))
 
     def step():
         for d_, h_ in ((q, hq), (k, hk), (v, hv), (do, hdo)):
             d_.copy_(h_, non_blocking=True)
-        plan.fwd(q, k, v, o, lse)
+        plan.fwd(q, k, v, o, lse, fws)
         plan.bwd(q, k, v, o, lse, do, dq, dk, dv, ws)
         for h_, d_ in ((out_o, o), (out_l, lse), (out_dq, dq), (out_dk, dk), (out_dv, dv)):
             h_.copy_(d_, non_blocking=True)

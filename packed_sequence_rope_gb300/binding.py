@@ -22,7 +22,7 @@ STATUS = {0: "AA_OK", 1: "AA_ERR_INVALID_ARG", 2: "AA_ERR_UNSUPPORTED", 3: "AA_E
 
 # every symbol include/anchorattn.h declares
 EXPORTS = ["aa_plan", "aa_plan_destroy", "aa_plan_metadata", "aa_plan_stats", "aa_plan_work",
-           "aa_rope_apply", "aa_fwd", "aa_bwd_workspace_bytes", "aa_bwd", "aa_bwd_static_workspace", "aa_check_device_error",
+           "aa_rope_apply", "aa_fwd", "aa_fwd_workspace_bytes", "aa_bwd_workspace_bytes", "aa_bwd", "aa_bwd_static_workspace", "aa_check_device_error",
            "aa_set_wait_limit", "aa_set_bwd_timing_events", "aa_status_string", "aa_last_error"]
 
 
@@ -60,7 +60,8 @@ def lib():
             "aa_plan_stats": ([vp, i64p, i64p, i64p], ctypes.c_int),
             "aa_plan_work": ([vp, i64p, i64p], ctypes.c_int),
             "aa_rope_apply": ([vp, vp, vp, i32, i32, vp], ctypes.c_int),
-            "aa_fwd": ([vp, vp, vp, vp, vp, vp, vp], ctypes.c_int),
+            "aa_fwd": ([vp, vp, vp, vp, vp, vp, vp, ctypes.c_size_t, vp], ctypes.c_int),
+            "aa_fwd_workspace_bytes": ([vp], ctypes.c_size_t),
             "aa_bwd_workspace_bytes": ([vp], ctypes.c_size_t),
             "aa_bwd": ([vp] + [vp] * 9 + [vp, ctypes.c_size_t, vp], ctypes.c_int),
             "aa_bwd_static_workspace": ([vp] + [vp] * 9 + [vp], ctypes.c_int),
@@ -178,13 +179,22 @@ class Plan:
                                    _stream(stream)))
         return y
 
-    def fwd(self, q, k, v, o=None, lse=None, stream=None):
+    def fwd_workspace_bytes(self):
+        return int(lib().aa_fwd_workspace_bytes(self._h))
+
+    def alloc_fwd_workspace(self, device):
+        import torch
+        return torch.empty(max(self.fwd_workspace_bytes(), 256), device=device, dtype=torch.uint8)
+
+    def fwd(self, q, k, v, o=None, lse=None, workspace=None, stream=None):
         import torch
         for t in (q, k, v):
             assert t.is_cuda and t.dtype == torch.bfloat16 and t.is_contiguous()
         o = torch.empty_like(q) if o is None else o
         lse = torch.empty(self.Hq, self.T, device=q.device, dtype=torch.float32) if lse is None else lse
-        _check(lib().aa_fwd(self._h, _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _stream(stream)))
+        ws = self.alloc_fwd_workspace(q.device) if workspace is None else workspace
+        _check(lib().aa_fwd(self._h, _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(ws),
+                            ctypes.c_size_t(ws.numel()), _stream(stream)))
         return o, lse
 
     def alloc_workspace(self, device):

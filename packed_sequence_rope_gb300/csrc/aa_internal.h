@@ -31,6 +31,7 @@ struct DevicePlan {
   int32_t* qtile_klo = nullptr;  // [n_tiles] first live key tile of each query tile
   float2* rope_hi = nullptr;   // [n_hi][D/2]  cos/sin((32*h) * theta_p)
   float2* rope_lo = nullptr;   // [D/2][32]    cos/sin(l * theta_p), p-major
+  float2* rope_step = nullptr; // [D/2]        cos/sin(theta_p)
   int32_t* err = nullptr;      // device error word (0 = ok)
 };
 
@@ -46,7 +47,7 @@ struct aa_plan_s {
   std::vector<int32_t> doc_id, pos_id, row_lo, key_hi;
   std::vector<aa::WorkItem> fwd_items, bwd_items;  // fwd: one item per (query-tile pair, head)
   std::vector<int32_t> qtile_klo;
-  std::vector<float2> rope_hi, rope_lo;
+  std::vector<float2> rope_hi, rope_lo, rope_step;
   int32_t n_hi = 0;
   int64_t unmasked_pairs = 0, live_tiles = 0, causal_tiles = 0;
   int64_t fwd_tiles = 0, bwd_tiles = 0;
@@ -62,6 +63,8 @@ aa_status fail(aa_status s, const std::string& msg);
 aa_status cuda_fail(cudaError_t e, const char* what);
 bool aligned16(const void* p);
 aa_status check_compute_plan(const aa_plan_s* p);
+// Rotate x [T, H, D] into y with the canonical tile rotation (no checks).
+aa_status launch_rope(const aa_plan_s* p, const void* x, void* y, int H, int inverse, cudaStream_t s);
 // Launch the backward kernels with an already-validated workspace pointer.
 aa_status launch_bwd_with_workspace(aa_plan_s* p, const void* q, const void* k, const void* v, const void* o,
                                     const float* lse, const void* dout, void* dq, void* dk, void* dv,

@@ -32,6 +32,7 @@ constexpr uint64_t kDrainLimitNs = 1000000000ull;
 constexpr int kPrepChunks = 64;  // row chunks of the anchor partial sums
 
 struct Workspace {
+  __nv_bfloat16* qr;  // [T, Hq, D] rotated Q (unused without RoPE)
   float* dq_acc;   // [T, Hq, D] fp32
   float* dsum;     // [Hq, T] fp32 (D_i)
   float* part_dv;  // [kPrepChunks, Hq, D]
@@ -44,6 +45,8 @@ Workspace carve(void* base, const aa_plan_s* p, size_t* total) {
   Workspace w;
   size_t off = 0;
   uint8_t* b = static_cast<uint8_t*>(base);
+  w.qr = reinterpret_cast<__nv_bfloat16*>(b + off);
+  if (p->cfg.rope_layout != AA_ROPE_NONE) off = align256(off + (size_t)p->T * p->Hq * p->D * 2);
   w.dq_acc = reinterpret_cast<float*>(b + off);
   off = align256(off + (size_t)p->T * p->Hq * p->D * 4);
   w.dsum = reinterpret_cast<float*>(b + off);
@@ -130,14 +133,12 @@ __global__ void __launch_bounds__(128) bwd_prep_kernel(const __nv_bfloat16* __re
     if (lane == 0) ws.dsum[(size_t)h * T + i] = dsum;
     float* acc = ws.dq_acc + base;
     if (anchor) {
-      float qv[EPL];
+      float qv[EPL];  // q~_i: q is the rotated Q here
 #pragma unroll
       for (int e = 0; e < EPL; ++e) qv[e] = __bfloat162float(q[base + e]);
-      rotate_lane(qv, __ldg(pos_id + i));
       float s = 0.f, dp = 0.f;
 #pragma unroll
       for (int e = 0; e < EPL; ++e) {
-        qv[e] = __bfloat162float(__float2bfloat16_rn(qv[e]));
         s = fmaf(qv[e], k0[e], s);
         dp = fmaf(dov[e], v0[e], dp);
       }
@@ -178,13 +179,16 @@ __global__ void __launch_bounds__(128) bwd_prep_kernel(const __nv_bfloat16* __re
 // One CTA per (key tile, kv head), 512 threads:
 //   warp 0      TMA producer: K, V once; Q_i, dO_i through a 2-stage ring
 //   warp 1      TMEM owner and MMA issuer (one thread)
-//   warps 4-7   P/dS group (thread = key row = TMEM lane): P^T packed bf16 into
-//               TMEM for the dV product, dS^T bf16 into shared memory
-//   warps 8-11  dQ group (thread = query row): drains dQ~ from TMEM into the
-//               fp32 accumulator with vector atomics, concurrently with the
-//               next tile's products
-//   warps 12-15 RoPE: K once, every Q tile as it lands
-// TMEM columns: S^T [0,128) (P^T over [0,64)), dP^T [128,256) (dQ~ reuses
+//   warps 2-3   RoPE fused into the K tile load (once per CTA; Q arrives
+//               rotated from the workspace) and staging of each query
+//               tile's LSE*log2(e) and D rows into shared memory
+//   warps 4-11  P/dS: two groups (query columns 0-63 and 64-127), thread = key
+//               row = TMEM lane; P^T packed bf16 into TMEM for the dV product,
+//               dS^T bf16 into shared memory
+//   warps 12-15 dQ drain (thread = query row): dQ~ from TMEM into the fp32
+//               accumulator with vector atomics, concurrently with the next
+//               tile's products
+// TMEM columns: S^T [0,128) (P^T over [0,32) and [64,96)), dP^T [128,256) (dQ~ reuses
 // [128,128+D) once dS is formed), dV [256,256+D), dK~ [256+D,256+2D).
 constexpr int kBwdThreads = 512;
 
@@ -215,6 +219,7 @@ struct BwdParams {
   const WorkItem* items;
   const float2* rope_hi;
   const float2* rope_lo;
+  const float2* rope_step;
   int32_t* err;
   uint64_t wait_limit_ns;
   int T, Hq, Hkv, group, layout;
@@ -226,7 +231,8 @@ __device__ __forceinline__ bool bwd_wait(uint64_t* bar, uint32_t parity, const B
   if (ptx::mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = ptx::global_timer_ns();
   while (true) {
-    if (ptx::mbar_try_wait(bar, parity)) return true;
+    for (int i = 0; i < 64; ++i)
+      if (ptx::mbar_try_wait_sleep(bar, parity, ptx::kSuspendHintNs)) return true;
     if (*abort_flag) return false;
     if (ptx::global_timer_ns() - t0 >= P.wait_limit_ns) {
       atomicCAS(P.err, 0, site);
@@ -265,14 +271,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     ptx::tma_prefetch_desc(&tmV);
     ptx::tma_prefetch_desc(&tmDO);
     ptx::mbar_init(&sm.kv_full, 1);
-    ptx::mbar_init(&sm.k_ready, 128);
+    ptx::mbar_init(&sm.k_ready, 64);
     for (int s = 0; s < 2; ++s) {
       ptx::mbar_init(&sm.qd_full[s], 1);
-      ptx::mbar_init(&sm.q_ready[s], 128);
+      ptx::mbar_init(&sm.q_ready[s], 64);
       ptx::mbar_init(&sm.qd_empty[s], 1);
     }
     ptx::mbar_init(&sm.st_full, 1);
-    ptx::mbar_init(&sm.p_full, 128);
+    ptx::mbar_init(&sm.p_full, 256);
     ptx::mbar_init(&sm.dq_full, 1);
     ptx::mbar_init(&sm.dq_free, 128);
     ptx::mbar_init(&sm.o_full, 1);
@@ -350,8 +356,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         ok = bwd_wait(&sm.p_full, step & 1, P, abort_flag, 414);
         if (!ok) break;
         ptx::tc_fence_after();
-        for (int kk = 0; kk < 8; ++kk)  // dV += P^T dO (P^T from TMEM)
-          ptx::mma_bf16_ts(t_dv, t_s + kk * 8, ptx::smem_desc_sw128(sdo + kk * 2048, 16384, 1024), idesc_kd,
+        for (int kk = 0; kk < 8; ++kk)  // dV += P^T dO (P^T from TMEM: q 0-63 at cols 0-31, 64-127 at 64-95)
+          ptx::mma_bf16_ts(t_dv, t_s + (kk < 4 ? kk * 8 : 64 + (kk - 4) * 8),
+                           ptx::smem_desc_sw128(sdo + kk * 2048, 16384, 1024), idesc_kd,
                            (step > 0 || kk > 0) ? 1u : 0u);
         for (int kk = 0; kk < 8; ++kk) {  // dK~ += dS^T Q~
           const uint32_t aoff = (kk >> 2) * 16384 + (kk & 3) * 32;
@@ -368,9 +375,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       ptx::mma_commit(&sm.drain);
       ptx::mbar_wait(&sm.drain, 0, kDrainLimitNs, P.err, 419);
     }
-  } else if (warp >= 4 && warp < 8) {
+  } else if (warp >= 4 && warp < 12) {
     // ------------------------------------------------------------ P / dS
     const int r = tid & 127;
+    const int cq = (warp - 4) >> 2;  // query columns [64 cq, 64 cq + 64)
     const int j = kt * kTile + r;
     const bool key_valid = j < P.T;
     const int jhi = key_valid ? __ldg(P.key_hi + j) : -1;  // rows [j, jhi] see key j
@@ -387,7 +395,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const float4* lse_s = reinterpret_cast<const float4*>(sm.lse2[s]);
       const float4* d_s = reinterpret_cast<const float4*>(sm.dsum[s]);
 #pragma unroll 1
-      for (int c = 0; c < 4; ++c) {
+      for (int c = 2 * cq; c < 2 * cq + 2; ++c) {
         float sv[32], dpv[32];
         ptx::tmem_ld32(t_s + lane_off + c * 32, sv);
         ptx::tmem_ld32(t_dp + lane_off + c * 32, dpv);
@@ -418,7 +426,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             pw[e / 2] = ptx::pack_bf16x2(p0, p1);
             dw[e / 2] = ptx::pack_bf16x2(p0 * (dpv[x] - dd[e]), p1 * (dpv[x + 1] - dd[e + 1]));
           }
-          ptx::tmem_st4(t_s + lane_off + c * 16 + gq * 4, pw);
+          // P^T packs over S^T columns this group has already read: query
+          // columns [64 cq, 64 cq + 64) land in TMEM columns [64 cq, 64 cq + 32)
+          ptx::tmem_st4(t_s + lane_off + 64 * cq + (c - 2 * cq) * 16 + gq * 4, pw);
           const int c8 = c * 4 + gq;  // 16-byte chunk along the 128 query columns
           *reinterpret_cast<uint4*>(sm.dst[c8 >> 3] + sw128_chunk(r, c8 & 7)) = make_uint4(dw[0], dw[1], dw[2], dw[3]);
         }
@@ -428,8 +438,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       ptx::tc_fence_before();
       ptx::mbar_arrive(&sm.p_full);
     }
-    if (ok) ok = bwd_wait(&sm.o_full, 0, P, abort_flag, 423);
-    if (ok) {
+    if (ok && cq == 0) ok = bwd_wait(&sm.o_full, 0, P, abort_flag, 423);
+    if (ok && cq == 0) {
       // ---- epilogue: dV and dk = R^T (scale dK~) for this thread's key row
       ptx::tc_fence_after();
       __nv_bfloat16* dvrow = P.dv + ((size_t)(key_valid ? j : 0) * P.Hkv + g) * HD;
@@ -490,7 +500,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         }
       }
     }
-  } else if (warp >= 8 && warp < 12) {
+  } else if (warp >= 12) {
     // ------------------------------------------------------------ dQ drain
     const int r = tid & 127;
     const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
@@ -516,26 +526,31 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       ptx::tc_fence_before();
       ptx::mbar_arrive(&sm.dq_free);
     }
-  } else if (warp >= 12) {
-    // ------------------------------------------------------------ RoPE
-    const int r = tid & 127;
+  } else if (warp == 2 || warp == 3) {
+    // ------------------------------------------------------------ RoPE + LSE/D staging
+    const int t = tid - 64;
+    const bool rot = P.layout != 2;
+    RopeUnits<HD, 64> ru;
+    if (rot) ru.begin(kt * kTile, P.T, P.pos_id, false, P.rope_hi, P.rope_lo, t);
     bool ok = bwd_wait(&sm.kv_full, 0, P, abort_flag, 441);
     if (ok) {
-      const int j = kt * kTile + r;
-      if (j < P.T) rope_row_smem<HD>(sm.k[0], r, __ldg(P.pos_id + j), P.layout, false, P.rope_hi, P.rope_lo);
+      if (rot) {
+        rope_smem_tile<HD, 64>(ru, sm.k[0], P.layout, P.rope_hi, P.rope_lo, P.rope_step, t);
+      }
       ptx::fence_proxy_async_smem();
       ptx::mbar_arrive(&sm.k_ready);
     }
     for (int step = 0; step < n_steps && ok; ++step) {
       const int s = step & 1;
+      const int i0 = step_qt(step) * kTile;
       ok = bwd_wait(&sm.qd_full[s], (step >> 1) & 1, P, abort_flag, 442);
       if (!ok) break;
-      const int i = step_qt(step) * kTile + r;
       const size_t hrow = (size_t)step_head(step) * P.T;
-      sm.lse2[s][r] = i < P.T ? __ldg(P.lse + hrow + i) * kLog2e : INFINITY;
-      sm.dsum[s][r] = i < P.T ? __ldg(P.ws.dsum + hrow + i) : 0.f;
-      if (i < P.T) rope_row_smem<HD>(sm.q[s][0], r, __ldg(P.pos_id + i), P.layout, false, P.rope_hi, P.rope_lo);
-      ptx::fence_proxy_async_smem();
+      for (int r = t; r < kTile; r += 64) {
+        const int i = i0 + r;
+        sm.lse2[s][r] = i < P.T ? __ldg(P.lse + hrow + i) * kLog2e : INFINITY;
+        sm.dsum[s][r] = i < P.T ? __ldg(P.ws.dsum + hrow + i) : 0.f;
+      }
       ptx::mbar_arrive(&sm.q_ready[s]);
     }
   }
@@ -634,8 +649,16 @@ aa_status launch_bwd(aa_plan_s* p, const void* q, const void* k, const void* v, 
   Workspace ws = carve(workspace, p, &need);
   cudaError_t e;
   const int rope_layout = p->cfg.rope_layout;
+  // Q is the streaming operand of the key-stationary tile loop: rotate it
+  // once here rather than on every visit
+  const void* qr = q;
+  if (rope_layout != AA_ROPE_NONE) {
+    aa_status rs = launch_rope(p, q, ws.qr, p->Hq, 0, s);
+    if (rs != AA_OK) return rs;
+    qr = ws.qr;
+  }
   bwd_prep_kernel<HD><<<dim3(kPrepChunks, p->Hq), 128, 0, s>>>(
-      static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(k),
+      static_cast<const __nv_bfloat16*>(qr), static_cast<const __nv_bfloat16*>(k),
       static_cast<const __nv_bfloat16*>(v), static_cast<const __nv_bfloat16*>(o),
       static_cast<const __nv_bfloat16*>(dout), lse, ws, p->dev.pos_id, p->dev.rope_hi, p->dev.rope_lo, p->T, p->Hq,
       p->group, rope_layout, p->anchor ? 1 : 0, p->scale);
@@ -643,7 +666,7 @@ aa_status launch_bwd(aa_plan_s* p, const void* q, const void* k, const void* v, 
 
   CUtensorMap tq, tk, tv, tdo;
   aa_status st;
-  if ((st = make_tile_map(&tq, q, p->T, p->Hq, HD)) != AA_OK) return st;
+  if ((st = make_tile_map(&tq, qr, p->T, p->Hq, HD)) != AA_OK) return st;
   if ((st = make_tile_map(&tk, k, p->T, p->Hkv, HD)) != AA_OK) return st;
   if ((st = make_tile_map(&tv, v, p->T, p->Hkv, HD)) != AA_OK) return st;
   if ((st = make_tile_map(&tdo, dout, p->T, p->Hq, HD)) != AA_OK) return st;
@@ -657,6 +680,7 @@ aa_status launch_bwd(aa_plan_s* p, const void* q, const void* k, const void* v, 
   P.items = p->dev.bwd_items;
   P.rope_hi = p->dev.rope_hi;
   P.rope_lo = p->dev.rope_lo;
+  P.rope_step = p->dev.rope_step;
   P.err = p->dev.err;
   P.wait_limit_ns = p->wait_limit_ns;
   P.T = p->T;

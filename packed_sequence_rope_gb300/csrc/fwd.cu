@@ -8,14 +8,17 @@
 //   LSE_i = ln sum_{j visible} exp(scale * (R_i q_i).(R_j k_j))
 // with the visible set {0} U [row_lo_i, i] (ANCHOR) or [row_lo_i, i].
 //
-// How. One CTA per (pair of 128-row query tiles, head), longest work first.
-// Warp roles (512 threads):
-//   warp 0      TMA producer: Q0/Q1 once, then K/V tiles through a 2-stage ring
+// How. K is rotated once per call by the standalone RoPE kernel into the
+// workspace (every query tile of a document re-reads it; rotating it on each
+// visit would cost as much CUDA-core work as the softmax). One CTA then runs
+// per (pair of 128-row query tiles, head), longest work first, 384 threads:
+//   warp 0      TMA producer: Q0/Q1 once, then rotated K / V tiles through a
+//               2-stage ring
 //   warp 1      TMEM owner and MMA issuer (one thread)
-//   warps 4-7   softmax for query tile 0 (thread = query row = TMEM lane)
-//   warps 8-11  softmax for query tile 1
-//   warps 12-15 RoPE: rotate Q0/Q1 once and every K tile once (fp32, rounded
-//               to bf16 in place), shared by both query tiles
+//   warps 4-7   query tile 0: rotates Q0 in shared memory as it lands (RoPE
+//               fused into the Q tile load), then its online softmax
+//               (thread = query row = TMEM lane)
+//   warps 8-11  the same for query tile 1
 // Tensor-memory columns: S0 [0,128) S1 [128,256) O0, O1 (D columns each). The
 // softmax writes P as packed bf16 over the first 64 columns of its S, and the
 // PV product reads it straight from TMEM (tcgen05.mma with A in TMEM).
@@ -33,7 +36,7 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: O is rescaled only when the max grows by > 2^8
 constexpr uint64_t kDrainLimitNs = 1000000000ull;
 constexpr int kStages = 2;
-constexpr int kThreads = 512;
+constexpr int kThreads = 384;
 
 template <int HD>
 struct FwdSmem {
@@ -41,17 +44,15 @@ struct FwdSmem {
   alignas(1024) uint8_t q[2][kB][16384];
   alignas(1024) uint8_t k[kStages][kB][16384];
   alignas(1024) uint8_t v[kStages][kB][16384];
-  float k0[HD];  // rotated anchor key (bf16-rounded)
-  float v0[HD];  // anchor value
-  uint64_t q_full, q_ready;
-  uint64_t kv_full[kStages], k_ready[kStages], kv_empty[kStages];
+  uint64_t q_full, q_ready[2];
+  uint64_t kv_full[kStages], kv_empty[kStages];
   uint64_t s_full[2], p_full[2], o_full, drain;
   uint32_t tmem_base;
   int abort_flag;
 };
 
 struct FwdParams {
-  const __nv_bfloat16* k;
+  const __nv_bfloat16* kr;  // rotated K [T, Hkv, D] (or K itself without RoPE)
   const __nv_bfloat16* v;
   __nv_bfloat16* o;
   float* lse;
@@ -61,6 +62,7 @@ struct FwdParams {
   const WorkItem* items;
   const float2* rope_hi;
   const float2* rope_lo;
+  const float2* rope_step;
   int32_t* err;
   uint64_t wait_limit_ns;
   int T, Hq, Hkv, group, layout, anchor, n_tiles;
@@ -73,7 +75,8 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, co
   if (ptx::mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = ptx::global_timer_ns();
   while (true) {
-    if (ptx::mbar_try_wait(bar, parity)) return true;
+    for (int i = 0; i < 64; ++i)
+      if (ptx::mbar_try_wait_sleep(bar, parity, ptx::kSuspendHintNs)) return true;
     if (*abort_flag) return false;
     if (ptx::global_timer_ns() - t0 >= P.wait_limit_ns) {
       atomicCAS(P.err, 0, site);
@@ -111,10 +114,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::tma_prefetch_desc(&tmK);
     ptx::tma_prefetch_desc(&tmV);
     ptx::mbar_init(&sm.q_full, 1);
-    ptx::mbar_init(&sm.q_ready, 128);
+    ptx::mbar_init(&sm.q_ready[0], 128);
+    ptx::mbar_init(&sm.q_ready[1], 128);
     for (int s = 0; s < kStages; ++s) {
       ptx::mbar_init(&sm.kv_full[s], 1);
-      ptx::mbar_init(&sm.k_ready[s], 128);
       ptx::mbar_init(&sm.kv_empty[s], 1);
     }
     for (int t = 0; t < 2; ++t) {
@@ -185,12 +188,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         first_pv[t] = false;
         return true;
       };
-      bool ok = wait_or_abort(&sm.q_ready, 0, P, abort_flag, 312);
+      bool ok = wait_or_abort(&sm.q_ready[0], 0, P, abort_flag, 312);
+      if (ok && has1) ok = wait_or_abort(&sm.q_ready[1], 0, P, abort_flag, 312);
       int pend1 = -1;  // stage whose PV1 is still to be issued
       int it = 0;
       for (int kt = kt_lo; kt <= kt_hi && ok; ++kt, ++it) {
         const int s = it % kStages;
-        ok = wait_or_abort(&sm.k_ready[s], (it / kStages) & 1, P, abort_flag, 313);
+        ok = wait_or_abort(&sm.kv_full[s], (it / kStages) & 1, P, abort_flag, 313);
         if (!ok) break;
         ptx::tc_fence_after();
         const bool in0 = kt >= lo0 && kt <= hi0, in1 = kt >= lo1 && kt <= hi1;
@@ -231,11 +235,37 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
     const uint32_t t_s = tmem + 128 * t + lane_off, t_o = tmem + 256 + HD * t + lane_off;
     float m = -INFINITY, l = 0.f, s0 = 0.f;
+    // RoPE fused into the Q tile load: rotate this group's tile in shared
+    // memory (table reads issued before the copy lands)
+    const bool rot = P.layout != 2;
+    RopeUnits<HD, 128> rq;
+    if (tile_exists && rot) rq.begin((qt0 + t) * kTile, P.T, P.pos_id, false, P.rope_hi, P.rope_lo, r);
     bool ok = tile_exists;
-    if (ok) ok = wait_or_abort(&sm.q_ready, 0, P, abort_flag, 321);
+    if (ok) ok = wait_or_abort(&sm.q_full, 0, P, abort_flag, 321);
+    if (ok && rot) rope_smem_tile<HD, 128>(rq, sm.q[t][0], P.layout, P.rope_hi, P.rope_lo, P.rope_step, r);
+    // every row of the tile is rotated before the MMA or the anchor dot reads it
+    if (t == 0) asm volatile("bar.sync 1, 128;" ::: "memory");
+    else asm volatile("bar.sync 2, 128;" ::: "memory");
+    if (ok) {
+      ptx::fence_proxy_async_smem();
+      ptx::mbar_arrive(&sm.q_ready[t]);
+    }
     if (ok && P.anchor) {
+      // s_i0 = q~_i . k~_0 with the rotated anchor key from the workspace
+      const uint4* k0 = reinterpret_cast<const uint4*>(P.kr + (size_t)g * HD);
       float acc = 0.f;
-      for (int c = 0; c < HD; ++c) acc = fmaf(tile_elem(sm.q[t][0], r, c), sm.k0[c], acc);
+#pragma unroll 4
+      for (int c8 = 0; c8 < HD / 8; ++c8) {
+        const uint4 kq = __ldg(k0 + c8);
+        const uint4 qq = *reinterpret_cast<const uint4*>(sm.q[t][0] + (c8 >> 3) * 16384 + sw128_chunk(r, c8 & 7));
+        const uint32_t ka[4] = {kq.x, kq.y, kq.z, kq.w}, qa[4] = {qq.x, qq.y, qq.z, qq.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float2 kf = ptx::unpack_bf16x2(ka[e]), qf = ptx::unpack_bf16x2(qa[e]);
+          acc = fmaf(qf.x, kf.x, acc);
+          acc = fmaf(qf.y, kf.y, acc);
+        }
+      }
       s0 = acc * sl2;
       m = s0;
       l = 1.f;
@@ -336,8 +366,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint32_t w[16];
 #pragma unroll
           for (int e = 0; e < 16; ++e) {
-            const float a = (ov[2 * e] + w0 * sm.v0[c * 32 + 2 * e]) * inv_l;
-            const float b = (ov[2 * e + 1] + w0 * sm.v0[c * 32 + 2 * e + 1]) * inv_l;
+            float2 v0 = make_float2(0.f, 0.f);
+            if (P.anchor) v0 = ptx::unpack_bf16x2(__ldg(reinterpret_cast<const uint32_t*>(P.v + (size_t)g * HD + c * 32) + e));
+            const float a = (ov[2 * e] + w0 * v0.x) * inv_l;
+            const float b = (ov[2 * e + 1] + w0 * v0.y) * inv_l;
             w[e] = ptx::pack_bf16x2(a, b);
           }
           uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
@@ -346,45 +378,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       if (row_valid) P.lse[(size_t)h * P.T + i] = (m + log2f(l)) * 0.69314718055994531f;
-    }
-  } else if (warp >= 12) {
-    // ------------------------------------------------------------ RoPE
-    const int r = tid & 127;
-    if (P.anchor && r < HD / 2) {
-      const int pos0 = __ldg(P.pos_id);
-      const __nv_bfloat16* k0 = P.k + (size_t)g * HD;
-      const __nv_bfloat16* v0 = P.v + (size_t)g * HD;
-      int ia, ib;
-      if (P.layout == 1) { ia = r; ib = r + HD / 2; } else { ia = 2 * r; ib = 2 * r + 1; }
-      float x = __bfloat162float(k0[ia]), y = __bfloat162float(k0[ib]);
-      if (P.layout != 2) {
-        const float2 cs = rope_cs(P.rope_hi, P.rope_lo, pos0, r, HD / 2);
-        rope_pair(x, y, cs.x, cs.y);
-      }
-      sm.k0[ia] = __bfloat162float(__float2bfloat16_rn(x));
-      sm.k0[ib] = __bfloat162float(__float2bfloat16_rn(y));
-      sm.v0[ia] = __bfloat162float(v0[ia]);
-      sm.v0[ib] = __bfloat162float(v0[ib]);
-    }
-    bool ok = wait_or_abort(&sm.q_full, 0, P, abort_flag, 331);
-    if (ok) {
-      for (int t = 0; t < (has1 ? 2 : 1); ++t) {
-        const int i = (qt0 + t) * kTile + r;
-        if (i < P.T) rope_row_smem<HD>(sm.q[t][0], r, __ldg(P.pos_id + i), P.layout, false, P.rope_hi, P.rope_lo);
-      }
-      // q_ready also publishes the anchor key/value rows written above
-      ptx::fence_proxy_async_smem();
-      ptx::mbar_arrive(&sm.q_ready);
-    }
-    int it = 0;
-    for (int kt = kt_lo; kt <= kt_hi && ok; ++kt, ++it) {
-      const int s = it % kStages;
-      ok = wait_or_abort(&sm.kv_full[s], (it / kStages) & 1, P, abort_flag, 332);
-      if (!ok) break;
-      const int j = kt * kTile + r;
-      if (j < P.T) rope_row_smem<HD>(sm.k[s][0], r, __ldg(P.pos_id + j), P.layout, false, P.rope_hi, P.rope_lo);
-      ptx::fence_proxy_async_smem();
-      ptx::mbar_arrive(&sm.k_ready[s]);
     }
   }
 
@@ -395,14 +388,19 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 template <int HD>
 aa_status launch_fwd(aa_plan_s* p, const void* q, const void* k, const void* v, void* o, float* lse,
-                     cudaStream_t s) {
+                     void* workspace, cudaStream_t s) {
   CUtensorMap tq, tk, tv;
   aa_status st;
+  const void* kr = k;
+  if (p->cfg.rope_layout != AA_ROPE_NONE) {
+    if ((st = launch_rope(p, k, workspace, p->Hkv, 0, s)) != AA_OK) return st;
+    kr = workspace;
+  }
   if ((st = make_tile_map(&tq, q, p->T, p->Hq, HD)) != AA_OK) return st;
-  if ((st = make_tile_map(&tk, k, p->T, p->Hkv, HD)) != AA_OK) return st;
+  if ((st = make_tile_map(&tk, kr, p->T, p->Hkv, HD)) != AA_OK) return st;
   if ((st = make_tile_map(&tv, v, p->T, p->Hkv, HD)) != AA_OK) return st;
   FwdParams P;
-  P.k = static_cast<const __nv_bfloat16*>(k);
+  P.kr = static_cast<const __nv_bfloat16*>(kr);
   P.v = static_cast<const __nv_bfloat16*>(v);
   P.o = static_cast<__nv_bfloat16*>(o);
   P.lse = lse;
@@ -412,6 +410,7 @@ aa_status launch_fwd(aa_plan_s* p, const void* q, const void* k, const void* v, 
   P.items = p->dev.fwd_items;
   P.rope_hi = p->dev.rope_hi;
   P.rope_lo = p->dev.rope_lo;
+  P.rope_step = p->dev.rope_step;
   P.err = p->dev.err;
   P.wait_limit_ns = p->wait_limit_ns;
   P.T = p->T;
@@ -436,13 +435,25 @@ aa_status launch_fwd(aa_plan_s* p, const void* q, const void* k, const void* v, 
 
 using namespace aa;
 
+extern "C" size_t aa_fwd_workspace_bytes(aa_plan_t p) {
+  if (!p || p->cfg.rope_layout == AA_ROPE_NONE) return 0;
+  return ((size_t)p->T * p->Hkv * p->D * 2 + 255) & ~size_t(255);
+}
+
 extern "C" aa_status aa_fwd(aa_plan_t p, const void* q, const void* k, const void* v, void* o, float* lse,
-                            aa_stream_t stream) {
+                            void* workspace, size_t workspace_bytes, aa_stream_t stream) {
   aa_status st = check_compute_plan(p);
   if (st != AA_OK) return st;
   if (!q || !k || !v || !o || !lse) return fail(AA_ERR_INVALID_ARG, "NULL tensor pointer");
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
     return fail(AA_ERR_INVALID_ARG, "tensors must be 16-byte aligned");
+  const size_t need = aa_fwd_workspace_bytes(p);
+  if (need > 0) {
+    if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+      return fail(AA_ERR_INVALID_ARG, "workspace must be a 256-byte aligned device pointer");
+    if (workspace_bytes < need) return fail(AA_ERR_INVALID_ARG, "workspace is smaller than aa_fwd_workspace_bytes()");
+  }
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  return p->D == 128 ? launch_fwd<128>(p, q, k, v, o, lse, s) : launch_fwd<64>(p, q, k, v, o, lse, s);
+  return p->D == 128 ? launch_fwd<128>(p, q, k, v, o, lse, workspace, s)
+                     : launch_fwd<64>(p, q, k, v, o, lse, workspace, s);
 }

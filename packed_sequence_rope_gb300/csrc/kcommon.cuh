@@ -93,6 +93,205 @@ __device__ __forceinline__ void rope_row_smem(uint8_t* tile, int r, int pos, int
   }
 }
 
+// ---------------------------------------------------------------- tile RoPE
+// Canonical rotation of a 128-row tile. Work unit = (quad qd of 4 consecutive
+// pairs, 16-row group g). The group's first row, and any row whose position
+// does not follow its predecessor's (a document start), take (cos, sin) from
+// the two-level tables; the other rows advance each pair's angle by one
+// theta_p with an exact complex product by (cos theta_p, sin theta_p). Over at
+// most 15 steps the drift stays near 1e-6 of the pair's magnitude, far below
+// the bf16 rounding of the result. Every kernel that rotates a tile (and
+// aa_rope_apply) runs this same unit decomposition and arithmetic, so fused
+// and standalone rotation agree bit for bit.
+//
+// Usage: RopeUnits<HD, NT> st; st.begin(...) loads the positions and the
+// group-start (cos, sin) values (issue it before waiting for the tile's data
+// to hide their latency); st.run(tile, ...) then rotates in place.
+// Tile accessors provide load4(r, qd, x[4], y[4]) / store4(r, qd, x, y) for
+// the 4 pairs of quad qd in tile row r. NT threads (a multiple of 32) with ids
+// t share the NU = HD/8 * 8 units.
+template <int HD, int NT>
+struct RopeUnits {
+  static constexpr int NQ = HD / 8;      // quads per row
+  static constexpr int NU = NQ * 8;      // units per tile
+  static constexpr int UPT = (NU + NT - 1) / NT;
+  static constexpr int RPL = 16 / NQ;    // positions each lane holds for its group
+  int pos[UPT][RPL];                     // positions of this lane's slice of its group's rows
+  float c0[UPT][4], s0[UPT][4];          // (cos, sin) at the group's first row
+
+  __device__ __forceinline__ void begin(int row0, int T, const int32_t* __restrict__ pos_id, bool inverse,
+                                        const float2* __restrict__ hi_tab, const float2* __restrict__ lo_tab, int t) {
+    const int lane = t & 31;
+#pragma unroll
+    for (int k = 0; k < UPT; ++k) {
+      const int u = t + k * NT;
+      const int qd = u % NQ, g = u / NQ;
+#pragma unroll
+      for (int m = 0; m < RPL; ++m) {
+        const int row = row0 + g * 16 + (lane % NQ) + m * NQ;
+        pos[k][m] = (u < NU && row < T) ? __ldg(pos_id + row) : -1;
+      }
+      const int p0 = (u < NU && row0 + g * 16 < T) ? __ldg(pos_id + row0 + g * 16) : 0;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float2 cs = rope_cs(hi_tab, lo_tab, p0, qd * 4 + e, HD / 2);
+        c0[k][e] = cs.x;
+        s0[k][e] = inverse ? -cs.y : cs.y;
+      }
+    }
+  }
+
+  // Rotates each unit in two batches of 8 rows, each in three phases so the
+  // row loads are in flight together: load, rotate in registers, store.
+  template <class Tile>
+  __device__ __forceinline__ void run(Tile& tile, bool inverse, const float2* __restrict__ hi_tab,
+                                      const float2* __restrict__ lo_tab, const float2* __restrict__ step_tab,
+                                      int t) const {
+    const int lane = t & 31;
+    const int gl = lane & ~(NQ - 1);  // first lane of this lane's group
+#pragma unroll
+    for (int k = 0; k < UPT; ++k) {
+      const int u = t + k * NT;
+      const int qd = u % NQ, g = u / NQ;
+      const bool unit_ok = u < NU;
+      float sc[4], ss[4], c[4], s[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float2 st = __ldg(step_tab + qd * 4 + e);
+        sc[e] = st.x;
+        ss[e] = inverse ? -st.y : st.y;
+        c[e] = c0[k][e];
+        s[e] = s0[k][e];
+      }
+      int prev = -2;
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {  // two batches of 8 rows
+        int pr[8];
+#pragma unroll
+        for (int r = 0; r < 8; ++r) {
+          const int rr = half * 8 + r;
+          pr[r] = __shfl_sync(0xffffffffu, pos[k][rr / NQ], gl + (rr % NQ));
+        }
+        typename Tile::Raw raw[8];
+#pragma unroll
+        for (int r = 0; r < 8; ++r)
+          if (unit_ok && pr[r] >= 0) raw[r] = tile.load_raw(g * 16 + half * 8 + r, qd);
+#pragma unroll
+        for (int r = 0; r < 8; ++r) {
+          if (!unit_ok || pr[r] < 0) continue;
+          if (half * 8 + r > 0) {
+            if (pr[r] == prev + 1) {
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const float nc = __fmaf_rn(c[e], sc[e], -__fmul_rn(s[e], ss[e]));
+                const float ns = __fmaf_rn(s[e], sc[e], __fmul_rn(c[e], ss[e]));
+                c[e] = nc;
+                s[e] = ns;
+              }
+            } else {
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const float2 cs = rope_cs(hi_tab, lo_tab, pr[r], qd * 4 + e, HD / 2);
+                c[e] = cs.x;
+                s[e] = inverse ? -cs.y : cs.y;
+              }
+            }
+          }
+          prev = pr[r];
+          float x[4], y[4];
+          Tile::unpack(raw[r], x, y);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) rope_pair(x[e], y[e], c[e], s[e]);
+          raw[r] = Tile::pack(x, y);
+        }
+#pragma unroll
+        for (int r = 0; r < 8; ++r)
+          if (unit_ok && pr[r] >= 0) tile.store_raw(g * 16 + half * 8 + r, qd, raw[r]);
+      }
+    }
+  }
+};
+
+// Packing of one quad (4 pairs) for the two pair layouts: layout 0 keeps
+// (2p, 2p+1) interleaved in 16 bytes; layout 1 holds the 4 first-half and the
+// 4 second-half elements as two 8-byte words.
+struct QuadRaw {
+  uint4 w;
+};
+__device__ __forceinline__ void quad_unpack(int layout, const QuadRaw& q, float* x, float* y) {
+  const uint32_t u[4] = {q.w.x, q.w.y, q.w.z, q.w.w};
+  if (layout == 0) {
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float2 v = ptx::unpack_bf16x2(u[e]);
+      x[e] = v.x;
+      y[e] = v.y;
+    }
+  } else {
+    const float2 a0 = ptx::unpack_bf16x2(u[0]), a1 = ptx::unpack_bf16x2(u[1]);
+    const float2 b0 = ptx::unpack_bf16x2(u[2]), b1 = ptx::unpack_bf16x2(u[3]);
+    x[0] = a0.x; x[1] = a0.y; x[2] = a1.x; x[3] = a1.y;
+    y[0] = b0.x; y[1] = b0.y; y[2] = b1.x; y[3] = b1.y;
+  }
+}
+__device__ __forceinline__ QuadRaw quad_pack(int layout, const float* x, const float* y) {
+  QuadRaw q;
+  if (layout == 0)
+    q.w = make_uint4(ptx::pack_bf16x2(x[0], y[0]), ptx::pack_bf16x2(x[1], y[1]), ptx::pack_bf16x2(x[2], y[2]),
+                     ptx::pack_bf16x2(x[3], y[3]));
+  else
+    q.w = make_uint4(ptx::pack_bf16x2(x[0], x[1]), ptx::pack_bf16x2(x[2], x[3]), ptx::pack_bf16x2(y[0], y[1]),
+                     ptx::pack_bf16x2(y[2], y[3]));
+  return q;
+}
+
+// Tile accessor over a [128][HD] bf16 tile in shared memory (HD/64 swizzled
+// 16 KB blocks). layout 0: pair p = elements (2p, 2p+1); layout 1: (p, p+HD/2).
+// The layout is a template parameter of the unpack/pack pair through `L`.
+template <int HD, int L>
+struct SmemTile {
+  using Raw = QuadRaw;
+  uint8_t* base;
+  __device__ __forceinline__ static uint32_t elem_off(int r, int e) {
+    return (uint32_t)((e >> 6) * 16384) + sw128_chunk(r, (e & 63) >> 3) + (uint32_t)((e & 7) * 2);
+  }
+  __device__ __forceinline__ QuadRaw load_raw(int r, int qd) const {
+    QuadRaw q;
+    if (L == 0) {
+      q.w = *reinterpret_cast<const uint4*>(base + (qd >> 3) * 16384 + sw128_chunk(r, qd & 7));
+    } else {
+      const uint2 a = *reinterpret_cast<const uint2*>(base + elem_off(r, 4 * qd));
+      const uint2 b = *reinterpret_cast<const uint2*>(base + elem_off(r, HD / 2 + 4 * qd));
+      q.w = make_uint4(a.x, a.y, b.x, b.y);
+    }
+    return q;
+  }
+  __device__ __forceinline__ void store_raw(int r, int qd, const QuadRaw& q) const {
+    if (L == 0) {
+      *reinterpret_cast<uint4*>(base + (qd >> 3) * 16384 + sw128_chunk(r, qd & 7)) = q.w;
+    } else {
+      *reinterpret_cast<uint2*>(base + elem_off(r, 4 * qd)) = make_uint2(q.w.x, q.w.y);
+      *reinterpret_cast<uint2*>(base + elem_off(r, HD / 2 + 4 * qd)) = make_uint2(q.w.z, q.w.w);
+    }
+  }
+  __device__ __forceinline__ static void unpack(const QuadRaw& q, float* x, float* y) { quad_unpack(L, q, x, y); }
+  __device__ __forceinline__ static QuadRaw pack(const float* x, const float* y) { return quad_pack(L, x, y); }
+};
+
+// Rotate a [128][HD] shared-memory tile with the layout chosen at run time.
+template <int HD, int NT>
+__device__ __forceinline__ void rope_smem_tile(const RopeUnits<HD, NT>& st, uint8_t* base, int layout,
+                                               const float2* hi_tab, const float2* lo_tab,
+                                               const float2* step_tab, int t) {
+  if (layout == 0) {
+    SmemTile<HD, 0> tile{base};
+    st.run(tile, false, hi_tab, lo_tab, step_tab, t);
+  } else if (layout == 1) {
+    SmemTile<HD, 1> tile{base};
+    st.run(tile, false, hi_tab, lo_tab, step_tab, t);
+  }
+}
+
 // Read element `c` of row `r` of a swizzled [128][HD] bf16 tile.
 __device__ __forceinline__ float tile_elem(const uint8_t* tile, int r, int c) {
   const __nv_bfloat16* p = reinterpret_cast<const __nv_bfloat16*>(

@@ -155,6 +155,9 @@ static void build_rope_tables(aa_plan_s* p) {
       const double ang = (double)h * kRopeSplit * theta[i];
       p->rope_hi[(size_t)h * half + i] = make_float2((float)std::cos(ang), (float)std::sin(ang));
     }
+  p->rope_step.resize(half);
+  for (int i = 0; i < half; ++i)
+    p->rope_step[i] = make_float2((float)std::cos(theta[i]), (float)std::sin(theta[i]));
   for (int i = 0; i < half; ++i)
     for (int l = 0; l < kRopeSplit; ++l) {
       const double ang = (double)l * theta[i];
@@ -180,7 +183,8 @@ static aa_status upload(T** dst, const std::vector<T>& src, cudaStream_t s, cons
 
 static void free_device(aa_plan_s* p) {
   DevicePlan& d = p->dev;
-  void* ptrs[] = {d.pos_id, d.row_lo, d.key_hi, d.fwd_items, d.bwd_items, d.qtile_klo, d.rope_hi, d.rope_lo, d.err};
+  void* ptrs[] = {d.pos_id, d.row_lo, d.key_hi, d.fwd_items, d.bwd_items, d.qtile_klo,
+                  d.rope_hi, d.rope_lo, d.rope_step, d.err};
   for (void* q : ptrs)
     if (q) cudaFree(q);
   d = DevicePlan{};
@@ -264,6 +268,7 @@ extern "C" aa_status aa_plan(const aa_config* cfg, const int32_t* cu_doclens_hos
       (st = upload(&d.qtile_klo, p->qtile_klo, s, "query-tile key ranges")) != AA_OK ||
       (st = upload(&d.rope_hi, p->rope_hi, s, "rope table (hi)")) != AA_OK ||
       (st = upload(&d.rope_lo, p->rope_lo, s, "rope table (lo)")) != AA_OK ||
+      (st = upload(&d.rope_step, p->rope_step, s, "rope step table")) != AA_OK ||
       (st = upload(&d.err, zero, s, "error word")) != AA_OK) {
     cudaStreamSynchronize(s);
     free_device(p);

@@ -3,9 +3,9 @@
 // fp32 rotation then a cast to bf16 as in §3.2 "Big-Picture Architecture")
 // and the host-side TMA descriptor helper.
 //
-// HBM-bound: one read and one write of x. Each thread rotates four pairs
-// (16 bytes of bf16 for the adjacent layout), grid-strided over the whole
-// tensor with a grid sized to the SM count.
+// HBM-bound: one read and one write of x, one CTA per (128-row tile, head),
+// with the same per-tile arithmetic as the rotation fused into the attention
+// kernels' tile loads (so the two agree bit for bit).
 #include <cudaTypedefs.h>
 
 #include <mutex>
@@ -14,53 +14,64 @@
 
 namespace aa {
 
-__global__ void __launch_bounds__(256) rope_apply_kernel(const __nv_bfloat16* __restrict__ x,
-                                                         __nv_bfloat16* __restrict__ y,
-                                                         const int32_t* __restrict__ pos_id,
-                                                         const float2* __restrict__ hi_tab,
-                                                         const float2* __restrict__ lo_tab, int64_t T, int H,
-                                                         int D, int layout, int inverse) {
-  const int half = D / 2;
-  const int quads = half / 4;  // groups of 4 pairs per (token, head)
-  const int64_t n = T * H * quads;
-  for (int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; idx < n;
-       idx += (int64_t)gridDim.x * blockDim.x) {
-    const int qd = (int)(idx % quads);
-    const int64_t row = idx / quads;  // token * H + head
-    const int t = (int)(row / H);
-    const int pos = __ldg(pos_id + t);
-    const __nv_bfloat16* xr = x + row * D;
-    __nv_bfloat16* yr = y + row * D;
-    if (layout == 0) {
-      uint4 w = *reinterpret_cast<const uint4*>(xr + qd * 8);
-      uint32_t* u = reinterpret_cast<uint32_t*>(&w);
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        float2 cs = rope_cs(hi_tab, lo_tab, pos, qd * 4 + e, half);
-        if (inverse) cs.y = -cs.y;
-        float2 v = ptx::unpack_bf16x2(u[e]);
-        rope_pair(v.x, v.y, cs.x, cs.y);
-        u[e] = ptx::pack_bf16x2(v.x, v.y);
-      }
-      *reinterpret_cast<uint4*>(yr + qd * 8) = w;
+// Accessor over one head of a [T, H, D] bf16 tensor in global memory, rows
+// relative to a 128-row tile; reads from x, writes to y (which may equal x).
+template <int HD, int L>
+struct GlobalTile {
+  using Raw = QuadRaw;
+  const __nv_bfloat16* x;
+  __nv_bfloat16* y;
+  int row0, H, head;
+  __device__ __forceinline__ size_t off(int r, int e) const { return ((size_t)(row0 + r) * H + head) * HD + e; }
+  __device__ __forceinline__ QuadRaw load_raw(int r, int qd) const {
+    QuadRaw q;
+    if (L == 0) {
+      q.w = *reinterpret_cast<const uint4*>(x + off(r, 8 * qd));
     } else {
-      uint2 wa = *reinterpret_cast<const uint2*>(xr + qd * 4);
-      uint2 wb = *reinterpret_cast<const uint2*>(xr + half + qd * 4);
-      __nv_bfloat16* a = reinterpret_cast<__nv_bfloat16*>(&wa);
-      __nv_bfloat16* b = reinterpret_cast<__nv_bfloat16*>(&wb);
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        float2 cs = rope_cs(hi_tab, lo_tab, pos, qd * 4 + e, half);
-        if (inverse) cs.y = -cs.y;
-        float u = __bfloat162float(a[e]), v = __bfloat162float(b[e]);
-        rope_pair(u, v, cs.x, cs.y);
-        a[e] = __float2bfloat16_rn(u);
-        b[e] = __float2bfloat16_rn(v);
-      }
-      *reinterpret_cast<uint2*>(yr + qd * 4) = wa;
-      *reinterpret_cast<uint2*>(yr + half + qd * 4) = wb;
+      const uint2 a = *reinterpret_cast<const uint2*>(x + off(r, 4 * qd));
+      const uint2 b = *reinterpret_cast<const uint2*>(x + off(r, HD / 2 + 4 * qd));
+      q.w = make_uint4(a.x, a.y, b.x, b.y);
+    }
+    return q;
+  }
+  __device__ __forceinline__ void store_raw(int r, int qd, const QuadRaw& q) const {
+    if (L == 0) {
+      *reinterpret_cast<uint4*>(y + off(r, 8 * qd)) = q.w;
+    } else {
+      *reinterpret_cast<uint2*>(y + off(r, 4 * qd)) = make_uint2(q.w.x, q.w.y);
+      *reinterpret_cast<uint2*>(y + off(r, HD / 2 + 4 * qd)) = make_uint2(q.w.z, q.w.w);
     }
   }
+  __device__ __forceinline__ static void unpack(const QuadRaw& q, float* a, float* b) { quad_unpack(L, q, a, b); }
+  __device__ __forceinline__ static QuadRaw pack(const float* a, const float* b) { return quad_pack(L, a, b); }
+};
+
+// One CTA of 128 threads per (128-row tile, head): the canonical tile
+// rotation of kcommon.cuh, straight from and to global memory.
+template <int HD, int L>
+__global__ void __launch_bounds__(128) rope_apply_kernel(const __nv_bfloat16* __restrict__ x,
+                                                         __nv_bfloat16* y, const int32_t* __restrict__ pos_id,
+                                                         const float2* __restrict__ hi_tab,
+                                                         const float2* __restrict__ lo_tab,
+                                                         const float2* __restrict__ step_tab, int T, int H,
+                                                         int inverse) {
+  GlobalTile<HD, L> tile{x, y, (int)blockIdx.x * kTile, H, (int)blockIdx.y};
+  RopeUnits<HD, 128> st;
+  st.begin(tile.row0, T, pos_id, inverse != 0, hi_tab, lo_tab, threadIdx.x);
+  st.run(tile, inverse != 0, hi_tab, lo_tab, step_tab, threadIdx.x);
+}
+
+template <int HD>
+void launch_rope_apply(const aa_plan_s* p, const void* x, void* y, int H, int inverse, cudaStream_t s) {
+  const dim3 grid((unsigned)p->n_tiles, (unsigned)H);
+  const auto* xi = static_cast<const __nv_bfloat16*>(x);
+  auto* yo = static_cast<__nv_bfloat16*>(y);
+  if (p->cfg.rope_layout == AA_ROPE_ADJACENT)
+    rope_apply_kernel<HD, 0><<<grid, 128, 0, s>>>(xi, yo, p->dev.pos_id, p->dev.rope_hi, p->dev.rope_lo,
+                                                  p->dev.rope_step, p->T, H, inverse);
+  else
+    rope_apply_kernel<HD, 1><<<grid, 128, 0, s>>>(xi, yo, p->dev.pos_id, p->dev.rope_hi, p->dev.rope_lo,
+                                                  p->dev.rope_step, p->T, H, inverse);
 }
 
 static PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {
@@ -91,6 +102,15 @@ aa_status make_tile_map(CUtensorMap* m, const void* base, int T, int H, int D) {
   return AA_OK;
 }
 
+aa_status launch_rope(const aa_plan_s* p, const void* x, void* y, int H, int inverse, cudaStream_t s) {
+  if (p->D == 128)
+    launch_rope_apply<128>(p, x, y, H, inverse, s);
+  else
+    launch_rope_apply<64>(p, x, y, H, inverse, s);
+  cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? AA_OK : cuda_fail(e, "rope_apply_kernel launch");
+}
+
 }  // namespace aa
 
 using namespace aa;
@@ -110,14 +130,5 @@ extern "C" aa_status aa_rope_apply(aa_plan_t p, const void* x, void* y, int32_t 
     cudaError_t e = cudaMemcpyAsync(y, x, (size_t)T * num_heads * D * 2, cudaMemcpyDeviceToDevice, s);
     return e == cudaSuccess ? AA_OK : cuda_fail(e, "aa_rope_apply copy");
   }
-  const int64_t n = T * num_heads * (D / 8);
-  const int threads = 256;
-  int64_t blocks = (n + threads - 1) / threads;
-  const int64_t cap = (int64_t)p->num_sms * 8;
-  if (blocks > cap) blocks = cap;
-  rope_apply_kernel<<<(unsigned)blocks, threads, 0, s>>>(
-      static_cast<const __nv_bfloat16*>(x), static_cast<__nv_bfloat16*>(y), p->dev.pos_id, p->dev.rope_hi,
-      p->dev.rope_lo, T, num_heads, D, p->cfg.rope_layout, inverse ? 1 : 0);
-  cudaError_t e = cudaGetLastError();
-  return e == cudaSuccess ? AA_OK : cuda_fail(e, "rope_apply_kernel launch");
+  return launch_rope(p, x, y, num_heads, inverse ? 1 : 0, s);
 }

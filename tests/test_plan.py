@@ -98,7 +98,7 @@ def test_invalid_arguments_rejected(aa, kwargs, cu, msg):
 def test_compute_on_host_only_plan_is_refused(aa):
     with _plan(aa, [1, 64], 64) as p:
         L = aa.lib()
-        assert L.aa_fwd(p._h, None, None, None, None, None, None) == 1
+        assert L.aa_fwd(p._h, None, None, None, None, None, None, 0, None) == 1
         assert "host_only" in L.aa_last_error().decode()
         assert L.aa_check_device_error(p._h, None) == 1
 
