@@ -185,11 +185,13 @@ __global__ void __launch_bounds__(128) bwd_prep_kernel(const __nv_bfloat16* __re
 //   warps 4-11  P/dS: two groups (query columns 0-63 and 64-127), thread = key
 //               row = TMEM lane; P^T packed bf16 into TMEM for the dV product,
 //               dS^T bf16 into shared memory
-//   warps 12-15 dQ drain (thread = query row): dQ~ from TMEM into the fp32
-//               accumulator with vector atomics, concurrently with the next
-//               tile's products
-// TMEM columns: S^T [0,128) (P^T over [0,32) and [64,96)), dP^T [128,256) (dQ~ reuses
-// [128,128+D) once dS is formed), dV [256,256+D), dK~ [256+D,256+2D).
+//   warps 12-15 dQ drain: dQ~ from TMEM into the fp32 accumulator. For
+//               D = 128 the MMA produces dQ~^T (lane = channel); the drain
+//               copies it into the step's dead Q~/dO stage buffers, releases
+//               TMEM at once and adds the copy with TMA bulk reductions that
+//               overlap the next tile; for D = 64 it uses vector atomics.
+// TMEM columns: S^T [0,128) (P^T over [0,32) and [64,96)), dP^T [128,256) (dQ~
+// or dQ~^T reuses [128,256) once dS is formed), dV [256,256+D), dK~ [256+D,256+2D).
 constexpr int kBwdThreads = 512;
 
 template <int HD>
@@ -247,7 +249,7 @@ template <int HD>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     attn_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
-                    const BwdParams P) {
+                    const __grid_constant__ CUtensorMap tmDQ, const BwdParams P) {
   // the layout fills the 227 KB limit exactly, so it relies on a 1 KB aligned
   // dynamic shared-memory base (checked: swizzled tiles need it)
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -365,11 +367,19 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           ptx::mma_bf16(t_dk, ptx::smem_desc_sw128(sds + aoff, 16, 1024),
                         ptx::smem_desc_sw128(sq + kk * 2048, 16384, 1024), idesc_kd, (step > 0 || kk > 0) ? 1u : 0u);
         }
-        for (int kk = 0; kk < 8; ++kk)  // dQ~ = dS K~
-          ptx::mma_bf16(t_dq, ptx::smem_desc_sw128(sds + kk * 2048, 16384, 1024),
-                        ptx::smem_desc_sw128(sk + kk * 2048, 16384, 1024), idesc_qd, kk > 0 ? 1u : 0u);
-        ptx::mma_commit(&sm.dq_full);
-        ptx::mma_commit(&sm.qd_empty[s]);
+        if constexpr (HD == 128) {
+          // dQ~^T = K~^T dS^T: TMEM lanes = channels, columns = query rows, so
+          // the drain's reductions are 128-byte coalesced per warp
+          constexpr uint32_t idesc_qt = ptx::idesc_bf16_f32(128, 128, 1, 1);
+          for (int kk = 0; kk < 8; ++kk)
+            ptx::mma_bf16(t_dq, ptx::smem_desc_sw128(sk + kk * 2048, 16384, 1024),
+                          ptx::smem_desc_sw128(sds + kk * 2048, 16384, 1024), idesc_qt, kk > 0 ? 1u : 0u);
+        } else {
+          for (int kk = 0; kk < 8; ++kk)  // dQ~ = dS K~ (TMEM lanes = query rows)
+            ptx::mma_bf16(t_dq, ptx::smem_desc_sw128(sds + kk * 2048, 16384, 1024),
+                          ptx::smem_desc_sw128(sk + kk * 2048, 16384, 1024), idesc_qd, kk > 0 ? 1u : 0u);
+        }
+        ptx::mma_commit(&sm.dq_full);  // the drain hands stage s back to the producer
       }
       if (ok) ptx::mma_commit(&sm.o_full);
       ptx::mma_commit(&sm.drain);
@@ -506,25 +516,62 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
     bool ok = true;
     for (int step = 0; step < n_steps && ok; ++step) {
-      const int h = step_head(step), i = step_qt(step) * kTile + r;
+      const int h = step_head(step), i0 = step_qt(step) * kTile;
       ok = bwd_wait(&sm.dq_full, step & 1, P, abort_flag, 431);
+      ok = ptx::bar_and(3, 128, ok);  // the drain group moves on (or stops) as one
       if (!ok) break;
       ptx::tc_fence_after();
-      float* dst = P.ws.dq_acc + ((size_t)(i < P.T ? i : 0) * P.Hq + h) * HD;
+      if constexpr (HD == 128) {
+        // lane r = channel. The step's Q~ / dO stage buffers are dead once its
+        // MMAs are done, so they hold scale*dQ~ as two [128 rows][64 channels]
+        // fp32 blocks: TMEM is released as soon as it is read, and two TMA
+        // bulk reductions add the blocks to the accumulator while the next
+        // tile computes. The stage returns to the producer once read.
+        const int s = step & 1;
+        float* stage = reinterpret_cast<float*>((r >> 6) == 0 ? sm.q[s][0] : sm.dout[s][0]);
+        const int ch = r & 63;
 #pragma unroll 1
-      for (int c = 0; c < HD / 32; ++c) {
-        float dq[32];
-        ptx::tmem_ld32(t_dq + lane_off + c * 32, dq);
-        ptx::tmem_wait_ld();
-        if (i < P.T) {
+        for (int c = 0; c < 4; ++c) {
+          float dq[32];
+          ptx::tmem_ld32(t_dq + lane_off + c * 32, dq);
+          ptx::tmem_wait_ld();
 #pragma unroll
-          for (int e = 0; e < 32; e += 4)
-            ptx::red_add_v4(dst + c * 32 + e, P.scale * dq[e], P.scale * dq[e + 1], P.scale * dq[e + 2],
-                            P.scale * dq[e + 3]);
+          for (int e = 0; e < 32; ++e) stage[(c * 32 + e) * 64 + ch] = P.scale * dq[e];
+        }
+        ptx::tc_fence_before();
+        ptx::mbar_arrive(&sm.dq_free);
+        ptx::fence_proxy_async_smem();
+        asm volatile("bar.sync 3, 128;" ::: "memory");
+        if (r == 0) {
+          ptx::tma_reduce_add_3d(&tmDQ, sm.q[s][0], 0, h, i0);
+          ptx::tma_reduce_add_3d(&tmDQ, sm.dout[s][0], 64, h, i0);
+          ptx::bulk_commit();
+          ptx::bulk_wait_read0();
+          ptx::mbar_arrive(&sm.qd_empty[s]);
+        }
+        continue;
+      } else {
+        if (r == 0) ptx::mbar_arrive(&sm.qd_empty[step & 1]);  // the step's MMAs are done
+        const int i = i0 + r;
+        float* dst = P.ws.dq_acc + ((size_t)(i < P.T ? i : 0) * P.Hq + h) * HD;
+#pragma unroll 1
+        for (int c = 0; c < HD / 32; ++c) {
+          float dq[32];
+          ptx::tmem_ld32(t_dq + lane_off + c * 32, dq);
+          ptx::tmem_wait_ld();
+          if (i < P.T) {
+#pragma unroll
+            for (int e = 0; e < 32; e += 4)
+              ptx::red_add_v4(dst + c * 32 + e, P.scale * dq[e], P.scale * dq[e + 1], P.scale * dq[e + 2],
+                              P.scale * dq[e + 3]);
+          }
         }
       }
       ptx::tc_fence_before();
       ptx::mbar_arrive(&sm.dq_free);
+    }
+    if constexpr (HD == 128) {
+      if (r == 0) ptx::bulk_wait0();  // reductions land before the CTA exits
     }
   } else if (warp == 2 || warp == 3) {
     // ------------------------------------------------------------ RoPE + LSE/D staging
@@ -670,6 +717,8 @@ aa_status launch_bwd(aa_plan_s* p, const void* q, const void* k, const void* v, 
   if ((st = make_tile_map(&tk, k, p->T, p->Hkv, HD)) != AA_OK) return st;
   if ((st = make_tile_map(&tv, v, p->T, p->Hkv, HD)) != AA_OK) return st;
   if ((st = make_tile_map(&tdo, dout, p->T, p->Hq, HD)) != AA_OK) return st;
+  CUtensorMap tdq;
+  if ((st = make_f32_half_map(&tdq, ws.dq_acc, p->T, p->Hq, HD)) != AA_OK) return st;
   BwdParams P;
   P.dk = static_cast<__nv_bfloat16*>(dk);
   P.dv = static_cast<__nv_bfloat16*>(dv);
@@ -694,7 +743,7 @@ aa_status launch_bwd(aa_plan_s* p, const void* q, const void* k, const void* v, 
   if (e != cudaSuccess) return cuda_fail(e, "attn_bwd_kernel smem attribute");
   if (p->bwd_ev_start && (e = cudaEventRecord(p->bwd_ev_start, s)) != cudaSuccess)
     return cuda_fail(e, "recording the bwd start event");
-  attn_bwd_kernel<HD><<<(unsigned)p->bwd_items.size(), kBwdThreads, smem, s>>>(tq, tk, tv, tdo, P);
+  attn_bwd_kernel<HD><<<(unsigned)p->bwd_items.size(), kBwdThreads, smem, s>>>(tq, tk, tv, tdo, tdq, P);
   if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(e, "attn_bwd_kernel launch");
   if (p->bwd_ev_stop && (e = cudaEventRecord(p->bwd_ev_stop, s)) != cudaSuccess)
     return cuda_fail(e, "recording the bwd stop event");

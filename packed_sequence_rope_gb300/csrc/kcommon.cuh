@@ -303,4 +303,8 @@ __device__ __forceinline__ float tile_elem(const uint8_t* tile, int r, int c) {
 // 128-byte swizzle (one 16 KB tile block per load).
 aa_status make_tile_map(CUtensorMap* m, const void* base, int T, int H, int D);
 
+// Host: tensor map over x [T, H, D] fp32 with a {64, 1, 128} box, no swizzle
+// (a [128 rows][64 channels] fp32 block, 32 KB).
+aa_status make_f32_half_map(CUtensorMap* m, const void* base, int T, int H, int D);
+
 }  // namespace aa
