@@ -202,8 +202,8 @@ struct BwdSmem {
   alignas(1024) uint8_t q[2][kB][16384];
   alignas(1024) uint8_t dout[2][kB][16384];
   alignas(1024) uint8_t dst[2][16384];  // dS^T: 128 keys x 128 query rows, bf16
-  float lse2[2][128];                   // LSE * log2(e) of each stage's query rows
-  float dsum[2][128];                   // D of each stage's query rows
+  float lse2[2][128];                   // -LSE * log2(e) of each stage's query rows
+  float dsum[2][128];                   // -D of each stage's query rows
   uint64_t kv_full, k_ready;
   uint64_t qd_full[2], q_ready[2], qd_empty[2];
   uint64_t st_full, p_full, dq_full, dq_free, o_full, drain;
@@ -421,20 +421,27 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             dd[e] = b4.x; dd[e + 1] = b4.y; dd[e + 2] = b4.z; dd[e + 3] = b4.w;
           }
           uint32_t pw[4], dw[4];
+          if (full) {
+            const float2 sl22 = make_float2(sl2, sl2);
 #pragma unroll
-          for (int e = 0; e < 8; e += 2) {
-            const int x = gq * 8 + e;
-            float p0, p1;
-            if (full) {
-              p0 = ptx::ex2(fmaf(sv[x], sl2, -lse2[e]));
-              p1 = ptx::ex2(fmaf(sv[x + 1], sl2, -lse2[e + 1]));
-            } else {
-              const int i = i0 + cb + e;
-              p0 = (i >= j && i <= jhi) ? ptx::ex2(fmaf(sv[x], sl2, -lse2[e])) : 0.f;
-              p1 = (i + 1 >= j && i + 1 <= jhi) ? ptx::ex2(fmaf(sv[x + 1], sl2, -lse2[e + 1])) : 0.f;
+            for (int e = 0; e < 8; e += 2) {
+              const int x = gq * 8 + e;
+              const float2 a = __ffma2_rn(make_float2(sv[x], sv[x + 1]), sl22, make_float2(lse2[e], lse2[e + 1]));
+              const float2 pp = make_float2(ptx::ex2(a.x), ptx::ex2(a.y));
+              const float2 dd2 = __fmul2_rn(pp, __fadd2_rn(make_float2(dpv[x], dpv[x + 1]), make_float2(dd[e], dd[e + 1])));
+              pw[e / 2] = ptx::pack_bf16x2(pp.x, pp.y);
+              dw[e / 2] = ptx::pack_bf16x2(dd2.x, dd2.y);
             }
-            pw[e / 2] = ptx::pack_bf16x2(p0, p1);
-            dw[e / 2] = ptx::pack_bf16x2(p0 * (dpv[x] - dd[e]), p1 * (dpv[x + 1] - dd[e + 1]));
+          } else {
+#pragma unroll
+            for (int e = 0; e < 8; e += 2) {
+              const int x = gq * 8 + e;
+              const int i = i0 + cb + e;
+              const float p0 = (i >= j && i <= jhi) ? ptx::ex2(fmaf(sv[x], sl2, lse2[e])) : 0.f;
+              const float p1 = (i + 1 >= j && i + 1 <= jhi) ? ptx::ex2(fmaf(sv[x + 1], sl2, lse2[e + 1])) : 0.f;
+              pw[e / 2] = ptx::pack_bf16x2(p0, p1);
+              dw[e / 2] = ptx::pack_bf16x2(p0 * (dpv[x] + dd[e]), p1 * (dpv[x + 1] + dd[e + 1]));
+            }
           }
           // P^T packs over S^T columns this group has already read: query
           // columns [64 cq, 64 cq + 64) land in TMEM columns [64 cq, 64 cq + 32)
@@ -595,8 +602,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const size_t hrow = (size_t)step_head(step) * P.T;
       for (int r = t; r < kTile; r += 64) {
         const int i = i0 + r;
-        sm.lse2[s][r] = i < P.T ? __ldg(P.lse + hrow + i) * kLog2e : INFINITY;
-        sm.dsum[s][r] = i < P.T ? __ldg(P.ws.dsum + hrow + i) : 0.f;
+        sm.lse2[s][r] = i < P.T ? -__ldg(P.lse + hrow + i) * kLog2e : -INFINITY;  // -LSE log2(e)
+        sm.dsum[s][r] = i < P.T ? -__ldg(P.ws.dsum + hrow + i) : 0.f;             // -D
       }
       ptx::mbar_arrive(&sm.q_ready[s]);
     }

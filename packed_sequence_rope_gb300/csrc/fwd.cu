@@ -327,13 +327,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::tmem_wait_ld();
         uint32_t w[16];
         if (full) {
+          const float2 sl22 = make_float2(sl2, sl2), nm2 = make_float2(-mm, -mm);
+          float2 rs2 = make_float2(0.f, 0.f);
 #pragma unroll
           for (int e = 0; e < 16; ++e) {
-            const float p0 = ptx::ex2(fmaf(sv[2 * e], sl2, -mm));
-            const float p1 = ptx::ex2(fmaf(sv[2 * e + 1], sl2, -mm));
-            rs += p0 + p1;
-            w[e] = ptx::pack_bf16x2(p0, p1);
+            const float2 a = __ffma2_rn(make_float2(sv[2 * e], sv[2 * e + 1]), sl22, nm2);
+            const float2 pp = make_float2(ptx::ex2(a.x), ptx::ex2(a.y));
+            rs2 = __fadd2_rn(rs2, pp);
+            w[e] = ptx::pack_bf16x2(pp.x, pp.y);
           }
+          rs += rs2.x + rs2.y;
         } else {
 #pragma unroll
           for (int e = 0; e < 16; ++e) {
