@@ -29,7 +29,7 @@ namespace {
 
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr uint64_t kDrainLimitNs = 1000000000ull;
-constexpr int kPrepChunks = 64;  // row chunks of the anchor partial sums
+constexpr int kPrepChunks = 256;  // row chunks of the anchor partial sums
 
 struct Workspace {
   __nv_bfloat16* qr;  // [T, Hq, D] rotated Q (unused without RoPE)
@@ -117,6 +117,7 @@ __global__ void __launch_bounds__(128) bwd_prep_kernel(const __nv_bfloat16* __re
 #pragma unroll
   for (int e = 0; e < EPL; ++e) pdv[e] = pdk[e] = 0.f;
 
+#pragma unroll 2
   for (int i = r_begin + warp; i < r_end; i += 4) {
     const size_t base = ((size_t)i * Hq + h) * HD + lane * EPL;
     float ov[EPL], dov[EPL];
@@ -629,13 +630,6 @@ __global__ void __launch_bounds__(256) dq_finalize_kernel(const float* __restric
     const float* a = acc + row * D;
     __nv_bfloat16* y = dq + row * D;
     float x0[4], x1[4];
-    int i0[4], i1[4];
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const int p = qd * 4 + e;
-      i0[e] = layout == 1 ? p : 2 * p;
-      i1[e] = layout == 1 ? p + half : 2 * p + 1;
-    }
     if (layout == 1) {
       const float4 u = *reinterpret_cast<const float4*>(a + qd * 4);
       const float4 w = *reinterpret_cast<const float4*>(a + half + qd * 4);
@@ -654,10 +648,15 @@ __global__ void __launch_bounds__(256) dq_finalize_kernel(const float* __restric
         rope_pair(x0[e], x1[e], cs.x, -cs.y);
       }
     }
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      y[i0[e]] = __float2bfloat16_rn(x0[e]);
-      y[i1[e]] = __float2bfloat16_rn(x1[e]);
+    if (layout == 1) {
+      *reinterpret_cast<uint2*>(y + qd * 4) =
+          make_uint2(ptx::pack_bf16x2(x0[0], x0[1]), ptx::pack_bf16x2(x0[2], x0[3]));
+      *reinterpret_cast<uint2*>(y + half + qd * 4) =
+          make_uint2(ptx::pack_bf16x2(x1[0], x1[1]), ptx::pack_bf16x2(x1[2], x1[3]));
+    } else {
+      *reinterpret_cast<uint4*>(y + qd * 8) =
+          make_uint4(ptx::pack_bf16x2(x0[0], x1[0]), ptx::pack_bf16x2(x0[1], x1[1]), ptx::pack_bf16x2(x0[2], x1[2]),
+                     ptx::pack_bf16x2(x0[3], x1[3]));
     }
   }
 }
