@@ -120,7 +120,8 @@ def _barrier(world):
     import torch
     if world > 1:
         torch.distributed.barrier()
-    torch.cuda.synchronize()
+    if torch.cuda.is_available():
+        torch.cuda.synchronize()
 
 
 # ----------------------------------------------------------------------------- our path

@@ -205,6 +205,14 @@ aa_status aa_set_wait_limit(aa_plan_t plan, uint64_t nanoseconds);
  * events are caller-owned and must outlive the calls that record them. */
 aa_status aa_set_bwd_timing_events(aa_plan_t plan, void* start, void* stop);
 
+/* Failure-detection self-test: launches one CTA that waits on a shared-memory
+ * barrier nothing ever arrives on, bounded by the plan's wait limit
+ * (aa_set_wait_limit). The wait runs out, the kernel records its site code in
+ * the plan's error word and returns, leaving the context usable; the next
+ * aa_check_device_error() returns AA_ERR_TIMEOUT. This is the same bounded
+ * wait every attention kernel uses. */
+aa_status aa_selftest_bounded_wait(aa_plan_t plan, aa_stream_t stream);
+
 const char* aa_status_string(aa_status status);
 const char* aa_last_error(void);
 

@@ -23,7 +23,8 @@ STATUS = {0: "AA_OK", 1: "AA_ERR_INVALID_ARG", 2: "AA_ERR_UNSUPPORTED", 3: "AA_E
 # every symbol include/anchorattn.h declares
 EXPORTS = ["aa_plan", "aa_plan_destroy", "aa_plan_metadata", "aa_plan_stats", "aa_plan_work",
            "aa_rope_apply", "aa_fwd", "aa_fwd_workspace_bytes", "aa_bwd_workspace_bytes", "aa_bwd", "aa_bwd_static_workspace", "aa_check_device_error",
-           "aa_set_wait_limit", "aa_set_bwd_timing_events", "aa_status_string", "aa_last_error"]
+           "aa_set_wait_limit", "aa_set_bwd_timing_events", "aa_selftest_bounded_wait", "aa_status_string",
+           "aa_last_error"]
 
 
 class AAConfig(ctypes.Structure):
@@ -68,6 +69,7 @@ def lib():
             "aa_check_device_error": ([vp, vp], ctypes.c_int),
             "aa_set_wait_limit": ([vp, ctypes.c_uint64], ctypes.c_int),
             "aa_set_bwd_timing_events": ([vp, vp, vp], ctypes.c_int),
+            "aa_selftest_bounded_wait": ([vp, vp], ctypes.c_int),
             "aa_status_string": ([ctypes.c_int], ctypes.c_char_p),
             "aa_last_error": ([], ctypes.c_char_p),
         }
@@ -166,6 +168,9 @@ class Plan:
         a = ctypes.c_void_p(start.cuda_event) if start is not None else None
         b = ctypes.c_void_p(stop.cuda_event) if stop is not None else None
         _check(lib().aa_set_bwd_timing_events(self._h, a, b))
+
+    def selftest_bounded_wait(self, stream=None):
+        _check(lib().aa_selftest_bounded_wait(self._h, _stream(stream)))
 
     def check_device_error(self, stream=None):
         _check(lib().aa_check_device_error(self._h, _stream(stream)))

@@ -125,9 +125,28 @@ aa_status make_f32_half_map(CUtensorMap* m, const void* base, int T, int H, int 
   return AA_OK;
 }
 
+// One warp waits on a barrier that expects one arrival and never gets it.
+__global__ void bounded_wait_selftest_kernel(int32_t* err, uint64_t limit_ns) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x == 0) {
+    ptx::mbar_init(&bar, 1);
+    ptx::fence_mbar_init();
+  }
+  __syncwarp();
+  if (threadIdx.x == 0) ptx::mbar_wait(&bar, 0, limit_ns, err, 900);
+}
+
 }  // namespace aa
 
 using namespace aa;
+
+extern "C" aa_status aa_selftest_bounded_wait(aa_plan_t p, aa_stream_t stream) {
+  aa_status st = check_compute_plan(p);
+  if (st != AA_OK) return st;
+  bounded_wait_selftest_kernel<<<1, 32, 0, reinterpret_cast<cudaStream_t>(stream)>>>(p->dev.err, p->wait_limit_ns);
+  cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? AA_OK : cuda_fail(e, "bounded_wait_selftest_kernel launch");
+}
 
 extern "C" aa_status aa_rope_apply(aa_plan_t p, const void* x, void* y, int32_t num_heads, int32_t inverse,
                                    aa_stream_t stream) {

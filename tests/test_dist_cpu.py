@@ -1,0 +1,54 @@
+"""The multi-rank bench plumbing (replicas under torchrun) on CPU with gloo:
+the step time every rank reports is the maximum over ranks, and the
+reference arm prints only on rank 0."""
+import os
+import socket
+import subprocess
+import sys
+
+import torch.multiprocessing as mp
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _free_port():
+    s = socket.socket()
+    s.bind(("127.0.0.1", 0))
+    port = s.getsockname()[1]
+    s.close()
+    return port
+
+
+def _worker(rank, world, port, q):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank), WORLD_SIZE=str(world))
+    sys.path.insert(0, ROOT)
+    import torch
+    import bench
+    torch.distributed.init_process_group("gloo", rank=rank, world_size=world)
+    r, w = bench._dist()
+    t = bench._max_over_ranks(10.0 + 5 * rank, w)
+    bench._barrier(w)
+    q.put((r, w, t))
+    torch.distributed.destroy_process_group()
+
+
+def test_max_over_ranks_gloo_world2():
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_worker, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    out = sorted(q.get(timeout=120) for _ in procs)
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    assert out == [(0, 2, 15.0), (1, 2, 15.0)]
+
+
+def test_reference_arm_prints_on_rank0_only():
+    env = dict(os.environ, RANK="1", WORLD_SIZE="2", LOCAL_RANK="1")
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--steps", "1",
+                        "--warmup", "0", "--workload", "tiny_256"], capture_output=True, text=True, env=env,
+                       timeout=300)
+    assert r.returncode == 0 and r.stdout.strip() == ""
