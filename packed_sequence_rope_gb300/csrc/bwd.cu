@@ -33,6 +33,7 @@ constexpr int kPrepChunks = 256;  // row chunks of the anchor partial sums
 
 struct Workspace {
   __nv_bfloat16* qr;  // [T, Hq, D] rotated Q (unused without RoPE)
+  __nv_bfloat16* kr;  // [T, Hkv, D] rotated K (unused without RoPE)
   float* dq_acc;   // [T, Hq, D] fp32
   float* dsum;     // [Hq, T] fp32 (D_i)
   float* part_dv;  // [kPrepChunks, Hq, D]
@@ -47,6 +48,8 @@ Workspace carve(void* base, const aa_plan_s* p, size_t* total) {
   uint8_t* b = static_cast<uint8_t*>(base);
   w.qr = reinterpret_cast<__nv_bfloat16*>(b + off);
   if (p->cfg.rope_layout != AA_ROPE_NONE) off = align256(off + (size_t)p->T * p->Hq * p->D * 2);
+  w.kr = reinterpret_cast<__nv_bfloat16*>(b + off);
+  if (p->cfg.rope_layout != AA_ROPE_NONE) off = align256(off + (size_t)p->T * p->Hkv * p->D * 2);
   w.dq_acc = reinterpret_cast<float*>(b + off);
   off = align256(off + (size_t)p->T * p->Hq * p->D * 4);
   w.dsum = reinterpret_cast<float*>(b + off);
@@ -180,9 +183,10 @@ __global__ void __launch_bounds__(128) bwd_prep_kernel(const __nv_bfloat16* __re
 // One CTA per (key tile, kv head), 512 threads:
 //   warp 0      TMA producer: K, V once; Q_i, dO_i through a 2-stage ring
 //   warp 1      TMEM owner and MMA issuer (one thread)
-//   warps 2-3   RoPE fused into the K tile load (once per CTA; Q arrives
-//               rotated from the workspace) and staging of each query
-//               tile's LSE*log2(e) and D rows into shared memory
+//   warps 2-3   staging of each query tile's -LSE*log2(e) and -D rows into
+//               shared memory (Q and K arrive rotated from the workspace: a
+//               per-CTA rotation in the tile load cost more than the once-per-
+//               call pass, since most CTAs here run only a handful of tiles)
 //   warps 4-11  P/dS: two groups (query columns 0-63 and 64-127), thread = key
 //               row = TMEM lane; P^T packed bf16 into TMEM for the dV product,
 //               dS^T bf16 into shared memory
@@ -584,17 +588,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   } else if (warp == 2 || warp == 3) {
     // ------------------------------------------------------------ RoPE + LSE/D staging
     const int t = tid - 64;
-    const bool rot = P.layout != 2;
-    RopeUnits<HD, 64> ru;
-    if (rot) ru.begin(kt * kTile, P.T, P.pos_id, false, P.rope_hi, P.rope_lo, t);
     bool ok = bwd_wait(&sm.kv_full, 0, P, abort_flag, 441);
-    if (ok) {
-      if (rot) {
-        rope_smem_tile<HD, 64>(ru, sm.k[0], P.layout, P.rope_hi, P.rope_lo, P.rope_step, t);
-      }
-      ptx::fence_proxy_async_smem();
-      ptx::mbar_arrive(&sm.k_ready);
-    }
+    if (ok) ptx::mbar_arrive(&sm.k_ready);
     for (int step = 0; step < n_steps && ok; ++step) {
       const int s = step & 1;
       const int i0 = step_qt(step) * kTile;
@@ -705,10 +700,13 @@ aa_status launch_bwd(aa_plan_s* p, const void* q, const void* k, const void* v, 
   // Q is the streaming operand of the key-stationary tile loop: rotate it
   // once here rather than on every visit
   const void* qr = q;
+  const void* kr = k;
   if (rope_layout != AA_ROPE_NONE) {
     aa_status rs = launch_rope(p, q, ws.qr, p->Hq, 0, s);
+    if (rs == AA_OK) rs = launch_rope(p, k, ws.kr, p->Hkv, 0, s);
     if (rs != AA_OK) return rs;
     qr = ws.qr;
+    kr = ws.kr;
   }
   bwd_prep_kernel<HD><<<dim3(kPrepChunks, p->Hq), 128, 0, s>>>(
       static_cast<const __nv_bfloat16*>(qr), static_cast<const __nv_bfloat16*>(k),
@@ -720,7 +718,7 @@ aa_status launch_bwd(aa_plan_s* p, const void* q, const void* k, const void* v, 
   CUtensorMap tq, tk, tv, tdo;
   aa_status st;
   if ((st = make_tile_map(&tq, qr, p->T, p->Hq, HD)) != AA_OK) return st;
-  if ((st = make_tile_map(&tk, k, p->T, p->Hkv, HD)) != AA_OK) return st;
+  if ((st = make_tile_map(&tk, kr, p->T, p->Hkv, HD)) != AA_OK) return st;
   if ((st = make_tile_map(&tv, v, p->T, p->Hkv, HD)) != AA_OK) return st;
   if ((st = make_tile_map(&tdo, dout, p->T, p->Hq, HD)) != AA_OK) return st;
   CUtensorMap tdq;
