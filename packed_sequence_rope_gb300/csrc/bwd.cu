@@ -442,8 +442,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             for (int e = 0; e < 8; e += 2) {
               const int x = gq * 8 + e;
               const int i = i0 + cb + e;
-              const float p0 = (i >= j && i <= jhi) ? ptx::ex2(fmaf(sv[x], sl2, lse2[e])) : 0.f;
-              const float p1 = (i + 1 >= j && i + 1 <= jhi) ? ptx::ex2(fmaf(sv[x + 1], sl2, lse2[e + 1])) : 0.f;
+              // masked elements feed -inf to ex2 (2^-inf = 0): selects, no branches
+              const float p0 = ptx::ex2((i >= j && i <= jhi) ? fmaf(sv[x], sl2, lse2[e]) : -INFINITY);
+              const float p1 = ptx::ex2((i + 1 >= j && i + 1 <= jhi) ? fmaf(sv[x + 1], sl2, lse2[e + 1]) : -INFINITY);
               pw[e / 2] = ptx::pack_bf16x2(p0, p1);
               dw[e / 2] = ptx::pack_bf16x2(p0 * (dpv[x] + dd[e]), p1 * (dpv[x + 1] + dd[e + 1]));
             }
