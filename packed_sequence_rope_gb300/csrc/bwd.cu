@@ -461,9 +461,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       ptx::tc_fence_before();
       ptx::mbar_arrive(&sm.p_full);
     }
-    if (ok && cq == 0) ok = bwd_wait(&sm.o_full, 0, P, abort_flag, 423);
-    if (ok && cq == 0) {
-      // ---- epilogue: dV and dk = R^T (scale dK~) for this thread's key row
+    if (ok) ok = bwd_wait(&sm.o_full, 0, P, abort_flag, 423);
+    if (ok) {
+      // ---- epilogue (group 0: dV, group 1: dk = R^T (scale dK~)) for this thread's key row
       ptx::tc_fence_after();
       __nv_bfloat16* dvrow = P.dv + ((size_t)(key_valid ? j : 0) * P.Hkv + g) * HD;
       __nv_bfloat16* dkrow = P.dk + ((size_t)(key_valid ? j : 0) * P.Hkv + g) * HD;
@@ -475,14 +475,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           dst[c] = make_uint4(ptx::pack_bf16x2(x[8 * c], x[8 * c + 1]), ptx::pack_bf16x2(x[8 * c + 2], x[8 * c + 3]),
                               ptx::pack_bf16x2(x[8 * c + 4], x[8 * c + 5]), ptx::pack_bf16x2(x[8 * c + 6], x[8 * c + 7]));
       };
+      if (cq == 0) {
 #pragma unroll 1
-      for (int c = 0; c < HD / 32; ++c) {
-        float x[32];
-        ptx::tmem_ld32(t_dv + lane_off + c * 32, x);
-        ptx::tmem_wait_ld();
-        if (key_valid) store32(dvrow, c * 32, x);
-      }
-      if (P.layout != 1) {
+        for (int c = 0; c < HD / 32; ++c) {
+          float x[32];
+          ptx::tmem_ld32(t_dv + lane_off + c * 32, x);
+          ptx::tmem_wait_ld();
+          if (key_valid) store32(dvrow, c * 32, x);
+        }
+      } else if (P.layout != 1) {
 #pragma unroll 1
         for (int c = 0; c < HD / 32; ++c) {
           float x[32];
