@@ -60,7 +60,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.t = threading.Thread(target=self._read, daemon=True)
             self.t.start()
         except FileNotFoundError:
@@ -369,7 +369,7 @@ def run_reference(args):
     cu = workload_cu_doclens(w)
     mask = {"anchor": 2, "intra_doc": 1, "causal": 0}[args.mask]
     pos = {"reset": 0, "continuous": 1}[args.pos]
-    budget = max(5.0, min(60.0, 120.0 / max(1, args.steps + args.warmup)))
+    budget = max(1.0, min(60.0, 120.0 / max(1, args.steps + args.warmup)))
     for _ in range(args.warmup):
         cpu_baseline(w, cu, mask, pos, budget_s=budget)
     vals = [cpu_baseline(w, cu, mask, pos, budget_s=budget) for _ in range(args.steps)]
@@ -389,7 +389,7 @@ def run_reference(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=30)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="llama7b_64k", choices=sorted(WORKLOADS))

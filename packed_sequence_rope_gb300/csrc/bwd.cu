@@ -15,11 +15,12 @@
 //      fp32 dQ accumulator is initialised with scale*dS_i0*k~_0 (so it needs
 //      no separate clearing pass) and per-chunk partial sums of dv_0, dk~_0
 //      are written.
-//   2. attn_bwd: one CTA per (key tile, kv head), K/V stationary in shared
-//      memory (K rotated once), looping over the group's query heads and the
-//      live query tiles. Five tcgen05 MMAs per tile (S^T, dP^T, dV, dK, dQ)
-//      with fp32 TMEM accumulators; dQ goes to the fp32 accumulator with
-//      vector atomics; dK/dV are rotated back and written once.
+//   2. attn_bwd: one CTA per (key tile, kv head), K~/V stationary in shared
+//      memory, looping over the group's query heads and the live query
+//      tiles. Five tcgen05 MMAs per tile (S^T, dP^T, dV, dK, dQ) with fp32
+//      TMEM accumulators; dQ~ is added into the fp32 accumulator (TMA bulk
+//      reductions for D = 128, vector atomics for D = 64); dK/dV are rotated
+//      back and written once.
 //   3. dq_finalize: dq = bf16(R^T dq~).
 //   4. anchor_finalize: dk_0 / dv_0 = fixed-order sums of the partials.
 #include "kcommon.cuh"
@@ -63,119 +64,147 @@ Workspace carve(void* base, const aa_plan_s* p, size_t* total) {
 }
 
 // ---------------------------------------------------------------- 1. prep
-// One warp per row; lane l holds channels [l*EPL, (l+1)*EPL).
-template <int HD>
-__global__ void __launch_bounds__(128) bwd_prep_kernel(const __nv_bfloat16* __restrict__ q,
-                                                       const __nv_bfloat16* __restrict__ k,
-                                                       const __nv_bfloat16* __restrict__ v,
-                                                       const __nv_bfloat16* __restrict__ o,
-                                                       const __nv_bfloat16* __restrict__ dout,
-                                                       const float* __restrict__ lse, Workspace ws,
-                                                       const int32_t* __restrict__ pos_id,
-                                                       const float2* __restrict__ hi_tab,
-                                                       const float2* __restrict__ lo_tab, int T, int Hq,
-                                                       int group, int layout, int anchor, float scale) {
-  constexpr int EPL = HD / 32;
-  const int h = blockIdx.y, g = h / group;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int rows_per_chunk = (T + kPrepChunks - 1) / kPrepChunks;
-  const int r_begin = blockIdx.x * rows_per_chunk;
-  const int r_end = min(T, r_begin + rows_per_chunk);
-  __shared__ float red_dv[4][HD], red_dk[4][HD];
+// 256 threads per (row chunk, head). A row is handled by HD/8 lanes holding
+// 8 channels (one 16-byte load per tensor) each, so a warp covers 32/(HD/8)
+// rows per pass and every load is a full 16-byte vector.
+constexpr int kPrepThreads = 256;
 
-  // rotated anchor key for this lane's channels (bf16-rounded, as the forward uses it)
-  float k0[EPL], v0[EPL];
-  auto rotate_lane = [&](float* x, int pos) {
-    if (layout == 2) return;
-    if (layout == 0) {
+template <int HD>
+__global__ void __launch_bounds__(kPrepThreads) bwd_prep_kernel(const __nv_bfloat16* __restrict__ q,
+                                                                const __nv_bfloat16* __restrict__ k,
+                                                                const __nv_bfloat16* __restrict__ v,
+                                                                const __nv_bfloat16* __restrict__ o,
+                                                                const __nv_bfloat16* __restrict__ dout,
+                                                                const float* __restrict__ lse, Workspace ws, int T,
+                                                                int Hq, int group, int anchor, float scale) {
+  constexpr int LPR = HD / 8;          // lanes per row
+  constexpr int RPW = 32 / LPR;        // rows per warp pass
+  constexpr int NW = kPrepThreads / 32;
+  // heads are the fast grid index: blocks resident together read whole
+  // [Hq, D] token rows rather than one head's rows at a stride
+  const int h = blockIdx.x, g = h / group;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int sub = lane / LPR, c0 = (lane % LPR) * 8;
+  const int rows_per_chunk = (T + kPrepChunks - 1) / kPrepChunks;
+  const int r_begin = blockIdx.y * rows_per_chunk;
+  const int r_end = min(T, r_begin + rows_per_chunk);
+  __shared__ float red_dv[NW][HD], red_dk[NW][HD];
+
+  auto unpack8 = [](const uint4& u, float* x) {
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
-      for (int e = 0; e < EPL; e += 2) {
-        const float2 cs = rope_cs(hi_tab, lo_tab, pos, (lane * EPL + e) >> 1, HD / 2);
-        rope_pair(x[e], x[e + 1], cs.x, cs.y);
-      }
-    } else {
-      const bool first = lane < 16;
-#pragma unroll
-      for (int e = 0; e < EPL; ++e) {
-        const float other = __shfl_xor_sync(0xffffffffu, x[e], 16);
-        const int pidx = (lane & 15) * EPL + e;
-        const float2 cs = rope_cs(hi_tab, lo_tab, pos, pidx, HD / 2);
-        float a = first ? x[e] : other, b = first ? other : x[e];
-        rope_pair(a, b, cs.x, cs.y);
-        x[e] = first ? a : b;
-      }
+    for (int j = 0; j < 4; ++j) {
+      const float2 f = ptx::unpack_bf16x2(w[j]);
+      x[2 * j] = f.x;
+      x[2 * j + 1] = f.y;
     }
   };
+  // the anchor key k~_0 (k is the rotated K, the forward's operand) and v_0
+  // for this lane's channels
+  float k0[8], v0[8];
   if (anchor) {
-#pragma unroll
-    for (int e = 0; e < EPL; ++e) {
-      k0[e] = __bfloat162float(k[(size_t)g * HD + lane * EPL + e]);
-      v0[e] = __bfloat162float(v[(size_t)g * HD + lane * EPL + e]);
-    }
-    rotate_lane(k0, __ldg(pos_id));
-#pragma unroll
-    for (int e = 0; e < EPL; ++e) k0[e] = __bfloat162float(__float2bfloat16_rn(k0[e]));
+    unpack8(*reinterpret_cast<const uint4*>(k + (size_t)g * HD + c0), k0);
+    unpack8(*reinterpret_cast<const uint4*>(v + (size_t)g * HD + c0), v0);
   }
-  float pdv[EPL], pdk[EPL];
+  float pdv[8], pdk[8];
 #pragma unroll
-  for (int e = 0; e < EPL; ++e) pdv[e] = pdk[e] = 0.f;
+  for (int e = 0; e < 8; ++e) pdv[e] = pdk[e] = 0.f;
 
-#pragma unroll 2
-  for (int i = r_begin + warp; i < r_end; i += 4) {
-    const size_t base = ((size_t)i * Hq + h) * HD + lane * EPL;
-    float ov[EPL], dov[EPL];
+  // sum over the LPR lanes of one row
+  auto row_sum = [](float x) {
 #pragma unroll
-    for (int e = 0; e < EPL; ++e) {
-      ov[e] = __bfloat162float(o[base + e]);
-      dov[e] = __bfloat162float(dout[base + e]);
+    for (int s = LPR / 2; s > 0; s >>= 1) x += __shfl_xor_sync(0xffffffffu, x, s);
+    return x;
+  };
+
+  // NB passes per iteration, all their loads issued before any arithmetic
+  // (enough bytes in flight per SM to cover HBM latency); the pass base is
+  // warp-uniform so every lane takes part in the shuffles
+  constexpr int NB = 4;
+  const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+  for (int ib = r_begin + warp * RPW; ib < r_end; ib += NB * NW * RPW) {
+    uint4 ro[NB], rd[NB], rq[NB];
+    float lse_v[NB];
+#pragma unroll
+    for (int b = 0; b < NB; ++b) {
+      const int i = ib + b * NW * RPW + sub;
+      const bool valid = i < r_end;
+      const size_t base = ((size_t)i * Hq + h) * HD + c0;
+      ro[b] = valid ? *reinterpret_cast<const uint4*>(o + base) : z;
+      rd[b] = valid ? *reinterpret_cast<const uint4*>(dout + base) : z;
+      rq[b] = valid && anchor ? *reinterpret_cast<const uint4*>(q + base) : z;
+      lse_v[b] = valid && anchor ? __ldg(lse + (size_t)h * T + i) : 0.f;
     }
-    float dsum = 0.f;
 #pragma unroll
-    for (int e = 0; e < EPL; ++e) dsum = fmaf(ov[e], dov[e], dsum);
+    for (int b = 0; b < NB; ++b) {
+      const int i = ib + b * NW * RPW + sub;
+      const bool valid = i < r_end;
+      const size_t base = ((size_t)i * Hq + h) * HD + c0;
+      float ov[8], dov[8];
+      unpack8(ro[b], ov);
+      unpack8(rd[b], dov);
+      float dsum = 0.f;
 #pragma unroll
-    for (int s = 16; s > 0; s >>= 1) dsum += __shfl_xor_sync(0xffffffffu, dsum, s);
-    if (lane == 0) ws.dsum[(size_t)h * T + i] = dsum;
-    float* acc = ws.dq_acc + base;
-    if (anchor) {
-      float qv[EPL];  // q~_i: q is the rotated Q here
+      for (int e = 0; e < 8; ++e) dsum = fmaf(ov[e], dov[e], dsum);
+      dsum = row_sum(dsum);
+      if (valid && c0 == 0) ws.dsum[(size_t)h * T + i] = dsum;
+      float4* acc = reinterpret_cast<float4*>(ws.dq_acc + base);
+      if (anchor) {
+        float qv[8];  // q~_i: q is the rotated Q here
+        unpack8(rq[b], qv);
+        float s = 0.f, dp = 0.f;
 #pragma unroll
-      for (int e = 0; e < EPL; ++e) qv[e] = __bfloat162float(q[base + e]);
-      float s = 0.f, dp = 0.f;
+        for (int e = 0; e < 8; ++e) {
+          s = fmaf(qv[e], k0[e], s);
+          dp = fmaf(dov[e], v0[e], dp);
+        }
+        s = row_sum(s);
+        dp = row_sum(dp);
+        const float p0 = valid ? exp2f((s * scale - lse_v[b]) * kLog2e) : 0.f;
+        const float ds0 = p0 * (dp - dsum);
+        const float sd = scale * ds0;
+        if (valid) {
+          acc[0] = make_float4(sd * k0[0], sd * k0[1], sd * k0[2], sd * k0[3]);
+          acc[1] = make_float4(sd * k0[4], sd * k0[5], sd * k0[6], sd * k0[7]);
+        }
 #pragma unroll
-      for (int e = 0; e < EPL; ++e) {
-        s = fmaf(qv[e], k0[e], s);
-        dp = fmaf(dov[e], v0[e], dp);
+        for (int e = 0; e < 8; ++e) {
+          pdv[e] = fmaf(p0, dov[e], pdv[e]);
+          pdk[e] = fmaf(sd, qv[e], pdk[e]);
+        }
+      } else if (valid) {
+        acc[0] = make_float4(0.f, 0.f, 0.f, 0.f);
+        acc[1] = make_float4(0.f, 0.f, 0.f, 0.f);
       }
-#pragma unroll
-      for (int sh = 16; sh > 0; sh >>= 1) {
-        s += __shfl_xor_sync(0xffffffffu, s, sh);
-        dp += __shfl_xor_sync(0xffffffffu, dp, sh);
-      }
-      const float p0 = exp2f((s * scale - __ldg(lse + (size_t)h * T + i)) * kLog2e);
-      const float ds0 = p0 * (dp - dsum);
-#pragma unroll
-      for (int e = 0; e < EPL; ++e) {
-        acc[e] = scale * ds0 * k0[e];
-        pdv[e] = fmaf(p0, dov[e], pdv[e]);
-        pdk[e] = fmaf(scale * ds0, qv[e], pdk[e]);
-      }
-    } else {
-#pragma unroll
-      for (int e = 0; e < EPL; ++e) acc[e] = 0.f;
     }
   }
   if (!anchor) return;
+  // fold the warp's row slots (same channels), then the warps in a fixed order
 #pragma unroll
-  for (int e = 0; e < EPL; ++e) {
-    red_dv[warp][lane * EPL + e] = pdv[e];
-    red_dk[warp][lane * EPL + e] = pdk[e];
+  for (int e = 0; e < 8; ++e) {
+#pragma unroll
+    for (int s = LPR; s < 32; s <<= 1) {
+      pdv[e] += __shfl_xor_sync(0xffffffffu, pdv[e], s);
+      pdk[e] += __shfl_xor_sync(0xffffffffu, pdk[e], s);
+    }
+  }
+  if (sub == 0) {
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      red_dv[warp][c0 + e] = pdv[e];
+      red_dk[warp][c0 + e] = pdk[e];
+    }
   }
   __syncthreads();
   for (int c = threadIdx.x; c < HD; c += blockDim.x) {
-    const float sdv = ((red_dv[0][c] + red_dv[1][c]) + red_dv[2][c]) + red_dv[3][c];
-    const float sdk = ((red_dk[0][c] + red_dk[1][c]) + red_dk[2][c]) + red_dk[3][c];
-    ws.part_dv[((size_t)blockIdx.x * Hq + h) * HD + c] = sdv;
-    ws.part_dk[((size_t)blockIdx.x * Hq + h) * HD + c] = sdk;
+    float sdv = 0.f, sdk = 0.f;
+#pragma unroll
+    for (int w = 0; w < NW; ++w) {
+      sdv += red_dv[w][c];
+      sdk += red_dk[w][c];
+    }
+    ws.part_dv[((size_t)blockIdx.y * Hq + h) * HD + c] = sdv;
+    ws.part_dk[((size_t)blockIdx.y * Hq + h) * HD + c] = sdk;
   }
 }
 
@@ -613,48 +642,76 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 }
 
 // ---------------------------------------------------------------- 3. dq
+// quads = D/8 threads per [T*H] row, each on one channel quad (4 rotation
+// pairs, 32 bytes of fp32); a thread takes NB rows per pass and issues all
+// their loads first. The rotations of the pass's tokens are composed once
+// into shared memory and shared by the token's heads (composing them per row
+// made the table lookups, not HBM, the limit).
+constexpr int kFinNB = 4;
+
+template <int HD>
 __global__ void __launch_bounds__(256) dq_finalize_kernel(const float* __restrict__ acc, __nv_bfloat16* __restrict__ dq,
                                                           const int32_t* __restrict__ pos_id,
                                                           const float2* __restrict__ hi_tab,
-                                                          const float2* __restrict__ lo_tab, int64_t T, int H,
-                                                          int D, int layout) {
-  const int half = D / 2, quads = half / 4;
-  const int64_t n = T * H * quads;
-  for (int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; idx < n; idx += (int64_t)gridDim.x * blockDim.x) {
-    const int qd = (int)(idx % quads);
-    const int64_t row = idx / quads;
-    const int pos = __ldg(pos_id + row / H);
-    const float* a = acc + row * D;
-    __nv_bfloat16* y = dq + row * D;
-    float x0[4], x1[4];
-    if (layout == 1) {
-      const float4 u = *reinterpret_cast<const float4*>(a + qd * 4);
-      const float4 w = *reinterpret_cast<const float4*>(a + half + qd * 4);
-      x0[0] = u.x; x0[1] = u.y; x0[2] = u.z; x0[3] = u.w;
-      x1[0] = w.x; x1[1] = w.y; x1[2] = w.z; x1[3] = w.w;
-    } else {
-      const float4 u = *reinterpret_cast<const float4*>(a + qd * 8);
-      const float4 w = *reinterpret_cast<const float4*>(a + qd * 8 + 4);
-      x0[0] = u.x; x1[0] = u.y; x0[1] = u.z; x1[1] = u.w;
-      x0[2] = w.x; x1[2] = w.y; x0[3] = w.z; x1[3] = w.w;
-    }
-    if (layout != 2) {
+                                                          const float2* __restrict__ lo_tab, int rows, int H,
+                                                          int layout) {
+  constexpr int half = HD / 2, quads = half / 4;
+  constexpr int RPB = 256 / quads;          // rows per block sub-pass
+  constexpr int PASS = kFinNB * RPB;        // rows per pass: at most PASS tokens
+  __shared__ float2 cs_s[PASS][half];
+  const int qd = threadIdx.x % quads, rsub = threadIdx.x / quads;
+  for (int r0 = blockIdx.x * PASS; r0 < rows; r0 += gridDim.x * PASS) {
+    float4 u[kFinNB], w[kFinNB];
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const float2 cs = rope_cs(hi_tab, lo_tab, pos, qd * 4 + e, half);
-        rope_pair(x0[e], x1[e], cs.x, -cs.y);
+    for (int b = 0; b < kFinNB; ++b) {
+      const float* a = acc + (size_t)min(r0 + b * RPB + rsub, rows - 1) * HD;
+      if (layout == 1) {
+        u[b] = *reinterpret_cast<const float4*>(a + qd * 4);
+        w[b] = *reinterpret_cast<const float4*>(a + half + qd * 4);
+      } else {
+        u[b] = *reinterpret_cast<const float4*>(a + qd * 8);
+        w[b] = *reinterpret_cast<const float4*>(a + qd * 8 + 4);
       }
     }
-    if (layout == 1) {
-      *reinterpret_cast<uint2*>(y + qd * 4) =
-          make_uint2(ptx::pack_bf16x2(x0[0], x0[1]), ptx::pack_bf16x2(x0[2], x0[3]));
-      *reinterpret_cast<uint2*>(y + half + qd * 4) =
-          make_uint2(ptx::pack_bf16x2(x1[0], x1[1]), ptx::pack_bf16x2(x1[2], x1[3]));
-    } else {
-      *reinterpret_cast<uint4*>(y + qd * 8) =
-          make_uint4(ptx::pack_bf16x2(x0[0], x1[0]), ptx::pack_bf16x2(x0[1], x1[1]), ptx::pack_bf16x2(x0[2], x1[2]),
-                     ptx::pack_bf16x2(x0[3], x1[3]));
+    const int t_first = r0 / H;
+    if (layout != 2) {
+      const int n = (min(r0 + PASS, rows) - 1) / H - t_first + 1;
+      for (int e = threadIdx.x; e < n * half; e += blockDim.x) {
+        const int tt = e / half, pr = e % half;
+        cs_s[tt][pr] = rope_cs(hi_tab, lo_tab, __ldg(pos_id + t_first + tt), pr, half);
+      }
+      __syncthreads();
     }
+#pragma unroll
+    for (int b = 0; b < kFinNB; ++b) {
+      const int row = r0 + b * RPB + rsub;
+      if (row >= rows) break;
+      __nv_bfloat16* y = dq + (size_t)row * HD;
+      float x0[4], x1[4];
+      if (layout == 1) {
+        x0[0] = u[b].x; x0[1] = u[b].y; x0[2] = u[b].z; x0[3] = u[b].w;
+        x1[0] = w[b].x; x1[1] = w[b].y; x1[2] = w[b].z; x1[3] = w[b].w;
+      } else {
+        x0[0] = u[b].x; x1[0] = u[b].y; x0[1] = u[b].z; x1[1] = u[b].w;
+        x0[2] = w[b].x; x1[2] = w[b].y; x0[3] = w[b].z; x1[3] = w[b].w;
+      }
+      if (layout != 2) {
+        const float2* cs = cs_s[row / H - t_first] + qd * 4;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) rope_pair(x0[e], x1[e], cs[e].x, -cs[e].y);
+      }
+      if (layout == 1) {
+        *reinterpret_cast<uint2*>(y + qd * 4) =
+            make_uint2(ptx::pack_bf16x2(x0[0], x0[1]), ptx::pack_bf16x2(x0[2], x0[3]));
+        *reinterpret_cast<uint2*>(y + half + qd * 4) =
+            make_uint2(ptx::pack_bf16x2(x1[0], x1[1]), ptx::pack_bf16x2(x1[2], x1[3]));
+      } else {
+        *reinterpret_cast<uint4*>(y + qd * 8) =
+            make_uint4(ptx::pack_bf16x2(x0[0], x1[0]), ptx::pack_bf16x2(x0[1], x1[1]),
+                       ptx::pack_bf16x2(x0[2], x1[2]), ptx::pack_bf16x2(x0[3], x1[3]));
+      }
+    }
+    if (layout != 2) __syncthreads();  // cs_s is rewritten by the next pass
   }
 }
 
@@ -710,11 +767,10 @@ aa_status launch_bwd(aa_plan_s* p, const void* q, const void* k, const void* v, 
     qr = ws.qr;
     kr = ws.kr;
   }
-  bwd_prep_kernel<HD><<<dim3(kPrepChunks, p->Hq), 128, 0, s>>>(
-      static_cast<const __nv_bfloat16*>(qr), static_cast<const __nv_bfloat16*>(k),
+  bwd_prep_kernel<HD><<<dim3(p->Hq, kPrepChunks), kPrepThreads, 0, s>>>(
+      static_cast<const __nv_bfloat16*>(qr), static_cast<const __nv_bfloat16*>(kr),
       static_cast<const __nv_bfloat16*>(v), static_cast<const __nv_bfloat16*>(o),
-      static_cast<const __nv_bfloat16*>(dout), lse, ws, p->dev.pos_id, p->dev.rope_hi, p->dev.rope_lo, p->T, p->Hq,
-      p->group, rope_layout, p->anchor ? 1 : 0, p->scale);
+      static_cast<const __nv_bfloat16*>(dout), lse, ws, p->T, p->Hq, p->group, p->anchor ? 1 : 0, p->scale);
   if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(e, "bwd_prep_kernel launch");
 
   CUtensorMap tq, tk, tv, tdo;
@@ -754,10 +810,17 @@ aa_status launch_bwd(aa_plan_s* p, const void* q, const void* k, const void* v, 
   if (p->bwd_ev_stop && (e = cudaEventRecord(p->bwd_ev_stop, s)) != cudaSuccess)
     return cuda_fail(e, "recording the bwd stop event");
 
-  const int64_t n = (int64_t)p->T * p->Hq * (HD / 8);
-  int64_t blocks = std::min<int64_t>((n + 255) / 256, (int64_t)p->num_sms * 8);
-  dq_finalize_kernel<<<(unsigned)blocks, 256, 0, s>>>(ws.dq_acc, static_cast<__nv_bfloat16*>(dq), p->dev.pos_id,
-                                                      p->dev.rope_hi, p->dev.rope_lo, p->T, p->Hq, HD, rope_layout);
+  // one full wave of resident blocks, grid-striding over the rows
+  static int fin_occ[2] = {0, 0};
+  int& occ = fin_occ[HD == 128];
+  if (occ == 0 && cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, dq_finalize_kernel<HD>, 256, 0) != cudaSuccess)
+    occ = 4;
+  const int rows = p->T * p->Hq;  // below 2^31: the plan checks T * Hq
+  const int per_block = kFinNB * (256 / (HD / 8));
+  const int64_t blocks = std::min<int64_t>((rows + per_block - 1) / per_block, (int64_t)p->num_sms * std::max(occ, 1));
+  dq_finalize_kernel<HD><<<(unsigned)blocks, 256, 0, s>>>(ws.dq_acc, static_cast<__nv_bfloat16*>(dq),
+                                                          p->dev.pos_id, p->dev.rope_hi, p->dev.rope_lo, rows,
+                                                          p->Hq, rope_layout);
   if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(e, "dq_finalize_kernel launch");
   if (p->anchor) {
     anchor_finalize_kernel<<<p->Hkv, 128, 2 * HD * sizeof(float), s>>>(
