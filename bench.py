@@ -124,6 +124,22 @@ def _barrier(world):
         torch.cuda.synchronize()
 
 
+def _captured_traffic(key):
+    """DRAM bytes per launch of the dominant kernel from the committed ncu capture
+    (profiles/traffic.json), or None when there is none or the kernel's source has
+    changed since the counters were taken."""
+    import hashlib
+    tpath = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        rec = json.load(open(tpath)).get(key)
+        src = open(os.path.join(ROOT, rec["kernel_source"]), "rb").read()
+        if hashlib.sha256(src).hexdigest() != rec["source_sha256"]:
+            return None
+        return int(rec["bytes"])
+    except Exception:
+        return None
+
+
 # ----------------------------------------------------------------------------- our path
 def run_ours(args):
     import torch
@@ -207,13 +223,7 @@ def run_ours(args):
     if fwd_ms > bwd_main_ms:
         dom_flops, dom_ms, dom_name = flops_fwd, fwd_ms, "attn_fwd_kernel"
     achieved = dom_flops / (dom_ms * 1e-3) / 1e12
-    traffic = None
-    tpath = os.path.join(ROOT, "profiles", "traffic.json")
-    if os.path.exists(tpath):
-        try:
-            traffic = json.load(open(tpath)).get(f"{args.workload}:{dom_name}")
-        except Exception:
-            traffic = None
+    traffic = _captured_traffic(f"{args.workload}:{dom_name}")
 
     extra = {}
     if args.compare_causal and mask != aa.MASK_CAUSAL and rank == 0:

@@ -173,8 +173,10 @@ aa_status aa_bwd(aa_plan_t plan, const void* q, const void* k, const void* v, co
  * it (held until the process exits) and allocates nothing itself.
  *  - Arguments and results are those of aa_bwd minus the workspace pair.
  *  - Plans whose aa_bwd_workspace_bytes() exceeds 64 MiB are rejected with
- *    AA_ERR_INVALID_ARG and a message giving both sizes (roughly T * Hq up to
- *    120K query rows at D = 128); nothing is launched.
+ *    AA_ERR_INVALID_ARG and a message giving both sizes; nothing is launched.
+ *    With RoPE at D = 128 a query row needs about 1 KB (rotated Q and K and
+ *    the fp32 dQ accumulator) and each query head 0.25 MiB of anchor
+ *    partials, so T * Hq up to about 55K query rows fit.
  *  - The plan's device must be current. The first call on a device looks up
  *    the array's device address (cudaGetSymbolAddress) once; make that first
  *    call before any stream capture on that device.
