@@ -13,6 +13,9 @@
  *                       Anchor Design", "Core design" and "Mask construction".
  *   [ARCH §3.2]         architecture page, §3.2 "Big-Picture Architecture":
  *                       RoPE in fp32, cast to bf16, inner products in bf16.
+ *   [ARCH §3.4 Diag]    architecture page, §3.4 "Diagnostic Methodology:
+ *                       Measuring the Breakdown", Eq. 4 (attention difference)
+ *                       and Eq. 5 (first-token logit difference).
  *
  * Conventions shared by every entry point
  * ---------------------------------------
@@ -214,6 +217,32 @@ aa_status aa_set_bwd_timing_events(aa_plan_t plan, void* start, void* stop);
  * aa_check_device_error() returns AA_ERR_TIMEOUT. This is the same bounded
  * wait every attention kernel uses. */
 aa_status aa_selftest_bounded_wait(aa_plan_t plan, aa_stream_t stream);
+
+/* Shift-discrepancy diagnostics. [ARCH §3.4 Diag], [ARCH §3.4 RoPE] (Eq. 3)
+ * Two plans that differ only in pos_shift (Δ1 for plan1, Δ2 for plan2) and one
+ * un-rotated input q [T, Hq, D], k [T, Hkv, D] (bf16). The library rotates q
+ * and k under both shifts with its own RoPE kernel (the bf16 operands its
+ * attention uses) and computes, with the plans' mask:
+ *   col_absdiff[h][j]         = sum_i |ATTN_ij(Δ1) - ATTN_ij(Δ2)|   (fp32 [Hq, T])
+ *   first_logit_absdiff[h][i] = |A_i0(Δ1) - A_i0(Δ2)|              (fp32 [Hq, T])
+ *     (0 for rows that cannot see token 0), A = scale * q~_i . k~_j the
+ *     pre-softmax logit, ATTN = softmax of A over the visible keys;
+ *   result (fp64, 2 + 2*Hq):  result[0] = D (Eq. 4) = sum_h sum_j
+ *     col_absdiff[h][j] / n_j with n_j the rows that may attend to key j;
+ *     result[1] = D_logit (Eq. 5) = (1/T) sum_h sum_i first_logit_absdiff[h][i];
+ *     result[2 + 2h], result[3 + 2h] = head h's two sums.
+ * Under exact arithmetic both are zero (Eq. 3); what they measure here is the
+ * bf16 rounding of the rotated operands. The logits are recomputed on CUDA
+ * cores in fp32 (an evaluation tool, not a training-step kernel); the column
+ * sums use atomics, so their last bits can vary run to run.
+ * workspace: aa_shift_diag_workspace_bytes(plan1) bytes (rotated Q and K under
+ * both shifts; 0 without RoPE), 16-byte aligned device memory. Errors: plans
+ * that differ in anything but pos_shift, a host-only plan, NULL or unaligned
+ * pointers, or a short workspace give AA_ERR_INVALID_ARG before any launch. */
+size_t aa_shift_diag_workspace_bytes(aa_plan_t plan);
+aa_status aa_shift_diag(aa_plan_t plan1, aa_plan_t plan2, const void* q, const void* k, float* col_absdiff,
+                        float* first_logit_absdiff, double* result, void* workspace, size_t workspace_bytes,
+                        aa_stream_t stream);
 
 const char* aa_status_string(aa_status status);
 const char* aa_last_error(void);

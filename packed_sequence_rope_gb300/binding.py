@@ -24,7 +24,7 @@ STATUS = {0: "AA_OK", 1: "AA_ERR_INVALID_ARG", 2: "AA_ERR_UNSUPPORTED", 3: "AA_E
 EXPORTS = ["aa_plan", "aa_plan_destroy", "aa_plan_metadata", "aa_plan_stats", "aa_plan_work",
            "aa_rope_apply", "aa_fwd", "aa_fwd_workspace_bytes", "aa_bwd_workspace_bytes", "aa_bwd", "aa_bwd_static_workspace", "aa_check_device_error",
            "aa_set_wait_limit", "aa_set_bwd_timing_events", "aa_selftest_bounded_wait", "aa_status_string",
-           "aa_last_error"]
+           "aa_last_error", "aa_shift_diag_workspace_bytes", "aa_shift_diag"]
 
 
 class AAConfig(ctypes.Structure):
@@ -72,6 +72,8 @@ def lib():
             "aa_selftest_bounded_wait": ([vp, vp], ctypes.c_int),
             "aa_status_string": ([ctypes.c_int], ctypes.c_char_p),
             "aa_last_error": ([], ctypes.c_char_p),
+            "aa_shift_diag_workspace_bytes": ([vp], ctypes.c_size_t),
+            "aa_shift_diag": ([vp, vp, vp, vp, vp, vp, vp, vp, ctypes.c_size_t, vp], ctypes.c_int),
         }
         for name, (args, res) in sig.items():
             f = getattr(L, name)
@@ -216,6 +218,23 @@ class Plan:
                             _ptr(dq), _ptr(dk), _ptr(dv), _ptr(ws), ctypes.c_size_t(ws.numel()),
                             _stream(stream)))
         return dq, dk, dv
+
+    def shift_diag(self, other, q, k, workspace=None, stream=None):
+        """aa_shift_diag: Eq. 4 / Eq. 5 shift discrepancies between this plan's
+        pos_shift and ``other``'s (same problem otherwise) for un-rotated q, k.
+        Returns (col [Hq, T], first [Hq, T], result) with result = float64
+        [D, D_logit, D_0, L_0, D_1, L_1, ...] on the device."""
+        import torch
+        for t in (q, k):
+            assert t.is_cuda and t.dtype == torch.bfloat16 and t.is_contiguous()
+        col = torch.empty(self.Hq, self.T, device=q.device, dtype=torch.float32)
+        first = torch.empty_like(col)
+        res = torch.empty(2 + 2 * self.Hq, device=q.device, dtype=torch.float64)
+        need = int(lib().aa_shift_diag_workspace_bytes(self._h))
+        ws = torch.empty(max(need, 256), device=q.device, dtype=torch.uint8) if workspace is None else workspace
+        _check(lib().aa_shift_diag(self._h, other._h, _ptr(q), _ptr(k), _ptr(col), _ptr(first), _ptr(res),
+                                   _ptr(ws), ctypes.c_size_t(ws.numel()), _stream(stream)))
+        return col, first, res
 
     def bwd_static_workspace(self, q, k, v, o, lse, dout, dq=None, dk=None, dv=None, stream=None):
         """aa_bwd_static_workspace: the backward pass with the library's static
