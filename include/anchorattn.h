@@ -105,6 +105,19 @@ typedef struct aa_plan_s* aa_plan_t;
 aa_status aa_plan(const aa_config* cfg, const int32_t* cu_doclens_host, int32_t num_docs,
                   aa_stream_t stream, aa_plan_t* out);
 
+/* aa_plan with caller-supplied rotation frequencies: theta (host double[D/2])
+ * replaces Eq. 6's theta_p = rope_base^(-2p/D) for every pair p [ARCH §3.4
+ * RoPE]; cfg->rope_base is then ignored. This carries the frequency tables of
+ * RoPE variants such as NTK-aware scaling or YaRN, which the pages compare
+ * with vanilla RoPE for 64K training (architecture page, §3.4 "Long-Context
+ * Training Protocol", "Vanilla RoPE vs. NTK vs. YaRN", Table 2) without
+ * defining their formulas: the caller computes the table, the library
+ * rotates with it (fp64 tables, fp32 rotation, bf16 operands, as for the
+ * default). The table is copied. Errors: NULL theta, or an entry that is not
+ * finite and >= 0, gives AA_ERR_INVALID_ARG; otherwise as aa_plan. */
+aa_status aa_plan_with_theta(const aa_config* cfg, const int32_t* cu_doclens_host, int32_t num_docs,
+                             const double* theta, aa_stream_t stream, aa_plan_t* out);
+
 /* Free a plan (synchronises the device). NULL is accepted. */
 aa_status aa_plan_destroy(aa_plan_t plan);
 

@@ -152,17 +152,19 @@ def rope_theta(d: int, base: float) -> np.ndarray:
     return np.power(float(base), -2.0 * p / d)
 
 
-def rotate(x, pos, base: float, layout: int = ROPE_ADJACENT, inverse: bool = False):
+def rotate(x, pos, base: float, layout: int = ROPE_ADJACENT, inverse: bool = False, theta=None):
     """Apply R_{pos,theta} (or its transpose) to x [T, H, d]; float64 out.
 
     ADJACENT pairs coordinates (2p, 2p+1) exactly as Eq. 6; HALF pairs
-    (p, p + d/2); NONE returns x unchanged. Angles are pos * theta_p in fp64.
+    (p, p + d/2); NONE returns x unchanged. Angles are pos * theta_p in fp64,
+    theta_p = base^(-2p/d) unless an explicit table ``theta`` [d/2] is given
+    (a RoPE variant's frequencies: Eq. 6 with other theta_p).
     """
     x = np.asarray(x, dtype=np.float64)
     if layout == ROPE_NONE:
         return x.copy()
     T, H, d = x.shape
-    theta = rope_theta(d, base)
+    theta = rope_theta(d, base) if theta is None else np.asarray(theta, dtype=np.float64)
     ang = np.asarray(pos, dtype=np.float64)[:, None] * theta[None, :]   # [T, d/2]
     c = np.cos(ang)[:, None, :]
     s = np.sin(ang)[:, None, :]
@@ -189,7 +191,7 @@ class Problem:
 
     def __init__(self, cu_doclens, T, num_q_heads, num_kv_heads, head_dim,
                  rope_base=1e4, mask_mode=MASK_ANCHOR, pos_mode=POS_RESET,
-                 rope_layout=ROPE_ADJACENT, softmax_scale=None, pos_shift=0):
+                 rope_layout=ROPE_ADJACENT, softmax_scale=None, pos_shift=0, theta=None):
         if num_q_heads % num_kv_heads:
             raise ValueError("query heads must be a multiple of kv heads")
         self.T, self.Hq, self.Hkv, self.d = T, num_q_heads, num_kv_heads, head_dim
@@ -200,14 +202,15 @@ class Problem:
         self.cu = None if mask_mode == MASK_CAUSAL else _check_cu(cu_doclens, T)
         self.doc = document_ids(cu_doclens, T, mask_mode)
         self.pos = position_ids(cu_doclens, T, mask_mode, pos_mode, pos_shift)
+        self.theta = None if theta is None else np.asarray(theta, dtype=np.float64)
 
     def kv_head(self, h):
         """Grouped-query mapping: query head h reads kv head floor(h * Hkv / Hq)."""
         return (h * self.Hkv) // self.Hq
 
     def rotated(self, q, k):
-        qr = rotate(np.asarray(q, np.float64), self.pos, self.base, self.layout)
-        kr = rotate(np.asarray(k, np.float64), self.pos, self.base, self.layout)
+        qr = rotate(np.asarray(q, np.float64), self.pos, self.base, self.layout, theta=self.theta)
+        kr = rotate(np.asarray(k, np.float64), self.pos, self.base, self.layout, theta=self.theta)
         return qr, kr
 
 
@@ -276,6 +279,6 @@ def backward(prob: Problem, q, k, v, dout, rows=None):
         dS = P * (dP - (P * dP).sum(axis=1, keepdims=True))
         dqr[rows, h, :] = prob.scale * (dS @ kr[:, g, :])
         dkr[:, g, :] += prob.scale * (dS.T @ qr[rows, h, :])
-    dq = rotate(dqr, prob.pos, prob.base, prob.layout, inverse=True)
-    dk = rotate(dkr, prob.pos, prob.base, prob.layout, inverse=True)
+    dq = rotate(dqr, prob.pos, prob.base, prob.layout, inverse=True, theta=prob.theta)
+    dk = rotate(dkr, prob.pos, prob.base, prob.layout, inverse=True, theta=prob.theta)
     return dq, dk, dv

@@ -40,8 +40,8 @@ def round_to_bf16(x) -> np.ndarray:
 
 
 def _rotated(prob: Problem, q, k, bf16_operands: bool):
-    qr = rotate(q, prob.pos, prob.base, prob.layout)
-    kr = rotate(k, prob.pos, prob.base, prob.layout)
+    qr = rotate(q, prob.pos, prob.base, prob.layout, theta=prob.theta)
+    kr = rotate(k, prob.pos, prob.base, prob.layout, theta=prob.theta)
     if bf16_operands:
         qr, kr = round_to_bf16(qr), round_to_bf16(kr)
     return qr, kr

@@ -47,6 +47,7 @@ struct aa_plan_s {
   std::vector<int32_t> doc_id, pos_id, row_lo, key_hi;
   std::vector<aa::WorkItem> fwd_items, bwd_items;  // fwd: one item per (query-tile pair, head)
   std::vector<int32_t> qtile_klo;
+  std::vector<double> theta;    // [D/2] rotation frequency of each pair (Eq. 6's theta_p)
   std::vector<float2> rope_hi, rope_lo, rope_step;
   int32_t n_hi = 0;
   int64_t unmasked_pairs = 0, live_tiles = 0, causal_tiles = 0;

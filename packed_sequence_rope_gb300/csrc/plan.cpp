@@ -180,9 +180,7 @@ static void build_rope_tables(aa_plan_s* p) {
   int max_pos = 0;
   for (int v : p->pos_id) max_pos = std::max(max_pos, v);
   p->n_hi = max_pos / kRopeSplit + 1;
-  std::vector<double> theta(half);
-  for (int i = 0; i < half; ++i)
-    theta[i] = std::pow(p->cfg.rope_base, -2.0 * (double)i / (double)p->D);
+  const std::vector<double>& theta = p->theta;
   p->rope_hi.resize((size_t)p->n_hi * half);
   p->rope_lo.resize((size_t)kRopeSplit * half);
   for (int h = 0; h < p->n_hi; ++h)
@@ -225,7 +223,7 @@ static void free_device(aa_plan_s* p) {
   d = DevicePlan{};
 }
 
-static aa_status validate(const aa_config* c, const int32_t* cu, int32_t num_docs) {
+static aa_status validate(const aa_config* c, const int32_t* cu, int32_t num_docs, const double* theta) {
   if (!c) return fail(AA_ERR_INVALID_ARG, "config is NULL");
   if (c->total_tokens < 2 || c->total_tokens >= (1 << 30))
     return fail(AA_ERR_INVALID_ARG, "total_tokens must be in [2, 2^30)");
@@ -241,8 +239,13 @@ static aa_status validate(const aa_config* c, const int32_t* cu, int32_t num_doc
     return fail(AA_ERR_INVALID_ARG, "unknown pos_mode");
   if (c->rope_layout < AA_ROPE_ADJACENT || c->rope_layout > AA_ROPE_NONE)
     return fail(AA_ERR_INVALID_ARG, "unknown rope_layout");
-  if (c->rope_layout != AA_ROPE_NONE && !(c->rope_base > 1.0 && std::isfinite(c->rope_base)))
+  if (theta) {
+    for (int i = 0; i < c->head_dim / 2; ++i)
+      if (!(theta[i] >= 0.0 && std::isfinite(theta[i])))
+        return fail(AA_ERR_INVALID_ARG, "theta[" + std::to_string(i) + "] must be finite and >= 0");
+  } else if (c->rope_layout != AA_ROPE_NONE && !(c->rope_base > 1.0 && std::isfinite(c->rope_base))) {
     return fail(AA_ERR_INVALID_ARG, "rope_base must be finite and > 1");
+  }
   if (c->pos_shift < 0 || (int64_t)c->pos_shift + c->total_tokens >= (1ll << 30))
     return fail(AA_ERR_INVALID_ARG, "pos_shift must be >= 0 and keep positions below 2^30");
   if (!std::isfinite(c->softmax_scale)) return fail(AA_ERR_INVALID_ARG, "softmax_scale is not finite");
@@ -260,11 +263,11 @@ static aa_status validate(const aa_config* c, const int32_t* cu, int32_t num_doc
 
 using namespace aa;
 
-extern "C" aa_status aa_plan(const aa_config* cfg, const int32_t* cu_doclens_host, int32_t num_docs,
-                             aa_stream_t stream, aa_plan_t* out) {
+static aa_status make_plan(const aa_config* cfg, const int32_t* cu_doclens_host, int32_t num_docs,
+                           const double* theta, aa_stream_t stream, aa_plan_t* out) {
   if (!out) return fail(AA_ERR_INVALID_ARG, "out is NULL");
   *out = nullptr;
-  aa_status st = validate(cfg, cu_doclens_host, num_docs);
+  aa_status st = validate(cfg, cu_doclens_host, num_docs, theta);
   if (st != AA_OK) return st;
   aa_plan_s* p = new (std::nothrow) aa_plan_s();
   if (!p) return fail(AA_ERR_NO_MEMORY, "plan allocation");
@@ -279,6 +282,9 @@ extern "C" aa_status aa_plan(const aa_config* cfg, const int32_t* cu_doclens_hos
   p->anchor = cfg->mask_mode == AA_MASK_ANCHOR;
   p->host_only = cfg->host_only != 0;
   if (cfg->mask_mode != AA_MASK_CAUSAL) p->cu.assign(cu_doclens_host, cu_doclens_host + num_docs + 1);
+  p->theta.resize(p->D / 2);
+  for (int i = 0; i < p->D / 2; ++i)  // Eq. 6: theta_p = base^(-2p/D), unless the caller supplies them
+    p->theta[i] = theta ? theta[i] : std::pow(cfg->rope_base, -2.0 * (double)i / (double)p->D);
   build_token_metadata(p);
   build_stats_and_work(p);
   build_rope_tables(p);
@@ -319,6 +325,17 @@ extern "C" aa_status aa_plan(const aa_config* cfg, const int32_t* cu_doclens_hos
   }
   *out = p;
   return AA_OK;
+}
+
+extern "C" aa_status aa_plan(const aa_config* cfg, const int32_t* cu_doclens_host, int32_t num_docs,
+                             aa_stream_t stream, aa_plan_t* out) {
+  return make_plan(cfg, cu_doclens_host, num_docs, nullptr, stream, out);
+}
+
+extern "C" aa_status aa_plan_with_theta(const aa_config* cfg, const int32_t* cu_doclens_host, int32_t num_docs,
+                                        const double* theta, aa_stream_t stream, aa_plan_t* out) {
+  if (!theta) return fail(AA_ERR_INVALID_ARG, "theta is NULL (use aa_plan for base^(-2p/D))");
+  return make_plan(cfg, cu_doclens_host, num_docs, theta, stream, out);
 }
 
 extern "C" aa_status aa_plan_destroy(aa_plan_t p) {

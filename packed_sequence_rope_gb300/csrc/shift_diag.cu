@@ -200,7 +200,7 @@ __global__ void __launch_bounds__(kThreads) shift_diag_reduce_kernel(const float
 bool same_problem(const aa_plan_s* a, const aa_plan_s* b) {
   return a->T == b->T && a->Hq == b->Hq && a->Hkv == b->Hkv && a->D == b->D &&
          a->cfg.mask_mode == b->cfg.mask_mode && a->cfg.pos_mode == b->cfg.pos_mode &&
-         a->cfg.rope_layout == b->cfg.rope_layout && a->cfg.rope_base == b->cfg.rope_base && a->scale == b->scale &&
+         a->cfg.rope_layout == b->cfg.rope_layout && a->theta == b->theta && a->scale == b->scale &&
          a->cu == b->cu && a->device == b->device;
 }
 

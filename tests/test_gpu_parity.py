@@ -185,3 +185,54 @@ def test_full_size_backward_documents(aa):
         for nm, got, ref in (("dq", dq[a:b], gq[a:b]), ("dk", dk[a:b], gk[a:b]), ("dv", dv[a:b], gv[a:b])):
             e = rel_l2(got, ref)
             assert e <= REL_L2, f"doc {d} {nm} rel-L2 {e:.3e}"
+
+
+# --------------------------------------------------------------------------- explicit frequency tables
+def _scaled_theta(D, base):
+    # a non-default table: the lowest-frequency half of the pairs slowed down 8x
+    # (the kind of per-pair rescaling RoPE variants apply)
+    th = orc.rope_theta(D, base)
+    th[D // 4:] /= 8.0
+    return th
+
+
+@pytest.mark.parametrize("layout", [orc.ROPE_ADJACENT, orc.ROPE_HALF])
+def test_rope_apply_custom_theta_matches_oracle(aa, layout):
+    T, H, D = 600, 2, 128
+    cu = [1, 250, 600]
+    theta = _scaled_theta(D, 1e4)
+    x = torch.randn(T, H, D, device="cuda").to(torch.bfloat16)
+    with aa.Plan(cu, T, H, H, D, 1e4, orc.MASK_ANCHOR, orc.POS_CONTINUOUS, layout, pos_shift=3000,
+                 theta=theta) as p:
+        y = p.rope_apply(x)
+        torch.cuda.synchronize()
+    pos = orc.position_ids(cu, T, orc.MASK_ANCHOR, orc.POS_CONTINUOUS, 3000)
+    ref = orc.rotate(f64(x), pos, 1e4, layout, theta=theta)
+    assert (np.abs(f64(y) - ref) <= _rope_bound(ref, f64(x), layout)).all()
+
+
+def test_fwd_bwd_custom_theta_elementwise(aa):
+    cu, T, Hq, Hkv, D = [1, 77, 400, 700], 700, 2, 1, 128
+    theta = _scaled_theta(D, 5e5)
+    q, k, v, do = inputs(T, Hq, Hkv, D, seed=31)
+    with aa.Plan(cu, T, Hq, Hkv, D, 5e5, theta=theta) as p:
+        o, lse = p.fwd(q, k, v)
+        dq, dk, dv = p.bwd(q, k, v, o, lse, do)
+        torch.cuda.synchronize()
+        p.check_device_error()
+    prob = orc.Problem(cu, T, Hq, Hkv, D, 5e5, orc.MASK_ANCHOR, orc.POS_RESET, orc.ROPE_ADJACENT, theta=theta)
+    O, L = orc.forward(prob, q.cpu(), k.cpu(), v.cpu())
+    check_forward(o, lse, O, L, tag="custom_theta")
+    gq, gk, gv = orc.backward(prob, q.cpu(), k.cpu(), v.cpu(), do.cpu())
+    for nm, got, ref in (("dq", dq, gq), ("dk", dk, gk), ("dv", dv, gv)):
+        assert rel_l2(got, ref) <= REL_L2, nm
+
+
+def test_default_theta_table_is_bit_identical_to_base(aa):
+    cu, T, H, D = [1, 300, 500], 500, 2, 64
+    q, k, v, _ = inputs(T, H, H, D, seed=32)
+    with aa.Plan(cu, T, H, H, D, 1e4) as p0, aa.Plan(cu, T, H, H, D, 1e4, theta=orc.rope_theta(D, 1e4)) as p1:
+        o0, l0 = p0.fwd(q, k, v)
+        o1, l1 = p1.fwd(q, k, v)
+        torch.cuda.synchronize()
+    assert torch.equal(o0, o1) and torch.equal(l0, l1)

@@ -305,3 +305,42 @@ def test_backward_rows_subset_is_document_separable():
     assert np.allclose(dq[rows], dq2[rows], atol=1e-12)
     assert np.allclose(dk[25:], dk2[25:], atol=1e-12)
     assert np.allclose(dv[25:], dv2[25:], atol=1e-12)
+
+
+# --------------------------------------------------------------------------- explicit frequency tables
+def test_rotate_explicit_theta_equals_base_formula():
+    rng = np.random.default_rng(21)
+    x = rng.standard_normal((40, 2, 16))
+    pos = rng.integers(0, 5000, 40)
+    a = orc.rotate(x, pos, 5e5)
+    b = orc.rotate(x, pos, 123.0, theta=orc.rope_theta(16, 5e5))   # base ignored with a table
+    assert np.array_equal(a, b)
+
+
+def test_rotate_zero_theta_is_identity():
+    rng = np.random.default_rng(22)
+    x = rng.standard_normal((30, 1, 8))
+    assert np.array_equal(orc.rotate(x, np.arange(30) * 97, 1e4, theta=np.zeros(4)), x)
+
+
+def test_rotate_custom_theta_complex_form():
+    # each adjacent pair as a complex number times exp(i * pos * theta_p)
+    rng = np.random.default_rng(23)
+    theta = rng.uniform(1e-5, 2.0, 8)
+    x = rng.standard_normal((25, 3, 16))
+    pos = rng.integers(0, 100000, 25)
+    z = (x[..., 0::2] + 1j * x[..., 1::2]) * np.exp(1j * pos[:, None, None] * theta[None, None, :])
+    y = orc.rotate(x, pos, 1e4, theta=theta)
+    assert np.allclose(y[..., 0::2], z.real, atol=1e-12) and np.allclose(y[..., 1::2], z.imag, atol=1e-12)
+
+
+def test_custom_theta_keeps_shift_invariance():
+    # Eq. 3 holds for any frequency table: shifting every position leaves the output unchanged
+    rng = np.random.default_rng(24)
+    theta = rng.uniform(1e-6, 1.0, 8)
+    T, cu = 150, [1, 60, 150]
+    q, k, v = (rng.standard_normal((T, 2, 16)) for _ in range(3))
+    mk = lambda s: orc.Problem(cu, T, 2, 2, 16, 1e4, orc.MASK_ANCHOR, orc.POS_RESET, pos_shift=s, theta=theta)
+    O0, L0 = orc.forward(mk(0), q, k, v)
+    O1, L1 = orc.forward(mk(777), q, k, v)
+    assert np.allclose(O0, O1, atol=1e-10) and np.allclose(L0, L1, atol=1e-10)

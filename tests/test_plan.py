@@ -126,3 +126,25 @@ def test_workload_stats_vs_oracle(aa, name):
         assert st["unmasked_pairs"] == orc.unmasked_pairs(cu, T, orc.MASK_ANCHOR)
         if T <= 8192:
             assert st["live_tiles"] == orc.tile_counts(cu, T, orc.MASK_ANCHOR)[0]
+
+
+def test_plan_with_theta_validation_and_metadata(aa):
+    cu = [1, 40, 100]
+    theta = orc.rope_theta(64, 5e5)
+    with aa.Plan(cu, 100, 2, 1, 64, 1e4, host_only=True) as p0, \
+            aa.Plan(cu, 100, 2, 1, 64, 1e4, host_only=True, theta=theta) as p1:
+        assert all(np.array_equal(a, b) for a, b in zip(p0.metadata(), p1.metadata()))
+    # the table replaces rope_base, which is then not checked
+    with aa.Plan(cu, 100, 2, 1, 64, 0.5, host_only=True, theta=theta):
+        pass
+    for bad, msg in ((np.nan, "theta\\[3\\]"), (-1.0, "theta\\[3\\]"), (np.inf, "theta\\[3\\]")):
+        t = theta.copy()
+        t[3] = bad
+        with pytest.raises(aa.AAError, match=msg):
+            aa.Plan(cu, 100, 2, 1, 64, 1e4, host_only=True, theta=t)
+    with pytest.raises(ValueError, match="head_dim / 2"):
+        aa.Plan(cu, 100, 2, 1, 64, 1e4, host_only=True, theta=theta[:10])
+    L = aa.lib()
+    h = ctypes.c_void_p()
+    cfg = aa.binding.AAConfig(100, 2, 1, 64, 1e4, 0.0, 0, orc.MASK_CAUSAL, 0, 0, 1)
+    assert L.aa_plan_with_theta(ctypes.byref(cfg), None, 0, None, None, ctypes.byref(h)) == 1
