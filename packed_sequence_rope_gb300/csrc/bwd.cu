@@ -369,7 +369,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       for (int step = 0; step < n_steps && ok; ++step) {
         const int s = step & 1;
         const uint32_t sq = ptx::smem_u32(sm.q[s][0]), sdo = ptx::smem_u32(sm.dout[s][0]);
-        ok = bwd_wait(&sm.q_ready[s], (step >> 1) & 1, P, abort_flag, 412);
+        // the products need only the tiles; the LSE/D rows are for P/dS
+        ok = bwd_wait(&sm.qd_full[s], (step >> 1) & 1, P, abort_flag, 412);
         if (!ok) break;
         ptx::tc_fence_after();
         for (int kk = 0; kk < HD / 16; ++kk) {
@@ -492,7 +493,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     }
     if (ok) ok = bwd_wait(&sm.o_full, 0, P, abort_flag, 423);
     if (ok) {
-      // ---- epilogue (group 0: dV, group 1: dk = R^T (scale dK~)) for this thread's key row
+      // ---- epilogue: dV and dk = R^T (scale dK~) for this thread's key row
       ptx::tc_fence_after();
       __nv_bfloat16* dvrow = P.dv + ((size_t)(key_valid ? j : 0) * P.Hkv + g) * HD;
       __nv_bfloat16* dkrow = P.dk + ((size_t)(key_valid ? j : 0) * P.Hkv + g) * HD;
@@ -504,6 +505,47 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           dst[c] = make_uint4(ptx::pack_bf16x2(x[8 * c], x[8 * c + 1]), ptx::pack_bf16x2(x[8 * c + 2], x[8 * c + 3]),
                               ptx::pack_bf16x2(x[8 * c + 4], x[8 * c + 5]), ptx::pack_bf16x2(x[8 * c + 6], x[8 * c + 7]));
       };
+      // dk unit u: 32 channels (adjacent pairs or no rotation) or, for the
+      // half-split pairing, channels [32u, 32u + 32) with their partners D/2 on
+      auto dk_unit = [&](int u) {
+        if (P.layout != 1) {
+          float x[32];
+          ptx::tmem_ld32(t_dk + lane_off + u * 32, x);
+          ptx::tmem_wait_ld();
+          if (key_valid) {
+#pragma unroll
+            for (int e = 0; e < 32; ++e) x[e] *= P.scale;
+            if (P.layout == 0) {
+#pragma unroll
+              for (int e = 0; e < 32; e += 2) {
+                const float2 cs = rope_cs(P.rope_hi, P.rope_lo, pos, (u * 32 + e) >> 1, HD / 2);
+                rope_pair(x[e], x[e + 1], cs.x, -cs.y);
+              }
+            }
+            store32(dkrow, u * 32, x);
+          }
+        } else {
+          float x[32], y[32];
+          ptx::tmem_ld32(t_dk + lane_off + u * 32, x);
+          ptx::tmem_ld32(t_dk + lane_off + HD / 2 + u * 32, y);
+          ptx::tmem_wait_ld();
+          if (key_valid) {
+#pragma unroll
+            for (int e = 0; e < 32; ++e) {
+              x[e] *= P.scale;
+              y[e] *= P.scale;
+              const float2 cs = rope_cs(P.rope_hi, P.rope_lo, pos, u * 32 + e, HD / 2);
+              rope_pair(x[e], y[e], cs.x, -cs.y);
+            }
+            store32(dkrow, u * 32, x);
+            store32(dkrow, HD / 2 + u * 32, y);
+          }
+        }
+      };
+      // the rotated dk units cost several times a dv chunk (cos/sin table
+      // reads): group 0 writes dv and the first dk unit, group 1 the rest
+      const int n_dk = P.layout == 1 ? HD / 64 : HD / 32;
+      const int split = n_dk >= 2 ? 1 : 0;
       if (cq == 0) {
 #pragma unroll 1
         for (int c = 0; c < HD / 32; ++c) {
@@ -512,45 +554,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           ptx::tmem_wait_ld();
           if (key_valid) store32(dvrow, c * 32, x);
         }
-      } else if (P.layout != 1) {
 #pragma unroll 1
-        for (int c = 0; c < HD / 32; ++c) {
-          float x[32];
-          ptx::tmem_ld32(t_dk + lane_off + c * 32, x);
-          ptx::tmem_wait_ld();
-          if (key_valid) {
-#pragma unroll
-            for (int e = 0; e < 32; ++e) x[e] *= P.scale;
-            if (P.layout == 0) {
-#pragma unroll
-              for (int e = 0; e < 32; e += 2) {
-                const float2 cs = rope_cs(P.rope_hi, P.rope_lo, pos, (c * 32 + e) >> 1, HD / 2);
-                rope_pair(x[e], x[e + 1], cs.x, -cs.y);
-              }
-            }
-            store32(dkrow, c * 32, x);
-          }
-        }
+        for (int u = 0; u < split; ++u) dk_unit(u);
       } else {
-        // pairs (p, p + D/2): columns c*32.. meet columns D/2 + c*32..
 #pragma unroll 1
-        for (int c = 0; c < HD / 64; ++c) {
-          float x[32], y[32];
-          ptx::tmem_ld32(t_dk + lane_off + c * 32, x);
-          ptx::tmem_ld32(t_dk + lane_off + HD / 2 + c * 32, y);
-          ptx::tmem_wait_ld();
-          if (key_valid) {
-#pragma unroll
-            for (int e = 0; e < 32; ++e) {
-              x[e] *= P.scale;
-              y[e] *= P.scale;
-              const float2 cs = rope_cs(P.rope_hi, P.rope_lo, pos, c * 32 + e, HD / 2);
-              rope_pair(x[e], y[e], cs.x, -cs.y);
-            }
-            store32(dkrow, c * 32, x);
-            store32(dkrow, HD / 2 + c * 32, y);
-          }
-        }
+        for (int u = split; u < n_dk; ++u) dk_unit(u);
       }
     }
   } else if (warp >= 12) {
@@ -614,7 +622,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       ptx::mbar_arrive(&sm.dq_free);
     }
     if constexpr (HD == 128) {
-      if (r == 0) ptx::bulk_wait0();  // reductions land before the CTA exits
+      // the reductions must have read their shared-memory sources before the
+      // CTA exits; their global writes complete with the kernel
+      if (r == 0) ptx::bulk_wait_read0();
     }
   } else if (warp == 2 || warp == 3) {
     // ------------------------------------------------------------ RoPE + LSE/D staging
