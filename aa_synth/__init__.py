@@ -135,3 +135,29 @@ def make_qkv(w: Workload, device="cpu", with_grad_out: bool = True, seed_offset:
     v = gaussian_bf16((T, Hkv, d), s + 3, device)
     do = gaussian_bf16((T, Hq, d), s + 4, device) if with_grad_out else None
     return q, k, v, do
+
+
+def interleaved_chunks(lengths, chunks_per_doc: int, rng) -> np.ndarray:
+    """doc_of_token [1 + sum(lengths)] for documents split into chunks and
+    interleaved at random, each document's chunks kept in order (the
+    "interleaved chunks" data layout): 0 for the anchor token, document k
+    (1-based) for its tokens. Split points are uniform; the merge picks the
+    next chunk from a random document with chunks left, weighted by how many
+    it has left."""
+    pieces = []
+    for k, n in enumerate(lengths, start=1):
+        c = min(chunks_per_doc, n)
+        cuts = np.sort(rng.choice(np.arange(1, n), size=c - 1, replace=False)) if c > 1 else np.array([], int)
+        sizes = np.diff(np.concatenate([[0], cuts, [n]]))
+        pieces.append([(k, int(sz)) for sz in sizes])
+    out = [0]
+    left = [len(p) for p in pieces]
+    nxt = [0] * len(pieces)
+    while sum(left):
+        w = np.asarray(left, dtype=np.float64)
+        d = int(rng.choice(len(pieces), p=w / w.sum()))
+        k, sz = pieces[d][nxt[d]]
+        out.extend([k] * sz)
+        nxt[d] += 1
+        left[d] -= 1
+    return np.asarray(out, dtype=np.int32)

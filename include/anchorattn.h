@@ -118,6 +118,28 @@ aa_status aa_plan(const aa_config* cfg, const int32_t* cu_doclens_host, int32_t 
 aa_status aa_plan_with_theta(const aa_config* cfg, const int32_t* cu_doclens_host, int32_t num_docs,
                              const double* theta, aa_stream_t stream, aa_plan_t* out);
 
+/* Plan for documents given per token, possibly in interleaved chunks
+ * [ARCH §3.4 Anchor "Mask construction"]; architecture page, §3.4
+ * "AnchorAttention with Interleaved Chunks" (documents split into chunks that
+ * are shuffled and recombined with the order inside each document kept).
+ * doc_of_token: host int32[T]; token 0 is the anchor and must be 0, every
+ * other token names its document with an id >= 1 (any values; chunks of one
+ * document share an id, so they see each other; give each chunk its own id
+ * to keep chunks apart). A token sees the anchor (ANCHOR mode) and the tokens
+ * j <= i of its own document. Positions: RESET counts 1, 2, ... through the
+ * document's tokens in order, CONTINUOUS is the token index; pos_shift adds.
+ * cfg->mask_mode must be ANCHOR or INTRA_DOC. aa_fwd / aa_bwd /
+ * aa_bwd_static_workspace / aa_rope_apply take and return tensors in the
+ * caller's token order (the library groups the tokens by document, runs its
+ * kernels and scatters the results back; the workspace sizes include the
+ * grouped copies); aa_plan_metadata returns the caller's document ids and
+ * positions; aa_plan_stats / aa_plan_work count the grouped layout's tiles.
+ * aa_shift_diag refuses segment plans (AA_ERR_UNSUPPORTED). Errors: NULL
+ * doc_of_token, doc_of_token[0] != 0, an id < 1 after it, or the aa_plan
+ * conditions give AA_ERR_INVALID_ARG. */
+aa_status aa_plan_segments(const aa_config* cfg, const int32_t* doc_of_token_host, aa_stream_t stream,
+                           aa_plan_t* out);
+
 /* Free a plan (synchronises the device). NULL is accepted. */
 aa_status aa_plan_destroy(aa_plan_t plan);
 

@@ -92,6 +92,27 @@ def position_ids(cu_doclens, T: int, mask_mode: int, pos_mode: int,
     return pos + int(pos_shift)
 
 
+def segment_position_ids(doc_of_token, pos_mode: int, pos_shift: int = 0) -> np.ndarray:
+    """Positions for documents given per token (interleaved chunks).
+
+    Architecture page, §3.4 "AnchorAttention with Interleaved Chunks": chunks
+    of one document keep their order, so a document's tokens are its tokens
+    in sequence order. RESET ("Document Token Indexing", Fig. 2 middle)
+    counts 1, 2, ... through them; CONTINUOUS is the token index; the anchor
+    (token 0) is at 0. ``pos_shift`` adds to every position (Eq. 3).
+    """
+    doc = np.asarray(doc_of_token, dtype=np.int64)
+    T = doc.size
+    if pos_mode == POS_CONTINUOUS:
+        return np.arange(T, dtype=np.int64) + pos_shift
+    pos = np.zeros(T, dtype=np.int64)
+    seen = {}
+    for i in range(1, T):
+        seen[doc[i]] = seen.get(doc[i], 0) + 1
+        pos[i] = seen[doc[i]]
+    return pos + pos_shift
+
+
 def mask_rows(rows, doc: np.ndarray, mask_mode: int) -> np.ndarray:
     """Boolean "may attend" matrix for the given query rows against all keys.
 
@@ -191,7 +212,7 @@ class Problem:
 
     def __init__(self, cu_doclens, T, num_q_heads, num_kv_heads, head_dim,
                  rope_base=1e4, mask_mode=MASK_ANCHOR, pos_mode=POS_RESET,
-                 rope_layout=ROPE_ADJACENT, softmax_scale=None, pos_shift=0, theta=None):
+                 rope_layout=ROPE_ADJACENT, softmax_scale=None, pos_shift=0, theta=None, doc_of_token=None):
         if num_q_heads % num_kv_heads:
             raise ValueError("query heads must be a multiple of kv heads")
         self.T, self.Hq, self.Hkv, self.d = T, num_q_heads, num_kv_heads, head_dim
@@ -199,9 +220,19 @@ class Problem:
         self.layout = rope_layout
         self.scale = (1.0 / np.sqrt(head_dim)) if not softmax_scale or softmax_scale <= 0 \
             else float(softmax_scale)
-        self.cu = None if mask_mode == MASK_CAUSAL else _check_cu(cu_doclens, T)
-        self.doc = document_ids(cu_doclens, T, mask_mode)
-        self.pos = position_ids(cu_doclens, T, mask_mode, pos_mode, pos_shift)
+        if doc_of_token is not None:
+            # documents given per token: token 0 is the anchor (0), the rest name
+            # their document (>= 1); the mask compares these ids directly
+            doc = np.asarray(doc_of_token, dtype=np.int64)
+            if doc.shape != (T,) or doc[0] != 0 or np.any(doc[1:] < 1) or mask_mode == MASK_CAUSAL:
+                raise ValueError("doc_of_token: [T] ids, 0 for the anchor only, ANCHOR or INTRA_DOC mode")
+            self.cu = None
+            self.doc = doc
+            self.pos = segment_position_ids(doc, pos_mode, pos_shift)
+        else:
+            self.cu = None if mask_mode == MASK_CAUSAL else _check_cu(cu_doclens, T)
+            self.doc = document_ids(cu_doclens, T, mask_mode)
+            self.pos = position_ids(cu_doclens, T, mask_mode, pos_mode, pos_shift)
         self.theta = None if theta is None else np.asarray(theta, dtype=np.float64)
 
     def kv_head(self, h):

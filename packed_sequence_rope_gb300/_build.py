@@ -12,7 +12,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libanchorattn.so")
-SOURCES = ["plan.cpp", "rope.cu", "fwd.cu", "bwd.cu", "bwd_static.cu", "shift_diag.cu"]
+SOURCES = ["plan.cpp", "rope.cu", "fwd.cu", "bwd.cu", "bwd_static.cu", "shift_diag.cu", "segments.cu"]
 ARCH = "-gencode=arch=compute_103a,code=sm_103a"
 
 

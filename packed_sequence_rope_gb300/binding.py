@@ -21,7 +21,7 @@ STATUS = {0: "AA_OK", 1: "AA_ERR_INVALID_ARG", 2: "AA_ERR_UNSUPPORTED", 3: "AA_E
           4: "AA_ERR_NO_MEMORY", 5: "AA_ERR_TIMEOUT"}
 
 # every symbol include/anchorattn.h declares
-EXPORTS = ["aa_plan", "aa_plan_with_theta", "aa_plan_destroy", "aa_plan_metadata", "aa_plan_stats", "aa_plan_work",
+EXPORTS = ["aa_plan", "aa_plan_with_theta", "aa_plan_segments", "aa_plan_destroy", "aa_plan_metadata", "aa_plan_stats", "aa_plan_work",
            "aa_rope_apply", "aa_fwd", "aa_fwd_workspace_bytes", "aa_bwd_workspace_bytes", "aa_bwd", "aa_bwd_static_workspace", "aa_check_device_error",
            "aa_set_wait_limit", "aa_set_bwd_timing_events", "aa_selftest_bounded_wait", "aa_status_string",
            "aa_last_error", "aa_shift_diag_workspace_bytes", "aa_shift_diag"]
@@ -58,6 +58,7 @@ def lib():
             "aa_plan": ([ctypes.POINTER(AAConfig), i32p, i32, vp, ctypes.POINTER(vp)], ctypes.c_int),
             "aa_plan_with_theta": ([ctypes.POINTER(AAConfig), i32p, i32, ctypes.POINTER(ctypes.c_double), vp,
                                     ctypes.POINTER(vp)], ctypes.c_int),
+            "aa_plan_segments": ([ctypes.POINTER(AAConfig), i32p, vp, ctypes.POINTER(vp)], ctypes.c_int),
             "aa_plan_destroy": ([vp], ctypes.c_int),
             "aa_plan_metadata": ([vp, i32p, i32p], ctypes.c_int),
             "aa_plan_stats": ([vp, i64p, i64p, i64p], ctypes.c_int),
@@ -106,9 +107,11 @@ class Plan:
     def __init__(self, cu_doclens, total_tokens, num_q_heads, num_kv_heads, head_dim,
                  rope_base=1e4, mask_mode=MASK_ANCHOR, pos_mode=POS_RESET,
                  rope_layout=ROPE_ADJACENT, softmax_scale=0.0, pos_shift=0,
-                 host_only=False, stream=None, theta=None):
+                 host_only=False, stream=None, theta=None, doc_of_token=None):
         """theta: optional [head_dim / 2] rotation frequencies (aa_plan_with_theta)
-        replacing rope_base^(-2p/D), e.g. an NTK- or YaRN-scaled table."""
+        replacing rope_base^(-2p/D), e.g. an NTK- or YaRN-scaled table.
+        doc_of_token: optional int32 [T] document id per token (aa_plan_segments;
+        token 0 = 0, the anchor); cu_doclens is then ignored."""
         self.cfg = AAConfig(int(total_tokens), int(num_q_heads), int(num_kv_heads), int(head_dim),
                             float(rope_base), float(softmax_scale or 0.0), int(pos_shift),
                             int(mask_mode), int(pos_mode), int(rope_layout), int(bool(host_only)))
@@ -122,7 +125,16 @@ class Plan:
             n = int(self._cu.size) - 1
         h = ctypes.c_void_p()
         st = ctypes.c_void_p(0) if host_only else _stream(stream)
-        if theta is None:
+        if doc_of_token is not None:
+            if theta is not None:
+                raise ValueError("doc_of_token and theta cannot be combined")
+            self._doc = np.ascontiguousarray(np.asarray(doc_of_token, dtype=np.int32))
+            if self._doc.shape != (self.T,):
+                raise ValueError("doc_of_token must have total_tokens entries")
+            _check(lib().aa_plan_segments(ctypes.byref(self.cfg),
+                                          self._doc.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)), st,
+                                          ctypes.byref(h)))
+        elif theta is None:
             _check(lib().aa_plan(ctypes.byref(self.cfg), cu, n, st, ctypes.byref(h)))
         else:
             self._theta = np.ascontiguousarray(np.asarray(theta, dtype=np.float64))

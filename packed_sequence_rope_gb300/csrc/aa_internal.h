@@ -33,6 +33,8 @@ struct DevicePlan {
   float2* rope_lo = nullptr;   // [D/2][32]    cos/sin(l * theta_p), p-major
   float2* rope_step = nullptr; // [D/2]        cos/sin(theta_p)
   int32_t* err = nullptr;      // device error word (0 = ok)
+  int32_t* perm = nullptr;     // segment plans: [T] caller token of each grouped position
+  int32_t* pos_orig = nullptr; // segment plans: [T] rotation index in the caller's token order
 };
 
 }  // namespace aa
@@ -44,7 +46,12 @@ struct aa_plan_s {
   bool anchor = false;          // anchor column handled outside the tile path
   bool host_only = false;
   std::vector<int32_t> cu;      // document boundaries (empty in CAUSAL mode)
-  std::vector<int32_t> doc_id, pos_id, row_lo, key_hi;
+  std::vector<int32_t> doc_id, pos_id, row_lo, key_hi;  // in the kernels' (grouped) token order
+  // Segment plans (aa_plan_segments): documents given per token, possibly in
+  // interleaved chunks. The kernels run on the stable grouping of the tokens
+  // by document; perm[t] is the caller's token at grouped position t.
+  bool segmented = false;
+  std::vector<int32_t> perm, seg_doc, seg_pos;  // seg_*: the caller's order
   std::vector<aa::WorkItem> fwd_items, bwd_items;  // fwd: one item per (query-tile pair, head)
   std::vector<int32_t> qtile_klo;
   std::vector<double> theta;    // [D/2] rotation frequency of each pair (Eq. 6's theta_p)
@@ -64,8 +71,23 @@ aa_status fail(aa_status s, const std::string& msg);
 aa_status cuda_fail(cudaError_t e, const char* what);
 bool aligned16(const void* p);
 aa_status check_compute_plan(const aa_plan_s* p);
-// Rotate x [T, H, D] into y with the canonical tile rotation (no checks).
-aa_status launch_rope(const aa_plan_s* p, const void* x, void* y, int H, int inverse, cudaStream_t s);
+// Rotate x [T, H, D] into y with the canonical tile rotation (no checks);
+// positions from `pos` (default: the plan's kernel-order pos_id).
+aa_status launch_rope(const aa_plan_s* p, const void* x, void* y, int H, int inverse, cudaStream_t s,
+                      const int32_t* pos = nullptr);
+// Forward kernels with an already-validated workspace (no segment handling).
+aa_status launch_fwd_with_workspace(aa_plan_s* p, const void* q, const void* k, const void* v, void* o, float* lse,
+                                    void* workspace, cudaStream_t s);
+size_t fwd_base_workspace_bytes(const aa_plan_s* p);
+size_t bwd_base_workspace_bytes(const aa_plan_s* p);
+// Segment plans: extra workspace behind the base one, and the gather / run /
+// scatter wrappers (segments.cu).
+size_t seg_fwd_extra_bytes(const aa_plan_s* p);
+size_t seg_bwd_extra_bytes(const aa_plan_s* p);
+aa_status seg_fwd(aa_plan_s* p, const void* q, const void* k, const void* v, void* o, float* lse, void* workspace,
+                  cudaStream_t s);
+aa_status seg_bwd(aa_plan_s* p, const void* q, const void* k, const void* v, const void* o, const float* lse,
+                  const void* dout, void* dq, void* dk, void* dv, void* workspace, cudaStream_t s);
 // Launch the backward kernels with an already-validated workspace pointer.
 aa_status launch_bwd_with_workspace(aa_plan_s* p, const void* q, const void* k, const void* v, const void* o,
                                     const float* lse, const void* dout, void* dq, void* dk, void* dv,

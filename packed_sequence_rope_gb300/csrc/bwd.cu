@@ -850,15 +850,20 @@ aa_status launch_bwd_with_workspace(aa_plan_s* p, const void* q, const void* k, 
                      : launch_bwd<64>(p, q, k, v, o, lse, dout, dq, dk, dv, workspace, s);
 }
 
+size_t bwd_base_workspace_bytes(const aa_plan_s* p) {
+  if (!p) return 0;
+  size_t total = 0;
+  carve(nullptr, p, &total);
+  return total;
+}
+
 }  // namespace aa
 
 using namespace aa;
 
 extern "C" size_t aa_bwd_workspace_bytes(aa_plan_t p) {
   if (!p) return 0;
-  size_t total = 0;
-  carve(nullptr, p, &total);
-  return total;
+  return bwd_base_workspace_bytes(p) + (p->segmented ? seg_bwd_extra_bytes(p) : 0);
 }
 
 extern "C" aa_status aa_bwd(aa_plan_t p, const void* q, const void* k, const void* v, const void* o,
@@ -876,6 +881,6 @@ extern "C" aa_status aa_bwd(aa_plan_t p, const void* q, const void* k, const voi
   if (workspace_bytes < aa_bwd_workspace_bytes(p))
     return fail(AA_ERR_INVALID_ARG, "workspace is smaller than aa_bwd_workspace_bytes()");
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  return p->D == 128 ? launch_bwd<128>(p, q, k, v, o, lse, dout, dq, dk, dv, workspace, s)
-                     : launch_bwd<64>(p, q, k, v, o, lse, dout, dq, dk, dv, workspace, s);
+  if (p->segmented) return seg_bwd(p, q, k, v, o, lse, dout, dq, dk, dv, workspace, s);
+  return launch_bwd_with_workspace(p, q, k, v, o, lse, dout, dq, dk, dv, workspace, s);
 }

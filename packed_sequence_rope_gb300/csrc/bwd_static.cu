@@ -65,5 +65,7 @@ extern "C" aa_status aa_bwd_static_workspace(aa_plan_t p, const void* q, const v
   if (current != p->device) return fail(AA_ERR_INVALID_ARG, "the plan's device must be the current device");
   void* ws = nullptr;
   if ((st = static_workspace_address(current, &ws)) != AA_OK) return st;
-  return launch_bwd_with_workspace(p, q, k, v, o, lse, dout, dq, dk, dv, ws, reinterpret_cast<cudaStream_t>(stream));
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (p->segmented) return seg_bwd(p, q, k, v, o, lse, dout, dq, dk, dv, ws, s);
+  return launch_bwd_with_workspace(p, q, k, v, o, lse, dout, dq, dk, dv, ws, s);
 }

@@ -434,13 +434,25 @@ aa_status launch_fwd(aa_plan_s* p, const void* q, const void* k, const void* v, 
 }
 
 }  // namespace
+
+size_t fwd_base_workspace_bytes(const aa_plan_s* p) {
+  if (!p || p->cfg.rope_layout == AA_ROPE_NONE) return 0;
+  return ((size_t)p->T * p->Hkv * p->D * 2 + 255) & ~size_t(255);
+}
+
+aa_status launch_fwd_with_workspace(aa_plan_s* p, const void* q, const void* k, const void* v, void* o, float* lse,
+                                    void* workspace, cudaStream_t s) {
+  return p->D == 128 ? launch_fwd<128>(p, q, k, v, o, lse, workspace, s)
+                     : launch_fwd<64>(p, q, k, v, o, lse, workspace, s);
+}
+
 }  // namespace aa
 
 using namespace aa;
 
 extern "C" size_t aa_fwd_workspace_bytes(aa_plan_t p) {
-  if (!p || p->cfg.rope_layout == AA_ROPE_NONE) return 0;
-  return ((size_t)p->T * p->Hkv * p->D * 2 + 255) & ~size_t(255);
+  if (!p) return 0;
+  return fwd_base_workspace_bytes(p) + (p->segmented ? seg_fwd_extra_bytes(p) : 0);
 }
 
 extern "C" aa_status aa_fwd(aa_plan_t p, const void* q, const void* k, const void* v, void* o, float* lse,
@@ -457,6 +469,6 @@ extern "C" aa_status aa_fwd(aa_plan_t p, const void* q, const void* k, const voi
     if (workspace_bytes < need) return fail(AA_ERR_INVALID_ARG, "workspace is smaller than aa_fwd_workspace_bytes()");
   }
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  return p->D == 128 ? launch_fwd<128>(p, q, k, v, o, lse, workspace, s)
-                     : launch_fwd<64>(p, q, k, v, o, lse, workspace, s);
+  if (p->segmented) return seg_fwd(p, q, k, v, o, lse, workspace, s);
+  return launch_fwd_with_workspace(p, q, k, v, o, lse, workspace, s);
 }

@@ -217,7 +217,7 @@ static aa_status upload(T** dst, const std::vector<T>& src, cudaStream_t s, cons
 static void free_device(aa_plan_s* p) {
   DevicePlan& d = p->dev;
   void* ptrs[] = {d.pos_id, d.row_lo, d.key_hi, d.fwd_items, d.bwd_items, d.qtile_klo,
-                  d.rope_hi, d.rope_lo, d.rope_step, d.err};
+                  d.rope_hi, d.rope_lo, d.rope_step, d.err, d.perm, d.pos_orig};
   for (void* q : ptrs)
     if (q) cudaFree(q);
   d = DevicePlan{};
@@ -263,10 +263,54 @@ static aa_status validate(const aa_config* c, const int32_t* cu, int32_t num_doc
 
 using namespace aa;
 
+// Segment plans: group the tokens by document (documents in order of first
+// appearance, tokens in their order inside a document; the anchor stays
+// first). The grouped layout is an ordinary contiguous packing with the same
+// visible pairs (same document and j <= i keep their meaning because the order
+// inside a document is kept) and the same positions (RESET: rank inside the
+// document; CONTINUOUS: the caller's token index, set explicitly below).
+static aa_status group_segments(const aa_config* cfg, const int32_t* doc_of_token, std::vector<int32_t>* perm,
+                                std::vector<int32_t>* cu) {
+  const int T = cfg->total_tokens;
+  if (!doc_of_token) return fail(AA_ERR_INVALID_ARG, "doc_of_token is NULL");
+  if (cfg->mask_mode == AA_MASK_CAUSAL)
+    return fail(AA_ERR_INVALID_ARG, "segment plans need mask_mode ANCHOR or INTRA_DOC");
+  if (doc_of_token[0] != 0) return fail(AA_ERR_INVALID_ARG, "doc_of_token[0] must be 0 (token 0 is the anchor)");
+  std::map<int32_t, int> group_of;  // document id -> group index (first appearance)
+  std::vector<std::vector<int32_t>> groups;
+  for (int i = 1; i < T; ++i) {
+    const int32_t d = doc_of_token[i];
+    if (d < 1) return fail(AA_ERR_INVALID_ARG, "doc_of_token[" + std::to_string(i) + "] must be >= 1");
+    auto it = group_of.find(d);
+    if (it == group_of.end()) {
+      it = group_of.emplace(d, (int)groups.size()).first;
+      groups.emplace_back();
+    }
+    groups[it->second].push_back(i);
+  }
+  perm->assign(1, 0);
+  cu->assign(1, 1);
+  for (auto& g : groups) {
+    perm->insert(perm->end(), g.begin(), g.end());
+    cu->push_back(cu->back() + (int32_t)g.size());
+  }
+  return AA_OK;
+}
+
 static aa_status make_plan(const aa_config* cfg, const int32_t* cu_doclens_host, int32_t num_docs,
-                           const double* theta, aa_stream_t stream, aa_plan_t* out) {
+                           const double* theta, const int32_t* doc_of_token, aa_stream_t stream, aa_plan_t* out) {
   if (!out) return fail(AA_ERR_INVALID_ARG, "out is NULL");
   *out = nullptr;
+  std::vector<int32_t> perm, seg_cu;
+  if (doc_of_token) {
+    if (!cfg) return fail(AA_ERR_INVALID_ARG, "config is NULL");
+    if (cfg->total_tokens < 2 || cfg->total_tokens >= (1 << 30))
+      return fail(AA_ERR_INVALID_ARG, "total_tokens must be in [2, 2^30)");
+    aa_status gs = group_segments(cfg, doc_of_token, &perm, &seg_cu);
+    if (gs != AA_OK) return gs;
+    cu_doclens_host = seg_cu.data();
+    num_docs = (int32_t)seg_cu.size() - 1;
+  }
   aa_status st = validate(cfg, cu_doclens_host, num_docs, theta);
   if (st != AA_OK) return st;
   aa_plan_s* p = new (std::nothrow) aa_plan_s();
@@ -286,6 +330,15 @@ static aa_status make_plan(const aa_config* cfg, const int32_t* cu_doclens_host,
   for (int i = 0; i < p->D / 2; ++i)  // Eq. 6: theta_p = base^(-2p/D), unless the caller supplies them
     p->theta[i] = theta ? theta[i] : std::pow(cfg->rope_base, -2.0 * (double)i / (double)p->D);
   build_token_metadata(p);
+  if (doc_of_token) {
+    p->segmented = true;
+    p->perm = perm;
+    p->seg_doc.assign(doc_of_token, doc_of_token + p->T);
+    if (cfg->pos_mode == AA_POS_CONTINUOUS)  // the caller's token index, not the grouped one
+      for (int t = 0; t < p->T; ++t) p->pos_id[t] = perm[t] + cfg->pos_shift;
+    p->seg_pos.assign(p->T, 0);
+    for (int t = 0; t < p->T; ++t) p->seg_pos[perm[t]] = p->pos_id[t];
+  }
   build_stats_and_work(p);
   build_rope_tables(p);
   if (p->host_only) {
@@ -310,7 +363,9 @@ static aa_status make_plan(const aa_config* cfg, const int32_t* cu_doclens_host,
       (st = upload(&d.rope_hi, p->rope_hi, s, "rope table (hi)")) != AA_OK ||
       (st = upload(&d.rope_lo, p->rope_lo, s, "rope table (lo)")) != AA_OK ||
       (st = upload(&d.rope_step, p->rope_step, s, "rope step table")) != AA_OK ||
-      (st = upload(&d.err, zero, s, "error word")) != AA_OK) {
+      (st = upload(&d.err, zero, s, "error word")) != AA_OK ||
+      (p->segmented && ((st = upload(&d.perm, p->perm, s, "segment permutation")) != AA_OK ||
+                        (st = upload(&d.pos_orig, p->seg_pos, s, "segment positions")) != AA_OK))) {
     cudaStreamSynchronize(s);
     free_device(p);
     delete p;
@@ -329,13 +384,19 @@ static aa_status make_plan(const aa_config* cfg, const int32_t* cu_doclens_host,
 
 extern "C" aa_status aa_plan(const aa_config* cfg, const int32_t* cu_doclens_host, int32_t num_docs,
                              aa_stream_t stream, aa_plan_t* out) {
-  return make_plan(cfg, cu_doclens_host, num_docs, nullptr, stream, out);
+  return make_plan(cfg, cu_doclens_host, num_docs, nullptr, nullptr, stream, out);
+}
+
+extern "C" aa_status aa_plan_segments(const aa_config* cfg, const int32_t* doc_of_token_host, aa_stream_t stream,
+                                      aa_plan_t* out) {
+  if (!doc_of_token_host) return fail(AA_ERR_INVALID_ARG, "doc_of_token is NULL");
+  return make_plan(cfg, nullptr, 0, nullptr, doc_of_token_host, stream, out);
 }
 
 extern "C" aa_status aa_plan_with_theta(const aa_config* cfg, const int32_t* cu_doclens_host, int32_t num_docs,
                                         const double* theta, aa_stream_t stream, aa_plan_t* out) {
   if (!theta) return fail(AA_ERR_INVALID_ARG, "theta is NULL (use aa_plan for base^(-2p/D))");
-  return make_plan(cfg, cu_doclens_host, num_docs, theta, stream, out);
+  return make_plan(cfg, cu_doclens_host, num_docs, theta, nullptr, stream, out);
 }
 
 extern "C" aa_status aa_plan_destroy(aa_plan_t p) {
@@ -350,8 +411,11 @@ extern "C" aa_status aa_plan_destroy(aa_plan_t p) {
 
 extern "C" aa_status aa_plan_metadata(aa_plan_t p, int32_t* doc_id_host, int32_t* pos_id_host) {
   if (!p) return fail(AA_ERR_INVALID_ARG, "plan is NULL");
-  if (doc_id_host) std::memcpy(doc_id_host, p->doc_id.data(), sizeof(int32_t) * p->T);
-  if (pos_id_host) std::memcpy(pos_id_host, p->pos_id.data(), sizeof(int32_t) * p->T);
+  // segment plans report the caller's document ids and token order
+  const std::vector<int32_t>& doc = p->segmented ? p->seg_doc : p->doc_id;
+  const std::vector<int32_t>& pos = p->segmented ? p->seg_pos : p->pos_id;
+  if (doc_id_host) std::memcpy(doc_id_host, doc.data(), sizeof(int32_t) * p->T);
+  if (pos_id_host) std::memcpy(pos_id_host, pos.data(), sizeof(int32_t) * p->T);
   return AA_OK;
 }
 

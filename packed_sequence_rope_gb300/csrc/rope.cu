@@ -62,16 +62,17 @@ __global__ void __launch_bounds__(128) rope_apply_kernel(const __nv_bfloat16* __
 }
 
 template <int HD>
-void launch_rope_apply(const aa_plan_s* p, const void* x, void* y, int H, int inverse, cudaStream_t s) {
+void launch_rope_apply(const aa_plan_s* p, const void* x, void* y, int H, int inverse, cudaStream_t s,
+                       const int32_t* pos) {
   const dim3 grid((unsigned)p->n_tiles, (unsigned)H);
   const auto* xi = static_cast<const __nv_bfloat16*>(x);
   auto* yo = static_cast<__nv_bfloat16*>(y);
   if (p->cfg.rope_layout == AA_ROPE_ADJACENT)
-    rope_apply_kernel<HD, 0><<<grid, 128, 0, s>>>(xi, yo, p->dev.pos_id, p->dev.rope_hi, p->dev.rope_lo,
-                                                  p->dev.rope_step, p->T, H, inverse);
+    rope_apply_kernel<HD, 0><<<grid, 128, 0, s>>>(xi, yo, pos, p->dev.rope_hi, p->dev.rope_lo, p->dev.rope_step,
+                                                  p->T, H, inverse);
   else
-    rope_apply_kernel<HD, 1><<<grid, 128, 0, s>>>(xi, yo, p->dev.pos_id, p->dev.rope_hi, p->dev.rope_lo,
-                                                  p->dev.rope_step, p->T, H, inverse);
+    rope_apply_kernel<HD, 1><<<grid, 128, 0, s>>>(xi, yo, pos, p->dev.rope_hi, p->dev.rope_lo, p->dev.rope_step,
+                                                  p->T, H, inverse);
 }
 
 static PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {
@@ -102,11 +103,13 @@ aa_status make_tile_map(CUtensorMap* m, const void* base, int T, int H, int D) {
   return AA_OK;
 }
 
-aa_status launch_rope(const aa_plan_s* p, const void* x, void* y, int H, int inverse, cudaStream_t s) {
+aa_status launch_rope(const aa_plan_s* p, const void* x, void* y, int H, int inverse, cudaStream_t s,
+                      const int32_t* pos) {
+  if (!pos) pos = p->dev.pos_id;
   if (p->D == 128)
-    launch_rope_apply<128>(p, x, y, H, inverse, s);
+    launch_rope_apply<128>(p, x, y, H, inverse, s, pos);
   else
-    launch_rope_apply<64>(p, x, y, H, inverse, s);
+    launch_rope_apply<64>(p, x, y, H, inverse, s, pos);
   cudaError_t e = cudaGetLastError();
   return e == cudaSuccess ? AA_OK : cuda_fail(e, "rope_apply_kernel launch");
 }
@@ -163,5 +166,6 @@ extern "C" aa_status aa_rope_apply(aa_plan_t p, const void* x, void* y, int32_t 
     cudaError_t e = cudaMemcpyAsync(y, x, (size_t)T * num_heads * D * 2, cudaMemcpyDeviceToDevice, s);
     return e == cudaSuccess ? AA_OK : cuda_fail(e, "aa_rope_apply copy");
   }
-  return launch_rope(p, x, y, num_heads, inverse ? 1 : 0, s);
+  // a segment plan's tensors arrive in the caller's token order
+  return launch_rope(p, x, y, num_heads, inverse ? 1 : 0, s, p->segmented ? p->dev.pos_orig : p->dev.pos_id);
 }

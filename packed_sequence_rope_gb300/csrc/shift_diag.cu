@@ -222,6 +222,8 @@ extern "C" aa_status aa_shift_diag(aa_plan_t p1, aa_plan_t p2, const void* q, co
   aa_status st = check_compute_plan(p1);
   if (st != AA_OK) return st;
   if ((st = check_compute_plan(p2)) != AA_OK) return st;
+  if (p1->segmented || p2->segmented)
+    return fail(AA_ERR_UNSUPPORTED, "aa_shift_diag: segment plans are not supported");
   if (!same_problem(p1, p2))
     return fail(AA_ERR_INVALID_ARG, "aa_shift_diag: the two plans must differ only in pos_shift");
   if (!q || !k || !col_absdiff || !first_logit_absdiff || !result)

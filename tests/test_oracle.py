@@ -344,3 +344,57 @@ def test_custom_theta_keeps_shift_invariance():
     O0, L0 = orc.forward(mk(0), q, k, v)
     O1, L1 = orc.forward(mk(777), q, k, v)
     assert np.allclose(O0, O1, atol=1e-10) and np.allclose(L0, L1, atol=1e-10)
+
+
+# --------------------------------------------------------------------------- documents given per token
+def test_interleaved_mask_and_positions_by_hand():
+    # tokens: anchor, d1, d2, d1, d2, d2, d1 (chunks of two documents interleaved)
+    doc = [0, 1, 2, 1, 2, 2, 1]
+    p = orc.Problem(None, 7, 1, 1, 4, 1e4, orc.MASK_ANCHOR, orc.POS_RESET, doc_of_token=doc)
+    m = orc.mask_rows(np.arange(7), p.doc, orc.MASK_ANCHOR)
+    want = [[0], [0, 1], [0, 2], [0, 1, 3], [0, 2, 4], [0, 2, 4, 5], [0, 1, 3, 6]]
+    for i, js in enumerate(want):
+        assert sorted(np.nonzero(m[i])[0].tolist()) == js, i
+    assert p.pos.tolist() == [0, 1, 1, 2, 2, 3, 3]
+    pc = orc.Problem(None, 7, 1, 1, 4, 1e4, orc.MASK_ANCHOR, orc.POS_CONTINUOUS, doc_of_token=doc, pos_shift=5)
+    assert pc.pos.tolist() == [5, 6, 7, 8, 9, 10, 11]
+    pi = orc.Problem(None, 7, 1, 1, 4, 1e4, orc.MASK_INTRA_DOC, orc.POS_RESET, doc_of_token=doc)
+    mi = orc.mask_rows(np.arange(7), pi.doc, orc.MASK_INTRA_DOC)
+    assert sorted(np.nonzero(mi[6])[0].tolist()) == [1, 3, 6] and np.nonzero(mi[0])[0].tolist() == [0]
+
+
+def test_contiguous_doc_map_equals_cu_path():
+    cu, T = [1, 30, 31, 90, 128], 128
+    doc = np.zeros(T, int)
+    for k in range(1, len(cu)):
+        doc[cu[k - 1]:cu[k]] = k
+    rng = np.random.default_rng(25)
+    q, k, v = (rng.standard_normal((T, 2, 16)) for _ in range(3))
+    for pos in (orc.POS_RESET, orc.POS_CONTINUOUS):
+        a = orc.Problem(cu, T, 2, 2, 16, 1e4, orc.MASK_ANCHOR, pos)
+        b = orc.Problem(None, T, 2, 2, 16, 1e4, orc.MASK_ANCHOR, pos, doc_of_token=doc)
+        assert np.array_equal(a.doc, b.doc) and np.array_equal(a.pos, b.pos)
+        Oa, La = orc.forward(a, q, k, v)
+        Ob, Lb = orc.forward(b, q, k, v)
+        assert np.array_equal(Oa, Ob) and np.array_equal(La, Lb)
+
+
+def test_interleaved_equals_grouped_layout():
+    # grouping a document's tokens (order kept) changes neither what a token
+    # sees nor its RESET position: outputs move with the tokens
+    from aa_synth import interleaved_chunks
+    rng = np.random.default_rng(26)
+    doc = interleaved_chunks([40, 25, 60], 4, rng)
+    T = doc.size
+    perm = np.concatenate([[0]] + [np.nonzero(doc == d)[0] for d in (1, 2, 3)])
+    cu = np.concatenate([[1], 1 + np.cumsum([40, 25, 60])])
+    q, k, v, do = (rng.standard_normal((T, 2, 16)) for _ in range(4))
+    a = orc.Problem(None, T, 2, 1, 16, 1e4, orc.MASK_ANCHOR, orc.POS_RESET, doc_of_token=doc)
+    b = orc.Problem(cu, T, 2, 1, 16, 1e4, orc.MASK_ANCHOR, orc.POS_RESET)
+    Oa, La = orc.forward(a, q, k[:, :1], v[:, :1])
+    Ob, Lb = orc.forward(b, q[perm], k[perm, :1], v[perm, :1])
+    assert np.allclose(Oa[perm], Ob, atol=1e-12) and np.allclose(La[:, perm], Lb, atol=1e-12)
+    ga = orc.backward(a, q, k[:, :1], v[:, :1], do)
+    gb = orc.backward(b, q[perm], k[perm, :1], v[perm, :1], do[perm])
+    for x, y in zip(ga, gb):
+        assert np.allclose(x[perm], y, atol=1e-10)

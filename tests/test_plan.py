@@ -148,3 +148,26 @@ def test_plan_with_theta_validation_and_metadata(aa):
     h = ctypes.c_void_p()
     cfg = aa.binding.AAConfig(100, 2, 1, 64, 1e4, 0.0, 0, orc.MASK_CAUSAL, 0, 0, 1)
     assert L.aa_plan_with_theta(ctypes.byref(cfg), None, 0, None, None, ctypes.byref(h)) == 1
+
+
+@pytest.mark.parametrize("pos", [orc.POS_RESET, orc.POS_CONTINUOUS])
+def test_segment_plan_metadata_vs_oracle(aa, pos):
+    from aa_synth import interleaved_chunks
+    doc = interleaved_chunks([300, 5, 170, 1, 90], 3, np.random.default_rng(7))
+    T = doc.size
+    with aa.Plan(None, T, 2, 1, 64, 1e4, orc.MASK_ANCHOR, pos, pos_shift=11, host_only=True,
+                 doc_of_token=doc) as p:
+        d, ps = p.metadata()
+        prob = orc.Problem(None, T, 2, 1, 64, 1e4, orc.MASK_ANCHOR, pos, pos_shift=11, doc_of_token=doc)
+        assert np.array_equal(d, doc) and np.array_equal(ps, prob.pos)
+        assert p.stats()["unmasked_pairs"] == int(orc.mask_rows(np.arange(T), prob.doc, orc.MASK_ANCHOR).sum())
+
+
+def test_segment_plan_rejects_bad_maps(aa):
+    doc = np.array([0, 1, 2, 1, 2], np.int32)
+    with pytest.raises(aa.AAError, match="ANCHOR or INTRA_DOC"):
+        aa.Plan(None, 5, 1, 1, 64, 1e4, orc.MASK_CAUSAL, host_only=True, doc_of_token=doc)
+    with pytest.raises(aa.AAError, match="doc_of_token\\[0\\]"):
+        aa.Plan(None, 5, 1, 1, 64, 1e4, host_only=True, doc_of_token=np.array([1, 1, 2, 1, 2]))
+    with pytest.raises(aa.AAError, match="doc_of_token\\[3\\]"):
+        aa.Plan(None, 5, 1, 1, 64, 1e4, host_only=True, doc_of_token=np.array([0, 1, 2, 0, 2]))
