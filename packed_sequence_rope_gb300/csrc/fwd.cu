@@ -279,22 +279,22 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int j0 = kt * kTile;
       // tiles every row of the warp sees entirely skip the per-element mask
       const bool full = __all_sync(0xffffffffu, lo <= j0 && j0 + kTile - 1 <= hi);
+      // the row's logits, read from TMEM once (one wait) and kept in registers
+      // for both passes
+      float sv[128];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) ptx::tmem_ld32(t_s + c * 32, sv + c * 32);
+      ptx::tmem_wait_ld();
       // pass 1: row max of the visible logits (scaled once at the end)
       float mt = -INFINITY;
+      if (full) {
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        float sv[32];
-        ptx::tmem_ld32(t_s + c * 32, sv);
-        ptx::tmem_wait_ld();
-        if (full) {
+        for (int e = 0; e < 128; e += 2) mt = fmaxf(mt, fmaxf(sv[e], sv[e + 1]));
+      } else {
 #pragma unroll
-          for (int e = 0; e < 32; e += 2) mt = fmaxf(mt, fmaxf(sv[e], sv[e + 1]));
-        } else {
-#pragma unroll
-          for (int e = 0; e < 32; ++e) {
-            const int j = j0 + c * 32 + e;
-            if (j >= lo && j <= hi) mt = fmaxf(mt, sv[e]);
-          }
+        for (int e = 0; e < 128; ++e) {
+          const int j = j0 + e;
+          if (j >= lo && j <= hi) mt = fmaxf(mt, sv[e]);
         }
       }
       mt *= sl2;
@@ -306,13 +306,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         l *= f;
         if (kt > lo_t) {  // O holds earlier tiles: S(kt) done implies their PV is done
 #pragma unroll 1
-          for (int c = 0; c < HD / 32; ++c) {
-            float ov[32];
-            ptx::tmem_ld32(t_o + c * 32, ov);
+          for (int c = 0; c < HD / 16; ++c) {
+            float ov[16];
+            ptx::tmem_ld16(t_o + c * 16, ov);
             ptx::tmem_wait_ld();
 #pragma unroll
-            for (int e = 0; e < 32; ++e) ov[e] *= f;
-            ptx::tmem_st32(t_o + c * 32, ov);
+            for (int e = 0; e < 16; ++e) ov[e] *= f;
+            ptx::tmem_st16f(t_o + c * 16, ov);
           }
         }
         m = mn;
@@ -322,16 +322,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float mm = (m == -INFINITY) ? 0.f : m;
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
-        float sv[32];
-        ptx::tmem_ld32(t_s + c * 32, sv);
-        ptx::tmem_wait_ld();
+        const float* sc = sv + c * 32;
         uint32_t w[16];
         if (full) {
           const float2 sl22 = make_float2(sl2, sl2), nm2 = make_float2(-mm, -mm);
           float2 rs2 = make_float2(0.f, 0.f);
 #pragma unroll
           for (int e = 0; e < 16; ++e) {
-            const float2 a = __ffma2_rn(make_float2(sv[2 * e], sv[2 * e + 1]), sl22, nm2);
+            const float2 a = __ffma2_rn(make_float2(sc[2 * e], sc[2 * e + 1]), sl22, nm2);
             const float2 pp = make_float2(ptx::ex2(a.x), ptx::ex2(a.y));
             rs2 = __fadd2_rn(rs2, pp);
             w[e] = ptx::pack_bf16x2(pp.x, pp.y);
@@ -341,8 +339,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int e = 0; e < 16; ++e) {
             const int j = j0 + c * 32 + 2 * e;
-            const float p0 = (j >= lo && j <= hi) ? ptx::ex2(fmaf(sv[2 * e], sl2, -mm)) : 0.f;
-            const float p1 = (j + 1 >= lo && j + 1 <= hi) ? ptx::ex2(fmaf(sv[2 * e + 1], sl2, -mm)) : 0.f;
+            const float p0 = (j >= lo && j <= hi) ? ptx::ex2(fmaf(sc[2 * e], sl2, -mm)) : 0.f;
+            const float p1 = (j + 1 >= lo && j + 1 <= hi) ? ptx::ex2(fmaf(sc[2 * e + 1], sl2, -mm)) : 0.f;
             rs += p0 + p1;
             w[e] = ptx::pack_bf16x2(p0, p1);
           }
