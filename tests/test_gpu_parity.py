@@ -236,3 +236,37 @@ def test_default_theta_table_is_bit_identical_to_base(aa):
         o1, l1 = p1.fwd(q, k, v)
         torch.cuda.synchronize()
     assert torch.equal(o0, o1) and torch.equal(l0, l1)
+
+
+def test_batched_rows_as_one_packing(aa):
+    # two packed rows run separately, and concatenated after one shared anchor
+    rows = [[1, 300, 310, 700], [1, 128, 600]]
+    Hq, Hkv, D = 2, 2, 128
+    per = [inputs(cu[-1], Hq, Hkv, D, seed=51 + b) for b, cu in enumerate(rows)]
+    for i in range(3):                      # the rows share the anchor's q, k, v
+        per[1][i][0] = per[0][i][0]
+    outs = []
+    for cu, (q, k, v, do) in zip(rows, per):
+        with aa.Plan(cu, cu[-1], Hq, Hkv, D, 1e4) as p:
+            o, lse = p.fwd(q, k, v)
+            outs.append((o, lse) + p.bwd(q, k, v, o, lse, do))
+    cat = lambda i: torch.cat([per[0][i][:1]] + [p_[i][1:] for p_ in per]).contiguous()
+    q, k, v, do = (cat(i) for i in range(4))
+    do[0] = per[0][3][0] + per[1][3][0]
+    T = q.shape[0]
+    cu = [1] + rows[0][1:] + [c + rows[0][-1] - 1 for c in rows[1][1:]]
+    with aa.Plan(cu, T, Hq, Hkv, D, 1e4) as p:
+        o, lse = p.fwd(q, k, v)
+        dq, dk, dv = p.bwd(q, k, v, o, lse, do)
+        torch.cuda.synchronize()
+    off = 1
+    for (o_r, l_r, dq_r, dk_r, dv_r), cu_r in zip(outs, rows):
+        n = cu_r[-1] - 1
+        sl = slice(off, off + n)
+        assert (o[sl].float() - o_r[1:].float()).abs().max().item() <= 2e-2
+        assert (lse[:, sl] - l_r[:, 1:]).abs().max().item() <= 1e-3
+        for got, ref in ((dq[sl], dq_r[1:]), (dk[sl], dk_r[1:]), (dv[sl], dv_r[1:])):
+            assert rel_l2(got, f64(ref)) <= REL_L2
+        off += n
+    assert rel_l2(dk[0:1], f64(outs[0][3][0:1] + outs[1][3][0:1])) <= REL_L2
+    assert rel_l2(dv[0:1], f64(outs[0][4][0:1] + outs[1][4][0:1])) <= REL_L2

@@ -398,3 +398,42 @@ def test_interleaved_equals_grouped_layout():
     gb = orc.backward(b, q[perm], k[perm, :1], v[perm, :1], do[perm])
     for x, y in zip(ga, gb):
         assert np.allclose(x[perm], y, atol=1e-10)
+
+
+def test_batched_rows_equal_one_concatenated_packing():
+    # the anchor attends only to itself, so every row of a batch holds the same
+    # anchor state: B packed rows = their documents concatenated after one
+    # shared anchor (RESET positions), outputs per document unchanged and the
+    # anchor's dk / dv summed over the rows
+    rng = np.random.default_rng(27)
+    rows = [[1, 40, 90], [1, 25, 30, 70]]          # cu_doclens of two rows
+    Ts = [c[-1] for c in rows]
+    a_q, a_k, a_v = (rng.standard_normal((1, 2, 16)) for _ in range(3))
+    per = []
+    for cu, T in zip(rows, Ts):
+        q, k, v, do = (rng.standard_normal((T, 2, 16)) for _ in range(4))
+        q[0], k[0], v[0] = a_q[0], a_k[0], a_v[0]
+        per.append((cu, T, q, k, v, do))
+    # concatenation: anchor, row 1's documents, row 2's documents
+    cat = lambda i: np.concatenate([per[0][i][:1]] + [p[i][1:] for p in per])
+    q, k, v, do = (cat(i) for i in (2, 3, 4, 5))
+    do[0] = per[0][5][0] + per[1][5][0]            # the shared anchor row's upstream gradient
+    T = 1 + sum(t - 1 for t in Ts)
+    cu = np.concatenate([[1]] + [np.asarray(per[0][0][1:])] + [np.asarray(per[1][0][1:]) + Ts[0] - 1])
+    big = orc.Problem(cu, T, 2, 2, 16, 1e4, orc.MASK_ANCHOR, orc.POS_RESET)
+    O, L = orc.forward(big, q, k, v)
+    dq, dk, dv = orc.backward(big, q, k, v, do)
+    off = 1
+    dk0 = np.zeros_like(dk[0]); dv0 = np.zeros_like(dv[0])
+    for cu_r, T_r, qr, kr, vr, dor in per:
+        small = orc.Problem(cu_r, T_r, 2, 2, 16, 1e4, orc.MASK_ANCHOR, orc.POS_RESET)
+        Or, Lr = orc.forward(small, qr, kr, vr)
+        gq, gk, gv = orc.backward(small, qr, kr, vr, dor)
+        sl = slice(off, off + T_r - 1)
+        assert np.allclose(O[sl], Or[1:], atol=1e-12) and np.allclose(L[:, sl], Lr[:, 1:], atol=1e-12)
+        assert np.allclose(dq[sl], gq[1:], atol=1e-10) and np.allclose(dk[sl], gk[1:], atol=1e-10)
+        assert np.allclose(dv[sl], gv[1:], atol=1e-10)
+        assert np.allclose(O[0], Or[0], atol=1e-12)                 # every row's anchor output is v_0
+        dk0 += gk[0]; dv0 += gv[0]
+        off += T_r - 1
+    assert np.allclose(dk[0], dk0, atol=1e-10) and np.allclose(dv[0], dv0, atol=1e-10)
