@@ -76,7 +76,7 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, co
   const uint64_t t0 = ptx::global_timer_ns();
   while (true) {
     for (int i = 0; i < 64; ++i)
-      if (ptx::mbar_try_wait_sleep(bar, parity, ptx::kSuspendHintNs)) return true;
+      if (ptx::mbar_try_wait(bar, parity)) return true;
     if (*abort_flag) return false;
     if (ptx::global_timer_ns() - t0 >= P.wait_limit_ns) {
       atomicCAS(P.err, 0, site);

@@ -51,22 +51,6 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
-// try_wait that lets the hardware suspend the warp (up to `hint_ns`) until the
-// phase completes, so waiting warps do not take issue slots from working ones.
-__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t parity, uint32_t hint_ns) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
-      : "memory");
-  return ok != 0;
-}
-
-constexpr uint32_t kSuspendHintNs = 20000;
-
 // Bounded wait for the phase with the given parity to complete. Returns false
 // (and records `site` in the device error word) once `limit_ns` has passed.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint64_t limit_ns,
@@ -75,7 +59,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint64
   const uint64_t t0 = global_timer_ns();
   while (true) {
     for (int i = 0; i < 64; ++i)
-      if (mbar_try_wait_sleep(bar, parity, kSuspendHintNs)) return true;
+      if (mbar_try_wait(bar, parity)) return true;
     if (global_timer_ns() - t0 >= limit_ns) {
       atomicCAS(err, 0, site);
       return false;
