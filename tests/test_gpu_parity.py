@@ -148,7 +148,7 @@ def _sample_rows(cu, T, n, seed):
     return rows
 
 
-@pytest.mark.parametrize("name", ["llama7b_8k", "llama7b_64k"])
+@pytest.mark.parametrize("name", ["llama7b_8k", "llama7b_64k", "gqa_128k"])
 def test_full_size_forward_sampled(aa, name):
     w = WORKLOADS[name]
     cu = workload_cu_doclens(w)
@@ -270,3 +270,33 @@ def test_batched_rows_as_one_packing(aa):
         off += n
     assert rel_l2(dk[0:1], f64(outs[0][3][0:1] + outs[1][3][0:1])) <= REL_L2
     assert rel_l2(dv[0:1], f64(outs[0][4][0:1] + outs[1][4][0:1])) <= REL_L2
+
+
+@pytest.mark.parametrize("name", ["llama7b_64k", "gqa_128k"])
+def test_full_size_backward_documents_long(aa, name):
+    # documents are independent apart from the anchor (pinned in the oracle
+    # tests: a packing equals per-document runs), so the gradients of one
+    # document's tokens at full size equal the oracle's on [anchor + that
+    # document] alone, with the same reset positions
+    w = WORKLOADS[name]
+    cu = workload_cu_doclens(w)
+    T = w.total_tokens
+    q, k, v, do = make_qkv(w, device="cuda")
+    with aa.Plan(cu, T, w.num_q_heads, w.num_kv_heads, w.head_dim, w.rope_base) as p:
+        o, lse = p.fwd(q, k, v)
+        dq, dk, dv = p.bwd(q, k, v, o, lse, do)
+        torch.cuda.synchronize()
+        p.check_device_error()
+    lens = np.diff(cu)
+    order = np.argsort(lens)
+    picks = sorted({int(order[0]), int(order[len(order) // 2]), int(order[-1])} if lens.max() <= 4096
+                   else {int(order[0]), int(order[len(order) // 2])})
+    host = [t.cpu() for t in (q, k, v, do)]
+    for d in picks:
+        a, b = int(cu[d]), int(cu[d + 1])
+        idx = torch.from_numpy(np.concatenate([[0], np.arange(a, b)]))
+        sub = orc.Problem([1, b - a + 1], b - a + 1, w.num_q_heads, w.num_kv_heads, w.head_dim, w.rope_base)
+        gq, gk, gv = orc.backward(sub, *(t[idx] for t in host))
+        for nm, got, ref in (("dq", dq[a:b], gq[1:]), ("dk", dk[a:b], gk[1:]), ("dv", dv[a:b], gv[1:])):
+            e = rel_l2(got, ref)
+            assert e <= REL_L2, f"{name} doc {d} ({b - a} tokens) {nm} rel-L2 {e:.3e}"
