@@ -15,9 +15,9 @@
 //      fp32 dQ accumulator is initialised with scale*dS_i0*k~_0 (so it needs
 //      no separate clearing pass) and per-chunk partial sums of dv_0, dk~_0
 //      are written.
-//   2. attn_bwd: one CTA per (key tile, kv head), K~/V stationary in shared
-//      memory, looping over the group's query heads and the live query
-//      tiles. Five tcgen05 MMAs per tile (S^T, dP^T, dV, dK, dQ) with fp32
+//   2. attn_bwd: persistent, one CTA per SM walking a list of (key tile, kv
+//      head) items; per item K~/V stay in shared memory while it loops over
+//      the group's query heads and the live query tiles. Five tcgen05 MMAs per tile (S^T, dP^T, dV, dK, dQ) with fp32
 //      TMEM accumulators; dQ~ is added into the fp32 accumulator (TMA bulk
 //      reductions for D = 128, vector atomics for D = 64); dK/dV are rotated
 //      back and written once.
@@ -209,21 +209,32 @@ __global__ void __launch_bounds__(kPrepThreads) bwd_prep_kernel(const __nv_bfloa
 }
 
 // ---------------------------------------------------------------- 2. main
-// One CTA per (key tile, kv head), 512 threads:
-//   warp 0      TMA producer: K, V once; Q_i, dO_i through a 2-stage ring
+// Persistent: one CTA per SM, each walking its own list of (key tile, kv
+// head) items (the planner's schedule). An item keeps K~/V stationary in
+// shared memory and loops over the group's query heads and live query tiles.
+// 512 threads:
+//   warp 0      TMA producer: an item's K, V once it may overwrite them; Q_i,
+//               dO_i through a 2-stage ring that runs on across items
 //   warp 1      TMEM owner and MMA issuer (one thread)
 //   warps 2-3   staging of each query tile's -LSE*log2(e) and -D rows into
 //               shared memory (Q and K arrive rotated from the workspace: a
-//               per-CTA rotation in the tile load cost more than the once-per-
-//               call pass, since most CTAs here run only a handful of tiles)
+//               rotation in the tile load cost more than the once-per-call
+//               pass, since most items run only a handful of tiles)
 //   warps 4-11  P/dS: two groups (query columns 0-63 and 64-127), thread = key
 //               row = TMEM lane; P^T packed bf16 into TMEM for the dV product,
-//               dS^T bf16 into shared memory
+//               dS^T bf16 into shared memory; at the end of an item they read
+//               dV and dK~ out of TMEM and write dv, dk
 //   warps 12-15 dQ drain: dQ~ from TMEM into the fp32 accumulator. For
 //               D = 128 the MMA produces dQ~^T (lane = channel); the drain
 //               copies it into the step's dead Q~/dO stage buffers, releases
 //               TMEM at once and adds the copy with TMA bulk reductions that
 //               overlap the next tile; for D = 64 it uses vector atomics.
+// Between items nothing drains: the next item's K~/V load waits only for the
+// last MMA that reads the old ones, and its first S^T / dP^T products run
+// while the P/dS warps are still writing the previous item's dk, dv. The
+// next item's first dV / dK~ products need those TMEM columns back; they come
+// after the P/dS warps' first arrival of that item, which follows their
+// epilogue reads.
 // TMEM columns: S^T [0,128) (P^T over [0,32) and [64,96)), dP^T [128,256) (dQ~
 // or dQ~^T reuses [128,256) once dS is formed), dV [256,256+D), dK~ [256+D,256+2D).
 constexpr int kBwdThreads = 512;
@@ -238,7 +249,7 @@ struct BwdSmem {
   alignas(1024) uint8_t dst[2][16384];  // dS^T: 128 keys x 128 query rows, bf16
   float lse2[2][128];                   // -LSE * log2(e) of each stage's query rows
   float dsum[2][128];                   // -D of each stage's query rows
-  uint64_t kv_full, k_ready;
+  uint64_t kv_full, kv_free;
   uint64_t qd_full[2], q_ready[2], qd_empty[2];
   uint64_t st_full, p_full, dq_full, dq_free, o_full, drain;
   uint32_t tmem_base;
@@ -252,7 +263,8 @@ struct BwdParams {
   Workspace ws;
   const int32_t* pos_id;
   const int32_t* key_hi;
-  const WorkItem* items;
+  const WorkItem* items;      // all CTAs' lists, CTA-major
+  const int32_t* cta_start;   // CTA c runs items[cta_start[c], cta_start[c + 1])
   const float2* rope_hi;
   const float2* rope_lo;
   const float2* rope_step;
@@ -261,6 +273,20 @@ struct BwdParams {
   int T, Hq, Hkv, group, layout;
   float scale;
 };
+
+// One item as the roles see it: key tile kt of kv head g; step s (0 <= s <
+// n_steps) is query head g * group + s / n_qt, query tile lo + s % n_qt.
+struct BwdItem {
+  int kt, g, lo, n_qt, n_steps;
+  __device__ int head(int step, int group) const { return g * group + step / n_qt; }
+  __device__ int qtile(int step) const { return lo + step % n_qt; }
+};
+
+__device__ __forceinline__ BwdItem load_item(const BwdParams& P, int it) {
+  const WorkItem w = P.items[it];
+  const int n_qt = w.hi - w.lo + 1;
+  return BwdItem{w.tile, w.head, w.lo, n_qt, n_qt * P.group};
+}
 
 __device__ __forceinline__ bool bwd_wait(uint64_t* bar, uint32_t parity, const BwdParams& P,
                                          volatile int* abort_flag, int site) {
@@ -278,7 +304,10 @@ __device__ __forceinline__ bool bwd_wait(uint64_t* bar, uint32_t parity, const B
   }
 }
 
-
+// Barrier phases: per-step barriers count the CTA's steps across all its
+// items (gs); per-item barriers (kv_full, kv_free, o_full) count its items
+// (li). Every wait is bounded; a timeout records the site in the error word
+// and stops every role of the CTA.
 template <int HD>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     attn_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
@@ -295,10 +324,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   constexpr int kTmemCols = 512;
   constexpr uint32_t kTileBytes = 128 * HD * 2;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const WorkItem item = P.items[blockIdx.x];
-  const int kt = item.tile, g = item.head;
-  const int n_qt = item.hi - item.lo + 1;
-  const int n_steps = n_qt * P.group;
+  const int it_begin = __ldg(P.cta_start + blockIdx.x), it_end = __ldg(P.cta_start + blockIdx.x + 1);
   volatile int* abort_flag = &sm.abort_flag;
 
   if (tid == 0) {
@@ -307,7 +333,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     ptx::tma_prefetch_desc(&tmV);
     ptx::tma_prefetch_desc(&tmDO);
     ptx::mbar_init(&sm.kv_full, 1);
-    ptx::mbar_init(&sm.k_ready, 64);
+    ptx::mbar_init(&sm.kv_free, 1);
     for (int s = 0; s < 2; ++s) {
       ptx::mbar_init(&sm.qd_full[s], 1);
       ptx::mbar_init(&sm.q_ready[s], 64);
@@ -329,31 +355,40 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   const uint32_t tmem = sm.tmem_base;
   const uint32_t t_s = tmem, t_dp = tmem + 128, t_dq = tmem + 128, t_dv = tmem + 256, t_dk = tmem + 256 + HD;
 
-  auto step_head = [&](int step) { return g * P.group + step / n_qt; };
-  auto step_qt = [&](int step) { return item.lo + step % n_qt; };
-
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
-      ptx::mbar_arrive_expect_tx(&sm.kv_full, 2 * kTileBytes);
-      for (int b = 0; b < HD / 64; ++b) {
-        ptx::tma_load_3d(sm.k[b], &tmK, &sm.kv_full, b * 64, g, kt * kTile);
-        ptx::tma_load_3d(sm.v[b], &tmV, &sm.kv_full, b * 64, g, kt * kTile);
-      }
-      int n_issued = 0;
+      int gs = 0, n_issued = 0, li_loaded = -1;
       bool ok = true;
-      for (int step = 0; step < n_steps; ++step, ++n_issued) {
-        const int s = step & 1;
-        if (step >= 2) ok = bwd_wait(&sm.qd_empty[s], ((step >> 1) - 1) & 1, P, abort_flag, 401);
+      for (int it = it_begin; it < it_end && ok; ++it) {
+        const int li = it - it_begin;
+        const BwdItem w = load_item(P, it);
+        // the previous item's last MMA has read K~/V
+        if (li > 0) ok = bwd_wait(&sm.kv_free, (li - 1) & 1, P, abort_flag, 400);
         if (!ok) break;
-        const int h = step_head(step), qt = step_qt(step);
-        ptx::mbar_arrive_expect_tx(&sm.qd_full[s], 2 * kTileBytes);
+        ptx::mbar_arrive_expect_tx(&sm.kv_full, 2 * kTileBytes);
         for (int b = 0; b < HD / 64; ++b) {
-          ptx::tma_load_3d(sm.q[s][b], &tmQ, &sm.qd_full[s], b * 64, h, qt * kTile);
-          ptx::tma_load_3d(sm.dout[s][b], &tmDO, &sm.qd_full[s], b * 64, h, qt * kTile);
+          ptx::tma_load_3d(sm.k[b], &tmK, &sm.kv_full, b * 64, w.g, w.kt * kTile);
+          ptx::tma_load_3d(sm.v[b], &tmV, &sm.kv_full, b * 64, w.g, w.kt * kTile);
+        }
+        li_loaded = li;
+        for (int step = 0; step < w.n_steps; ++step, ++gs) {
+          const int s = gs & 1;
+          if (gs >= 2) ok = bwd_wait(&sm.qd_empty[s], ((gs >> 1) - 1) & 1, P, abort_flag, 401);
+          if (!ok) break;
+          const int h = w.head(step, P.group), qt = w.qtile(step);
+          ptx::mbar_arrive_expect_tx(&sm.qd_full[s], 2 * kTileBytes);
+          for (int b = 0; b < HD / 64; ++b) {
+            ptx::tma_load_3d(sm.q[s][b], &tmQ, &sm.qd_full[s], b * 64, h, qt * kTile);
+            ptx::tma_load_3d(sm.dout[s][b], &tmDO, &sm.qd_full[s], b * 64, h, qt * kTile);
+          }
+          n_issued = gs + 1;
         }
       }
-      ptx::mbar_wait(&sm.kv_full, 0, kDrainLimitNs, P.err, 409);
+      // no copy may be in flight when the CTA exits (matters after an abort);
+      // every earlier phase of these barriers completed before the next
+      // copy into the same buffer was issued
+      if (li_loaded >= 0) ptx::mbar_wait(&sm.kv_full, li_loaded & 1, kDrainLimitNs, P.err, 409);
       for (int u = (n_issued > 2 ? n_issued - 2 : 0); u < n_issued; ++u)
         ptx::mbar_wait(&sm.qd_full[u & 1], (u >> 1) & 1, kDrainLimitNs, P.err, 409);
     }
@@ -365,58 +400,70 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       constexpr uint32_t idesc_qd = ptx::idesc_bf16_f32(128, HD, 1, 1);   // dQ
       const uint32_t sk = ptx::smem_u32(sm.k[0]), sv = ptx::smem_u32(sm.v[0]);
       const uint32_t sds = ptx::smem_u32(sm.dst[0]);
-      bool ok = bwd_wait(&sm.k_ready, 0, P, abort_flag, 411);
-      for (int step = 0; step < n_steps && ok; ++step) {
-        const int s = step & 1;
-        const uint32_t sq = ptx::smem_u32(sm.q[s][0]), sdo = ptx::smem_u32(sm.dout[s][0]);
-        // the products need only the tiles; the LSE/D rows are for P/dS
-        ok = bwd_wait(&sm.qd_full[s], (step >> 1) & 1, P, abort_flag, 412);
-        if (!ok) break;
-        ptx::tc_fence_after();
-        for (int kk = 0; kk < HD / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-          ptx::mma_bf16(t_s, ptx::smem_desc_sw128(sk + off, 16, 1024), ptx::smem_desc_sw128(sq + off, 16, 1024),
-                        idesc_kt, kk > 0);
-        }
-        if (step > 0) {
-          // dQ~ of the previous tile must be drained before dP^T overwrites it
-          ok = bwd_wait(&sm.dq_free, (step - 1) & 1, P, abort_flag, 413);
+      int gs = 0;
+      bool ok = true;
+      for (int it = it_begin; it < it_end && ok; ++it) {
+        const int li = it - it_begin;
+        const int n_steps = load_item(P, it).n_steps;
+        ok = bwd_wait(&sm.kv_full, li & 1, P, abort_flag, 411);
+        for (int step = 0; step < n_steps && ok; ++step, ++gs) {
+          const int s = gs & 1;
+          const uint32_t sq = ptx::smem_u32(sm.q[s][0]), sdo = ptx::smem_u32(sm.dout[s][0]);
+          // the products need only the tiles; the LSE/D rows are for P/dS
+          ok = bwd_wait(&sm.qd_full[s], (gs >> 1) & 1, P, abort_flag, 412);
           if (!ok) break;
           ptx::tc_fence_after();
+          for (int kk = 0; kk < HD / 16; ++kk) {
+            const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+            ptx::mma_bf16(t_s, ptx::smem_desc_sw128(sk + off, 16, 1024), ptx::smem_desc_sw128(sq + off, 16, 1024),
+                          idesc_kt, kk > 0);
+          }
+          if (gs > 0) {
+            // dQ~ of the previous tile must be drained before dP^T overwrites it
+            ok = bwd_wait(&sm.dq_free, (gs - 1) & 1, P, abort_flag, 413);
+            if (!ok) break;
+            ptx::tc_fence_after();
+          }
+          for (int kk = 0; kk < HD / 16; ++kk) {
+            const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+            ptx::mma_bf16(t_dp, ptx::smem_desc_sw128(sv + off, 16, 1024),
+                          ptx::smem_desc_sw128(sdo + off, 16, 1024), idesc_kt, kk > 0);
+          }
+          ptx::mma_commit(&sm.st_full);
+          // P/dS of this step; at an item's first step this also means the
+          // P/dS warps have read the previous item's dV / dK~ out of TMEM
+          ok = bwd_wait(&sm.p_full, gs & 1, P, abort_flag, 414);
+          if (!ok) break;
+          ptx::tc_fence_after();
+          for (int kk = 0; kk < 8; ++kk)  // dV += P^T dO (P^T from TMEM: q 0-63 at cols 0-31, 64-127 at 64-95)
+            ptx::mma_bf16_ts(t_dv, t_s + (kk < 4 ? kk * 8 : 64 + (kk - 4) * 8),
+                             ptx::smem_desc_sw128(sdo + kk * 2048, 16384, 1024), idesc_kd,
+                             (step > 0 || kk > 0) ? 1u : 0u);
+          for (int kk = 0; kk < 8; ++kk) {  // dK~ += dS^T Q~
+            const uint32_t aoff = (kk >> 2) * 16384 + (kk & 3) * 32;
+            ptx::mma_bf16(t_dk, ptx::smem_desc_sw128(sds + aoff, 16, 1024),
+                          ptx::smem_desc_sw128(sq + kk * 2048, 16384, 1024), idesc_kd,
+                          (step > 0 || kk > 0) ? 1u : 0u);
+          }
+          if constexpr (HD == 128) {
+            // dQ~^T = K~^T dS^T: TMEM lanes = channels, columns = query rows, so
+            // the drain's reductions are 128-byte coalesced per warp
+            constexpr uint32_t idesc_qt = ptx::idesc_bf16_f32(128, 128, 1, 1);
+            for (int kk = 0; kk < 8; ++kk)
+              ptx::mma_bf16(t_dq, ptx::smem_desc_sw128(sk + kk * 2048, 16384, 1024),
+                            ptx::smem_desc_sw128(sds + kk * 2048, 16384, 1024), idesc_qt, kk > 0 ? 1u : 0u);
+          } else {
+            for (int kk = 0; kk < 8; ++kk)  // dQ~ = dS K~ (TMEM lanes = query rows)
+              ptx::mma_bf16(t_dq, ptx::smem_desc_sw128(sds + kk * 2048, 16384, 1024),
+                            ptx::smem_desc_sw128(sk + kk * 2048, 16384, 1024), idesc_qd, kk > 0 ? 1u : 0u);
+          }
+          ptx::mma_commit(&sm.dq_full);  // the drain hands stage s back to the producer
         }
-        for (int kk = 0; kk < HD / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-          ptx::mma_bf16(t_dp, ptx::smem_desc_sw128(sv + off, 16, 1024), ptx::smem_desc_sw128(sdo + off, 16, 1024),
-                        idesc_kt, kk > 0);
+        if (ok) {
+          ptx::mma_commit(&sm.kv_free);  // K~/V read for the last time
+          ptx::mma_commit(&sm.o_full);   // dV, dK~ complete
         }
-        ptx::mma_commit(&sm.st_full);
-        ok = bwd_wait(&sm.p_full, step & 1, P, abort_flag, 414);
-        if (!ok) break;
-        ptx::tc_fence_after();
-        for (int kk = 0; kk < 8; ++kk)  // dV += P^T dO (P^T from TMEM: q 0-63 at cols 0-31, 64-127 at 64-95)
-          ptx::mma_bf16_ts(t_dv, t_s + (kk < 4 ? kk * 8 : 64 + (kk - 4) * 8),
-                           ptx::smem_desc_sw128(sdo + kk * 2048, 16384, 1024), idesc_kd,
-                           (step > 0 || kk > 0) ? 1u : 0u);
-        for (int kk = 0; kk < 8; ++kk) {  // dK~ += dS^T Q~
-          const uint32_t aoff = (kk >> 2) * 16384 + (kk & 3) * 32;
-          ptx::mma_bf16(t_dk, ptx::smem_desc_sw128(sds + aoff, 16, 1024),
-                        ptx::smem_desc_sw128(sq + kk * 2048, 16384, 1024), idesc_kd, (step > 0 || kk > 0) ? 1u : 0u);
-        }
-        if constexpr (HD == 128) {
-          // dQ~^T = K~^T dS^T: TMEM lanes = channels, columns = query rows, so
-          // the drain's reductions are 128-byte coalesced per warp
-          constexpr uint32_t idesc_qt = ptx::idesc_bf16_f32(128, 128, 1, 1);
-          for (int kk = 0; kk < 8; ++kk)
-            ptx::mma_bf16(t_dq, ptx::smem_desc_sw128(sk + kk * 2048, 16384, 1024),
-                          ptx::smem_desc_sw128(sds + kk * 2048, 16384, 1024), idesc_qt, kk > 0 ? 1u : 0u);
-        } else {
-          for (int kk = 0; kk < 8; ++kk)  // dQ~ = dS K~ (TMEM lanes = query rows)
-            ptx::mma_bf16(t_dq, ptx::smem_desc_sw128(sds + kk * 2048, 16384, 1024),
-                          ptx::smem_desc_sw128(sk + kk * 2048, 16384, 1024), idesc_qd, kk > 0 ? 1u : 0u);
-        }
-        ptx::mma_commit(&sm.dq_full);  // the drain hands stage s back to the producer
       }
-      if (ok) ptx::mma_commit(&sm.o_full);
       ptx::mma_commit(&sm.drain);
       ptx::mbar_wait(&sm.drain, 0, kDrainLimitNs, P.err, 419);
     }
@@ -424,86 +471,97 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     // ------------------------------------------------------------ P / dS
     const int r = tid & 127;
     const int cq = (warp - 4) >> 2;  // query columns [64 cq, 64 cq + 64)
-    const int j = kt * kTile + r;
-    const bool key_valid = j < P.T;
-    const int jhi = key_valid ? __ldg(P.key_hi + j) : -1;  // rows [j, jhi] see key j
     const float sl2 = P.scale * kLog2e;
     const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
+    int gs = 0;
     bool ok = true;
-    for (int step = 0; step < n_steps && ok; ++step) {
-      const int s = step & 1, i0 = step_qt(step) * kTile;
-      const bool full = __all_sync(0xffffffffu, j <= i0 && i0 + kTile - 1 <= jhi);
-      ok = bwd_wait(&sm.q_ready[s], (step >> 1) & 1, P, abort_flag, 420);  // LSE/D staged
-      if (ok) ok = bwd_wait(&sm.st_full, step & 1, P, abort_flag, 421);
-      if (!ok) break;
-      ptx::tc_fence_after();
-      const float4* lse_s = reinterpret_cast<const float4*>(sm.lse2[s]);
-      const float4* d_s = reinterpret_cast<const float4*>(sm.dsum[s]);
+    for (int it = it_begin; it < it_end && ok; ++it) {
+      const int li = it - it_begin;
+      const BwdItem w = load_item(P, it);
+      const int j = w.kt * kTile + r;
+      const bool key_valid = j < P.T;
+      const int jhi = key_valid ? __ldg(P.key_hi + j) : -1;  // rows [j, jhi] see key j
+      for (int step = 0; step < w.n_steps && ok; ++step, ++gs) {
+        const int s = gs & 1, i0 = w.qtile(step) * kTile;
+        const bool full = __all_sync(0xffffffffu, j <= i0 && i0 + kTile - 1 <= jhi);
+        ok = bwd_wait(&sm.q_ready[s], (gs >> 1) & 1, P, abort_flag, 420);  // LSE/D staged
+        if (ok) ok = bwd_wait(&sm.st_full, gs & 1, P, abort_flag, 421);
+        if (!ok) break;
+        ptx::tc_fence_after();
+        const float4* lse_s = reinterpret_cast<const float4*>(sm.lse2[s]);
+        const float4* d_s = reinterpret_cast<const float4*>(sm.dsum[s]);
 #pragma unroll 1
-      for (int c = 2 * cq; c < 2 * cq + 2; ++c) {
-        float sv[32], dpv[32];
-        ptx::tmem_ld32(t_s + lane_off + c * 32, sv);
-        ptx::tmem_ld32(t_dp + lane_off + c * 32, dpv);
-        ptx::tmem_wait_ld();
+        for (int c = 2 * cq; c < 2 * cq + 2; ++c) {
+          float sv[32], dpv[32];
+          ptx::tmem_ld32(t_s + lane_off + c * 32, sv);
+          ptx::tmem_ld32(t_dp + lane_off + c * 32, dpv);
+          ptx::tmem_wait_ld();
 #pragma unroll
-        for (int gq = 0; gq < 4; ++gq) {  // 8 query columns at a time
-          const int cb = c * 32 + gq * 8;
-          float lse2[8], dd[8];
+          for (int gq = 0; gq < 4; ++gq) {  // 8 query columns at a time
+            const int cb = c * 32 + gq * 8;
+            float lse2[8], dd[8];
 #pragma unroll
-          for (int e = 0; e < 8; e += 4) {
-            const float4 a4 = lse_s[(cb + e) >> 2], b4 = d_s[(cb + e) >> 2];
-            lse2[e] = a4.x; lse2[e + 1] = a4.y; lse2[e + 2] = a4.z; lse2[e + 3] = a4.w;
-            dd[e] = b4.x; dd[e + 1] = b4.y; dd[e + 2] = b4.z; dd[e + 3] = b4.w;
-          }
-          uint32_t pw[4], dw[4];
-          if (full) {
-            const float2 sl22 = make_float2(sl2, sl2);
-#pragma unroll
-            for (int e = 0; e < 8; e += 2) {
-              const int x = gq * 8 + e;
-              const float2 a = __ffma2_rn(make_float2(sv[x], sv[x + 1]), sl22, make_float2(lse2[e], lse2[e + 1]));
-              const float2 pp = make_float2(ptx::ex2(a.x), ptx::ex2(a.y));
-              const float2 dd2 = __fmul2_rn(pp, __fadd2_rn(make_float2(dpv[x], dpv[x + 1]), make_float2(dd[e], dd[e + 1])));
-              pw[e / 2] = ptx::pack_bf16x2(pp.x, pp.y);
-              dw[e / 2] = ptx::pack_bf16x2(dd2.x, dd2.y);
+            for (int e = 0; e < 8; e += 4) {
+              const float4 a4 = lse_s[(cb + e) >> 2], b4 = d_s[(cb + e) >> 2];
+              lse2[e] = a4.x; lse2[e + 1] = a4.y; lse2[e + 2] = a4.z; lse2[e + 3] = a4.w;
+              dd[e] = b4.x; dd[e + 1] = b4.y; dd[e + 2] = b4.z; dd[e + 3] = b4.w;
             }
-          } else {
+            uint32_t pw[4], dw[4];
+            if (full) {
+              const float2 sl22 = make_float2(sl2, sl2);
 #pragma unroll
-            for (int e = 0; e < 8; e += 2) {
-              const int x = gq * 8 + e;
-              const int i = i0 + cb + e;
-              // masked elements feed -inf to ex2 (2^-inf = 0): selects, no branches
-              const float p0 = ptx::ex2((i >= j && i <= jhi) ? fmaf(sv[x], sl2, lse2[e]) : -INFINITY);
-              const float p1 = ptx::ex2((i + 1 >= j && i + 1 <= jhi) ? fmaf(sv[x + 1], sl2, lse2[e + 1]) : -INFINITY);
-              pw[e / 2] = ptx::pack_bf16x2(p0, p1);
-              dw[e / 2] = ptx::pack_bf16x2(p0 * (dpv[x] + dd[e]), p1 * (dpv[x + 1] + dd[e + 1]));
+              for (int e = 0; e < 8; e += 2) {
+                const int x = gq * 8 + e;
+                const float2 a =
+                    __ffma2_rn(make_float2(sv[x], sv[x + 1]), sl22, make_float2(lse2[e], lse2[e + 1]));
+                const float2 pp = make_float2(ptx::ex2(a.x), ptx::ex2(a.y));
+                const float2 dd2 =
+                    __fmul2_rn(pp, __fadd2_rn(make_float2(dpv[x], dpv[x + 1]), make_float2(dd[e], dd[e + 1])));
+                pw[e / 2] = ptx::pack_bf16x2(pp.x, pp.y);
+                dw[e / 2] = ptx::pack_bf16x2(dd2.x, dd2.y);
+              }
+            } else {
+#pragma unroll
+              for (int e = 0; e < 8; e += 2) {
+                const int x = gq * 8 + e;
+                const int i = i0 + cb + e;
+                // masked elements feed -inf to ex2 (2^-inf = 0): selects, no branches
+                const float p0 = ptx::ex2((i >= j && i <= jhi) ? fmaf(sv[x], sl2, lse2[e]) : -INFINITY);
+                const float p1 =
+                    ptx::ex2((i + 1 >= j && i + 1 <= jhi) ? fmaf(sv[x + 1], sl2, lse2[e + 1]) : -INFINITY);
+                pw[e / 2] = ptx::pack_bf16x2(p0, p1);
+                dw[e / 2] = ptx::pack_bf16x2(p0 * (dpv[x] + dd[e]), p1 * (dpv[x + 1] + dd[e + 1]));
+              }
             }
+            // P^T packs over S^T columns this group has already read: query
+            // columns [64 cq, 64 cq + 64) land in TMEM columns [64 cq, 64 cq + 32)
+            ptx::tmem_st4(t_s + lane_off + 64 * cq + (c - 2 * cq) * 16 + gq * 4, pw);
+            const int c8 = c * 4 + gq;  // 16-byte chunk along the 128 query columns
+            *reinterpret_cast<uint4*>(sm.dst[c8 >> 3] + sw128_chunk(r, c8 & 7)) =
+                make_uint4(dw[0], dw[1], dw[2], dw[3]);
           }
-          // P^T packs over S^T columns this group has already read: query
-          // columns [64 cq, 64 cq + 64) land in TMEM columns [64 cq, 64 cq + 32)
-          ptx::tmem_st4(t_s + lane_off + 64 * cq + (c - 2 * cq) * 16 + gq * 4, pw);
-          const int c8 = c * 4 + gq;  // 16-byte chunk along the 128 query columns
-          *reinterpret_cast<uint4*>(sm.dst[c8 >> 3] + sw128_chunk(r, c8 & 7)) = make_uint4(dw[0], dw[1], dw[2], dw[3]);
         }
+        ptx::tmem_wait_st();
+        ptx::fence_proxy_async_smem();
+        ptx::tc_fence_before();
+        ptx::mbar_arrive(&sm.p_full);
       }
-      ptx::tmem_wait_st();
-      ptx::fence_proxy_async_smem();
-      ptx::tc_fence_before();
-      ptx::mbar_arrive(&sm.p_full);
-    }
-    if (ok) ok = bwd_wait(&sm.o_full, 0, P, abort_flag, 423);
-    if (ok) {
-      // ---- epilogue: dV and dk = R^T (scale dK~) for this thread's key row
+      if (ok) ok = bwd_wait(&sm.o_full, li & 1, P, abort_flag, 423);
+      if (!ok) break;
+      // ---- epilogue: dV and dk = R^T (scale dK~) for this thread's key row.
+      // Its TMEM reads all complete (tmem_wait_ld) before this thread's next
+      // p_full arrival, which the next item's dV / dK~ products wait for.
       ptx::tc_fence_after();
-      __nv_bfloat16* dvrow = P.dv + ((size_t)(key_valid ? j : 0) * P.Hkv + g) * HD;
-      __nv_bfloat16* dkrow = P.dk + ((size_t)(key_valid ? j : 0) * P.Hkv + g) * HD;
+      __nv_bfloat16* dvrow = P.dv + ((size_t)(key_valid ? j : 0) * P.Hkv + w.g) * HD;
+      __nv_bfloat16* dkrow = P.dk + ((size_t)(key_valid ? j : 0) * P.Hkv + w.g) * HD;
       const int pos = key_valid ? __ldg(P.pos_id + j) : 0;
       auto store32 = [&](__nv_bfloat16* row, int c0, const float* x) {
         uint4* dst = reinterpret_cast<uint4*>(row + c0);
 #pragma unroll
         for (int c = 0; c < 4; ++c)
           dst[c] = make_uint4(ptx::pack_bf16x2(x[8 * c], x[8 * c + 1]), ptx::pack_bf16x2(x[8 * c + 2], x[8 * c + 3]),
-                              ptx::pack_bf16x2(x[8 * c + 4], x[8 * c + 5]), ptx::pack_bf16x2(x[8 * c + 6], x[8 * c + 7]));
+                              ptx::pack_bf16x2(x[8 * c + 4], x[8 * c + 5]),
+                              ptx::pack_bf16x2(x[8 * c + 6], x[8 * c + 7]));
       };
       // dk unit u: 32 channels (adjacent pairs or no rotation) or, for the
       // half-split pairing, channels [32u, 32u + 32) with their partners D/2 on
@@ -565,61 +623,65 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     // ------------------------------------------------------------ dQ drain
     const int r = tid & 127;
     const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
+    int gs = 0;
     bool ok = true;
-    for (int step = 0; step < n_steps && ok; ++step) {
-      const int h = step_head(step), i0 = step_qt(step) * kTile;
-      ok = bwd_wait(&sm.dq_full, step & 1, P, abort_flag, 431);
-      ok = ptx::bar_and(3, 128, ok);  // the drain group moves on (or stops) as one
-      if (!ok) break;
-      ptx::tc_fence_after();
-      if constexpr (HD == 128) {
-        // lane r = channel. The step's Q~ / dO stage buffers are dead once its
-        // MMAs are done, so they hold scale*dQ~ as two [128 rows][64 channels]
-        // fp32 blocks: TMEM is released as soon as it is read, and two TMA
-        // bulk reductions add the blocks to the accumulator while the next
-        // tile computes. The stage returns to the producer once read.
-        const int s = step & 1;
-        float* stage = reinterpret_cast<float*>((r >> 6) == 0 ? sm.q[s][0] : sm.dout[s][0]);
-        const int ch = r & 63;
+    for (int it = it_begin; it < it_end && ok; ++it) {
+      const BwdItem w = load_item(P, it);
+      for (int step = 0; step < w.n_steps && ok; ++step, ++gs) {
+        const int h = w.head(step, P.group), i0 = w.qtile(step) * kTile;
+        ok = bwd_wait(&sm.dq_full, gs & 1, P, abort_flag, 431);
+        ok = ptx::bar_and(3, 128, ok);  // the drain group moves on (or stops) as one
+        if (!ok) break;
+        ptx::tc_fence_after();
+        if constexpr (HD == 128) {
+          // lane r = channel. The step's Q~ / dO stage buffers are dead once its
+          // MMAs are done, so they hold scale*dQ~ as two [128 rows][64 channels]
+          // fp32 blocks: TMEM is released as soon as it is read, and two TMA
+          // bulk reductions add the blocks to the accumulator while the next
+          // tile computes. The stage returns to the producer once read.
+          const int s = gs & 1;
+          float* stage = reinterpret_cast<float*>((r >> 6) == 0 ? sm.q[s][0] : sm.dout[s][0]);
+          const int ch = r & 63;
 #pragma unroll 1
-        for (int c = 0; c < 4; ++c) {
-          float dq[32];
-          ptx::tmem_ld32(t_dq + lane_off + c * 32, dq);
-          ptx::tmem_wait_ld();
+          for (int c = 0; c < 4; ++c) {
+            float dq[32];
+            ptx::tmem_ld32(t_dq + lane_off + c * 32, dq);
+            ptx::tmem_wait_ld();
 #pragma unroll
-          for (int e = 0; e < 32; ++e) stage[(c * 32 + e) * 64 + ch] = P.scale * dq[e];
+            for (int e = 0; e < 32; ++e) stage[(c * 32 + e) * 64 + ch] = P.scale * dq[e];
+          }
+          ptx::tc_fence_before();
+          ptx::mbar_arrive(&sm.dq_free);
+          ptx::fence_proxy_async_smem();
+          asm volatile("bar.sync 3, 128;" ::: "memory");
+          if (r == 0) {
+            ptx::tma_reduce_add_3d(&tmDQ, sm.q[s][0], 0, h, i0);
+            ptx::tma_reduce_add_3d(&tmDQ, sm.dout[s][0], 64, h, i0);
+            ptx::bulk_commit();
+            ptx::bulk_wait_read0();
+            ptx::mbar_arrive(&sm.qd_empty[s]);
+          }
+          continue;
+        } else {
+          if (r == 0) ptx::mbar_arrive(&sm.qd_empty[gs & 1]);  // the step's MMAs are done
+          const int i = i0 + r;
+          float* dst = P.ws.dq_acc + ((size_t)(i < P.T ? i : 0) * P.Hq + h) * HD;
+#pragma unroll 1
+          for (int c = 0; c < HD / 32; ++c) {
+            float dq[32];
+            ptx::tmem_ld32(t_dq + lane_off + c * 32, dq);
+            ptx::tmem_wait_ld();
+            if (i < P.T) {
+#pragma unroll
+              for (int e = 0; e < 32; e += 4)
+                ptx::red_add_v4(dst + c * 32 + e, P.scale * dq[e], P.scale * dq[e + 1], P.scale * dq[e + 2],
+                                P.scale * dq[e + 3]);
+            }
+          }
         }
         ptx::tc_fence_before();
         ptx::mbar_arrive(&sm.dq_free);
-        ptx::fence_proxy_async_smem();
-        asm volatile("bar.sync 3, 128;" ::: "memory");
-        if (r == 0) {
-          ptx::tma_reduce_add_3d(&tmDQ, sm.q[s][0], 0, h, i0);
-          ptx::tma_reduce_add_3d(&tmDQ, sm.dout[s][0], 64, h, i0);
-          ptx::bulk_commit();
-          ptx::bulk_wait_read0();
-          ptx::mbar_arrive(&sm.qd_empty[s]);
-        }
-        continue;
-      } else {
-        if (r == 0) ptx::mbar_arrive(&sm.qd_empty[step & 1]);  // the step's MMAs are done
-        const int i = i0 + r;
-        float* dst = P.ws.dq_acc + ((size_t)(i < P.T ? i : 0) * P.Hq + h) * HD;
-#pragma unroll 1
-        for (int c = 0; c < HD / 32; ++c) {
-          float dq[32];
-          ptx::tmem_ld32(t_dq + lane_off + c * 32, dq);
-          ptx::tmem_wait_ld();
-          if (i < P.T) {
-#pragma unroll
-            for (int e = 0; e < 32; e += 4)
-              ptx::red_add_v4(dst + c * 32 + e, P.scale * dq[e], P.scale * dq[e + 1], P.scale * dq[e + 2],
-                              P.scale * dq[e + 3]);
-          }
-        }
       }
-      ptx::tc_fence_before();
-      ptx::mbar_arrive(&sm.dq_free);
     }
     if constexpr (HD == 128) {
       // the reductions must have read their shared-memory sources before the
@@ -627,22 +689,25 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       if (r == 0) ptx::bulk_wait_read0();
     }
   } else if (warp == 2 || warp == 3) {
-    // ------------------------------------------------------------ RoPE + LSE/D staging
+    // ------------------------------------------------------------ LSE/D staging
     const int t = tid - 64;
-    bool ok = bwd_wait(&sm.kv_full, 0, P, abort_flag, 441);
-    if (ok) ptx::mbar_arrive(&sm.k_ready);
-    for (int step = 0; step < n_steps && ok; ++step) {
-      const int s = step & 1;
-      const int i0 = step_qt(step) * kTile;
-      ok = bwd_wait(&sm.qd_full[s], (step >> 1) & 1, P, abort_flag, 442);
-      if (!ok) break;
-      const size_t hrow = (size_t)step_head(step) * P.T;
-      for (int r = t; r < kTile; r += 64) {
-        const int i = i0 + r;
-        sm.lse2[s][r] = i < P.T ? -__ldg(P.lse + hrow + i) * kLog2e : -INFINITY;  // -LSE log2(e)
-        sm.dsum[s][r] = i < P.T ? -__ldg(P.ws.dsum + hrow + i) : 0.f;             // -D
+    int gs = 0;
+    bool ok = true;
+    for (int it = it_begin; it < it_end && ok; ++it) {
+      const BwdItem w = load_item(P, it);
+      for (int step = 0; step < w.n_steps && ok; ++step, ++gs) {
+        const int s = gs & 1;
+        const int i0 = w.qtile(step) * kTile;
+        ok = bwd_wait(&sm.qd_full[s], (gs >> 1) & 1, P, abort_flag, 442);
+        if (!ok) break;
+        const size_t hrow = (size_t)w.head(step, P.group) * P.T;
+        for (int r = t; r < kTile; r += 64) {
+          const int i = i0 + r;
+          sm.lse2[s][r] = i < P.T ? -__ldg(P.lse + hrow + i) * kLog2e : -INFINITY;  // -LSE log2(e)
+          sm.dsum[s][r] = i < P.T ? -__ldg(P.ws.dsum + hrow + i) : 0.f;             // -D
+        }
+        ptx::mbar_arrive(&sm.q_ready[s]);
       }
-      ptx::mbar_arrive(&sm.q_ready[s]);
     }
   }
 
@@ -799,6 +864,7 @@ aa_status launch_bwd(aa_plan_s* p, const void* q, const void* k, const void* v, 
   P.pos_id = p->dev.pos_id;
   P.key_hi = p->dev.key_hi;
   P.items = p->dev.bwd_items;
+  P.cta_start = p->dev.bwd_cta_start;
   P.rope_hi = p->dev.rope_hi;
   P.rope_lo = p->dev.rope_lo;
   P.rope_step = p->dev.rope_step;
@@ -815,8 +881,12 @@ aa_status launch_bwd(aa_plan_s* p, const void* q, const void* k, const void* v, 
   if (e != cudaSuccess) return cuda_fail(e, "attn_bwd_kernel smem attribute");
   if (p->bwd_ev_start && (e = cudaEventRecord(p->bwd_ev_start, s)) != cudaSuccess)
     return cuda_fail(e, "recording the bwd start event");
-  attn_bwd_kernel<HD><<<(unsigned)p->bwd_items.size(), kBwdThreads, smem, s>>>(tq, tk, tv, tdo, tdq, P);
-  if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(e, "attn_bwd_kernel launch");
+  // persistent: one CTA per list of the planner's schedule (at most one per SM)
+  const unsigned n_cta = (unsigned)(p->bwd_cta_start.size() - 1);
+  if (!p->bwd_items.empty()) {
+    attn_bwd_kernel<HD><<<n_cta, kBwdThreads, smem, s>>>(tq, tk, tv, tdo, tdq, P);
+    if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(e, "attn_bwd_kernel launch");
+  }
   if (p->bwd_ev_stop && (e = cudaEventRecord(p->bwd_ev_stop, s)) != cudaSuccess)
     return cuda_fail(e, "recording the bwd stop event");
 

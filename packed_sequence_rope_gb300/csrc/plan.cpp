@@ -13,6 +13,7 @@
 #include <algorithm>
 #include <map>
 #include <new>
+#include <queue>
 #include <string>
 
 #include "aa_internal.h"
@@ -169,6 +170,36 @@ static void build_stats_and_work(aa_plan_s* p) {
   for (auto& w : p->bwd_items) p->bwd_tiles += (int64_t)(w.hi - w.lo + 1) * p->group;
 }
 
+// Persistent backward schedule: the kernel runs one CTA per SM, each walking
+// its own list of items. Items are dealt out in work-list order, each to the
+// CTA with the least estimated work so far (one unit per query-tile step plus
+// one for the item's K/V load and dK/dV epilogue, which mostly overlap the
+// neighbouring items), so the CTAs busy at any moment hold neighbouring items
+// of the list (the (document, head) grouping above keeps its L2 reuse) and
+// all CTAs finish close together. Ties go to the lower CTA index.
+static void build_bwd_schedule(aa_plan_s* p) {
+  const int n = (int)p->bwd_items.size();
+  const int ncta = std::max(1, std::min(n, p->num_sms));
+  std::vector<std::vector<WorkItem>> lists(ncta);
+  using Load = std::pair<int64_t, int>;
+  std::priority_queue<Load, std::vector<Load>, std::greater<Load>> least;
+  for (int c = 0; c < ncta; ++c) least.push({0, c});
+  for (const WorkItem& w : p->bwd_items) {
+    const Load top = least.top();
+    least.pop();
+    lists[top.second].push_back(w);
+    least.push({top.first + 1 + (int64_t)(w.hi - w.lo + 1) * p->group, top.second});
+  }
+  std::vector<WorkItem> flat;
+  flat.reserve(n);
+  p->bwd_cta_start.assign(1, 0);
+  for (const auto& l : lists) {
+    flat.insert(flat.end(), l.begin(), l.end());
+    p->bwd_cta_start.push_back((int32_t)flat.size());
+  }
+  p->bwd_items.swap(flat);
+}
+
 // Two-level cos/sin tables for Eq. 6: pos = 32*h + l, so
 // (cos, sin)(pos*theta_p) is the complex product of rope_hi[h][p] and
 // rope_lo[p][l]. Entries are computed in fp64 and rounded once to fp32.
@@ -216,7 +247,7 @@ static aa_status upload(T** dst, const std::vector<T>& src, cudaStream_t s, cons
 
 static void free_device(aa_plan_s* p) {
   DevicePlan& d = p->dev;
-  void* ptrs[] = {d.pos_id, d.row_lo, d.key_hi, d.fwd_items, d.bwd_items, d.qtile_klo,
+  void* ptrs[] = {d.pos_id, d.row_lo, d.key_hi, d.fwd_items, d.bwd_items, d.bwd_cta_start, d.qtile_klo,
                   d.rope_hi, d.rope_lo, d.rope_step, d.err, d.perm, d.pos_orig};
   for (void* q : ptrs)
     if (q) cudaFree(q);
@@ -351,6 +382,7 @@ static aa_status make_plan(const aa_config* cfg, const int32_t* cu_doclens_host,
     delete p;
     return cuda_fail(e, "device query");
   }
+  build_bwd_schedule(p);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   std::vector<int32_t> zero(1, 0);
   DevicePlan& d = p->dev;
@@ -359,6 +391,7 @@ static aa_status make_plan(const aa_config* cfg, const int32_t* cu_doclens_host,
       (st = upload(&d.key_hi, p->key_hi, s, "key_hi")) != AA_OK ||
       (st = upload(&d.fwd_items, p->fwd_items, s, "fwd work list")) != AA_OK ||
       (st = upload(&d.bwd_items, p->bwd_items, s, "bwd work list")) != AA_OK ||
+      (st = upload(&d.bwd_cta_start, p->bwd_cta_start, s, "bwd schedule")) != AA_OK ||
       (st = upload(&d.qtile_klo, p->qtile_klo, s, "query-tile key ranges")) != AA_OK ||
       (st = upload(&d.rope_hi, p->rope_hi, s, "rope table (hi)")) != AA_OK ||
       (st = upload(&d.rope_lo, p->rope_lo, s, "rope table (lo)")) != AA_OK ||
