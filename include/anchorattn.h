@@ -172,20 +172,20 @@ aa_status aa_rope_apply(aa_plan_t plan, const void* x, void* y, int32_t num_head
  *   O_i = sum_{j visible} softmax_j(scale * (R_i q_i).(R_j k_j)) v_j,
  *   LSE_i = ln sum_{j visible} exp(scale * (R_i q_i).(R_j k_j)).
  * q [T,Hq,D], k/v [T,Hkv,D] bf16 in; o [T,Hq,D] bf16, lse [Hq,T] fp32 out.
- * Query head h reads kv head h / (Hq / Hkv). Q is rotated inside the
- * attention kernel as its tiles load; K, which every query tile of its
- * document re-reads, is rotated once per call into `workspace` (caller-owned
- * device memory of at least aa_fwd_workspace_bytes(plan) bytes, 256-byte
- * aligned, contents ignored; NULL allowed when that size is 0). */
+ * Query head h reads kv head h / (Hq / Hkv). Q and K are rotated once per
+ * call into `workspace` (caller-owned device memory of at least
+ * aa_fwd_workspace_bytes(plan) bytes, 256-byte aligned, contents ignored;
+ * NULL allowed when that size is 0), which the attention kernel then reads. */
 aa_status aa_fwd(aa_plan_t plan, const void* q, const void* k, const void* v, void* o,
                  float* lse, void* workspace, size_t workspace_bytes, aa_stream_t stream);
 
-/* Bytes of device scratch aa_fwd needs (the rotated K, T*Hkv*D bf16; 0 with
- * AA_ROPE_NONE). */
+/* Bytes of device scratch aa_fwd needs (the rotated K and Q, T*(Hkv+Hq)*D
+ * bf16; 0 with AA_ROPE_NONE; segment plans add their grouped copies). */
 size_t aa_fwd_workspace_bytes(aa_plan_t plan);
 
-/* Bytes of device scratch aa_bwd needs (rotated Q, fp32 dQ accumulator,
- * per-row D, anchor partial sums). */
+/* Bytes of device scratch aa_bwd needs (rotated Q and K, fp32 dQ
+ * accumulator, per-row D, anchor partial sums; segment plans add their
+ * grouped copies). */
 size_t aa_bwd_workspace_bytes(aa_plan_t plan);
 
 /* Backward of aa_fwd: given dout = dL/dO, writes dq [T,Hq,D], dk/dv

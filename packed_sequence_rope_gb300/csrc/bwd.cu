@@ -307,7 +307,8 @@ __device__ __forceinline__ bool bwd_wait(uint64_t* bar, uint32_t parity, const B
 // Barrier phases: per-step barriers count the CTA's steps across all its
 // items (gs); per-item barriers (kv_full, kv_free, o_full) count its items
 // (li). Every wait is bounded; a timeout records the site in the error word
-// and stops every role of the CTA.
+// and stops every role of the CTA. Waits followed by warp-collective steps
+// are made warp-uniform by a vote (the drain group by a barrier reduction).
 template <int HD>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     attn_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
@@ -486,6 +487,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const bool full = __all_sync(0xffffffffu, j <= i0 && i0 + kTile - 1 <= jhi);
         ok = bwd_wait(&sm.q_ready[s], (gs >> 1) & 1, P, abort_flag, 420);  // LSE/D staged
         if (ok) ok = bwd_wait(&sm.st_full, gs & 1, P, abort_flag, 421);
+        ok = __all_sync(0xffffffffu, ok);  // the warp leaves (or stays) as one
         if (!ok) break;
         ptx::tc_fence_after();
         const float4* lse_s = reinterpret_cast<const float4*>(sm.lse2[s]);
@@ -547,6 +549,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         ptx::mbar_arrive(&sm.p_full);
       }
       if (ok) ok = bwd_wait(&sm.o_full, li & 1, P, abort_flag, 423);
+      ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       // ---- epilogue: dV and dk = R^T (scale dK~) for this thread's key row.
       // Its TMEM reads all complete (tmem_wait_ld) before this thread's next

@@ -8,17 +8,23 @@
 //   LSE_i = ln sum_{j visible} exp(scale * (R_i q_i).(R_j k_j))
 // with the visible set {0} U [row_lo_i, i] (ANCHOR) or [row_lo_i, i].
 //
-// How. K is rotated once per call by the standalone RoPE kernel into the
-// workspace (every query tile of a document re-reads it; rotating it on each
-// visit would cost as much CUDA-core work as the softmax). One CTA then runs
-// per (pair of 128-row query tiles, head), longest work first, 384 threads:
-//   warp 0      TMA producer: Q0/Q1 once, then rotated K / V tiles through a
-//               2-stage ring
+// How. Q and K are rotated once per call by the standalone RoPE kernel into
+// the workspace: every query tile of a document re-reads K, and a Q tile
+// rotated inside the attention kernel would put the rotation between one
+// item's last products and the next item's first. The attention kernel is
+// persistent: one CTA per SM walks its list of (pair of 128-row query tiles,
+// head) items, 384 threads:
+//   warp 0      TMA producer: each item's rotated Q0/Q1 as soon as the
+//               previous item's last S product of that tile has run, and the
+//               rotated K / V tiles through a 2-stage ring that runs on
+//               across items
 //   warp 1      TMEM owner and MMA issuer (one thread)
-//   warps 4-7   query tile 0: rotates Q0 in shared memory as it lands (RoPE
-//               fused into the Q tile load), then its online softmax
-//               (thread = query row = TMEM lane)
+//   warps 4-7   query tile 0: online softmax (thread = query row = TMEM lane)
+//               and epilogue
 //   warps 8-11  the same for query tile 1
+// Between items nothing drains: the next item's loads and first products
+// overlap the last key tiles and the epilogues, and group 0 writes its O
+// while group 1 finishes.
 // Tensor-memory columns: S0 [0,128) S1 [128,256) O0, O1 (D columns each). The
 // softmax writes P as packed bf16 over the first 64 columns of its S, and the
 // PV product reads it straight from TMEM (tcgen05.mma with A in TMEM).
@@ -44,9 +50,9 @@ struct FwdSmem {
   alignas(1024) uint8_t q[2][kB][16384];
   alignas(1024) uint8_t k[kStages][kB][16384];
   alignas(1024) uint8_t v[kStages][kB][16384];
-  uint64_t q_full, q_ready[2];
+  uint64_t q_full[2], q_free[2];
   uint64_t kv_full[kStages], kv_empty[kStages];
-  uint64_t s_full[2], p_full[2], o_full, drain;
+  uint64_t s_full[2], p_full[2], o_full[2], drain;
   uint32_t tmem_base;
   int abort_flag;
 };
@@ -59,7 +65,8 @@ struct FwdParams {
   const int32_t* pos_id;
   const int32_t* row_lo;
   const int32_t* qtile_klo;
-  const WorkItem* items;
+  const WorkItem* items;     // all CTAs' lists, CTA-major
+  const int32_t* cta_start;  // CTA c runs items[cta_start[c], cta_start[c + 1])
   const float2* rope_hi;
   const float2* rope_lo;
   const float2* rope_step;
@@ -68,6 +75,28 @@ struct FwdParams {
   int T, Hq, Hkv, group, layout, anchor, n_tiles;
   float scale;
 };
+
+// One item as the roles see it: query tiles qt0 and qt0 + 1 (when it exists)
+// of head h over key tiles [kt_lo, kt_hi]; query tile t visits [lo[t], hi[t]].
+struct FwdItem {
+  int h, qt0, kt_lo, kt_hi, lo[2], hi[2];
+  bool has1;
+};
+
+__device__ __forceinline__ FwdItem load_fwd_item(const FwdParams& P, int it) {
+  const WorkItem w = P.items[it];
+  FwdItem f;
+  f.h = w.head;
+  f.qt0 = 2 * w.tile;
+  f.kt_lo = w.lo;
+  f.kt_hi = w.hi;
+  f.has1 = f.qt0 + 1 < P.n_tiles;
+  f.lo[0] = __ldg(P.qtile_klo + f.qt0);
+  f.hi[0] = f.qt0;
+  f.lo[1] = f.has1 ? __ldg(P.qtile_klo + f.qt0 + 1) : 1;  // empty range for a missing second tile
+  f.hi[1] = f.has1 ? f.qt0 + 1 : 0;
+  return f;
+}
 
 // Bounded wait that also gives up as soon as another role of the CTA aborted.
 __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, const FwdParams& P,
@@ -86,6 +115,13 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, co
   }
 }
 
+// Barrier phases: the K/V ring counts the CTA's key-tile steps across its
+// items; s_full / p_full count each query tile's softmax steps; q_full,
+// q_free and o_full count the items in which the query tile exists.
+// The roles synchronise through mbarriers only (every wait bounded), so an
+// abort in one role never strands another at a named barrier; inside a warp
+// each wait's outcome is made uniform by a vote before any warp-collective
+// step, so no lane leaves a loop that the rest of its warp stays in.
 template <int HD>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
@@ -99,32 +135,24 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr uint32_t kTileBytes = 128 * HD * 2;
   constexpr int kTmemCols = 512;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const WorkItem item = P.items[blockIdx.x];
-  const int h = item.head, g = h / P.group;
-  const int qt0 = 2 * item.tile;
-  const bool has1 = qt0 + 1 < P.n_tiles;
-  // key-tile range of each query tile (empty for a missing second tile)
-  const int lo0 = __ldg(P.qtile_klo + qt0), hi0 = qt0;
-  const int lo1 = has1 ? __ldg(P.qtile_klo + qt0 + 1) : 1, hi1 = has1 ? qt0 + 1 : 0;
-  const int kt_lo = item.lo, kt_hi = item.hi;
+  const int it_begin = __ldg(P.cta_start + blockIdx.x), it_end = __ldg(P.cta_start + blockIdx.x + 1);
   volatile int* abort_flag = &sm.abort_flag;
 
   if (tid == 0) {
     ptx::tma_prefetch_desc(&tmQ);
     ptx::tma_prefetch_desc(&tmK);
     ptx::tma_prefetch_desc(&tmV);
-    ptx::mbar_init(&sm.q_full, 1);
-    ptx::mbar_init(&sm.q_ready[0], 128);
-    ptx::mbar_init(&sm.q_ready[1], 128);
+    for (int t = 0; t < 2; ++t) {
+      ptx::mbar_init(&sm.q_full[t], 1);
+      ptx::mbar_init(&sm.q_free[t], 128);
+      ptx::mbar_init(&sm.s_full[t], 1);
+      ptx::mbar_init(&sm.p_full[t], 128);
+      ptx::mbar_init(&sm.o_full[t], 1);
+    }
     for (int s = 0; s < kStages; ++s) {
       ptx::mbar_init(&sm.kv_full[s], 1);
       ptx::mbar_init(&sm.kv_empty[s], 1);
     }
-    for (int t = 0; t < 2; ++t) {
-      ptx::mbar_init(&sm.s_full[t], 1);
-      ptx::mbar_init(&sm.p_full[t], 128);
-    }
-    ptx::mbar_init(&sm.o_full, 1);
     ptx::mbar_init(&sm.drain, 1);
     sm.abort_flag = 0;
     ptx::fence_mbar_init();
@@ -138,26 +166,37 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
-      ptx::mbar_arrive_expect_tx(&sm.q_full, (has1 ? 2 : 1) * kTileBytes);
-      for (int b = 0; b < HD / 64; ++b) {
-        ptx::tma_load_3d(sm.q[0][b], &tmQ, &sm.q_full, b * 64, h, qt0 * kTile);
-        if (has1) ptx::tma_load_3d(sm.q[1][b], &tmQ, &sm.q_full, b * 64, h, (qt0 + 1) * kTile);
-      }
-      int n_issued = 0;
+      int nq[2] = {0, 0}, ks = 0;
       bool ok = true;
-      for (int kt = kt_lo; kt <= kt_hi && ok; ++kt, ++n_issued) {
-        const int s = n_issued % kStages;
-        if (n_issued >= kStages) ok = wait_or_abort(&sm.kv_empty[s], ((n_issued / kStages) - 1) & 1, P, abort_flag, 301);
-        if (!ok) break;
-        ptx::mbar_arrive_expect_tx(&sm.kv_full[s], 2 * kTileBytes);
-        for (int b = 0; b < HD / 64; ++b) {
-          ptx::tma_load_3d(sm.k[s][b], &tmK, &sm.kv_full[s], b * 64, g, kt * kTile);
-          ptx::tma_load_3d(sm.v[s][b], &tmV, &sm.kv_full[s], b * 64, g, kt * kTile);
+      for (int it = it_begin; it < it_end && ok; ++it) {
+        const FwdItem w = load_fwd_item(P, it);
+        const int g = w.h / P.group;
+        for (int t = 0; t < (w.has1 ? 2 : 1) && ok; ++t) {
+          // the tile's previous Q has had its last S product and its anchor dot
+          if (nq[t] > 0) ok = wait_or_abort(&sm.q_free[t], (nq[t] - 1) & 1, P, abort_flag, 300);
+          if (!ok) break;
+          ptx::mbar_arrive_expect_tx(&sm.q_full[t], kTileBytes);
+          for (int b = 0; b < HD / 64; ++b)
+            ptx::tma_load_3d(sm.q[t][b], &tmQ, &sm.q_full[t], b * 64, w.h, (w.qt0 + t) * kTile);
+          ++nq[t];
+        }
+        for (int kt = w.kt_lo; kt <= w.kt_hi && ok; ++kt) {
+          const int s = ks % kStages;
+          if (ks >= kStages) ok = wait_or_abort(&sm.kv_empty[s], ((ks / kStages) - 1) & 1, P, abort_flag, 301);
+          if (!ok) break;
+          ptx::mbar_arrive_expect_tx(&sm.kv_full[s], 2 * kTileBytes);
+          for (int b = 0; b < HD / 64; ++b) {
+            ptx::tma_load_3d(sm.k[s][b], &tmK, &sm.kv_full[s], b * 64, g, kt * kTile);
+            ptx::tma_load_3d(sm.v[s][b], &tmV, &sm.kv_full[s], b * 64, g, kt * kTile);
+          }
+          ++ks;
         }
       }
-      // let every issued copy land before the CTA can exit
-      ptx::mbar_wait(&sm.q_full, 0, kDrainLimitNs, P.err, 309);
-      for (int u = (n_issued > kStages ? n_issued - kStages : 0); u < n_issued; ++u)
+      // let every issued copy land before the CTA can exit (each earlier
+      // phase of these barriers completed before the buffer was refilled)
+      for (int t = 0; t < 2; ++t)
+        if (nq[t] > 0) ptx::mbar_wait(&sm.q_full[t], (nq[t] - 1) & 1, kDrainLimitNs, P.err, 309);
+      for (int u = (ks > kStages ? ks - kStages : 0); u < ks; ++u)
         ptx::mbar_wait(&sm.kv_full[u % kStages], (u / kStages) & 1, kDrainLimitNs, P.err, 309);
     }
   } else if (warp == 1) {
@@ -168,14 +207,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t t_s[2] = {tmem, tmem + 128};
       const uint32_t t_o[2] = {tmem + 256, tmem + 256 + HD};
       uint32_t ph_p[2] = {0, 0};
-      bool first_pv[2] = {true, true};
-      auto issue_s = [&](int t, int s) {
+      int nq[2] = {0, 0}, ks = 0;
+      bool first_pv[2], ready[2];
+      auto issue_s = [&](int t, int s) -> bool {
+        if (!ready[t]) {  // this item's Q tile t has landed (first use only)
+          if (!wait_or_abort(&sm.q_full[t], nq[t] & 1, P, abort_flag, 312)) return false;
+          ready[t] = true;
+          ptx::tc_fence_after();
+        }
         for (int kk = 0; kk < HD / 16; ++kk) {
           const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
           ptx::mma_bf16(t_s[t], ptx::smem_desc_sw128(ptx::smem_u32(sm.q[t][0]) + off, 16, 1024),
                         ptx::smem_desc_sw128(ptx::smem_u32(sm.k[s][0]) + off, 16, 1024), idesc_s, kk > 0);
         }
         ptx::mma_commit(&sm.s_full[t]);
+        return true;
       };
       auto issue_pv = [&](int t, int s) -> bool {
         if (!wait_or_abort(&sm.p_full[t], ph_p[t], P, abort_flag, 311)) return false;
@@ -188,34 +234,42 @@ __global__ void __launch_bounds__(kThreads, 1)
         first_pv[t] = false;
         return true;
       };
-      bool ok = wait_or_abort(&sm.q_ready[0], 0, P, abort_flag, 312);
-      if (ok && has1) ok = wait_or_abort(&sm.q_ready[1], 0, P, abort_flag, 312);
-      int pend1 = -1;  // stage whose PV1 is still to be issued
-      int it = 0;
-      for (int kt = kt_lo; kt <= kt_hi && ok; ++kt, ++it) {
-        const int s = it % kStages;
-        ok = wait_or_abort(&sm.kv_full[s], (it / kStages) & 1, P, abort_flag, 313);
-        if (!ok) break;
-        ptx::tc_fence_after();
-        const bool in0 = kt >= lo0 && kt <= hi0, in1 = kt >= lo1 && kt <= hi1;
-        if (in0) issue_s(0, s);
-        if (pend1 >= 0) {
+      bool ok = true;
+      for (int it = it_begin; it < it_end && ok; ++it) {
+        const FwdItem w = load_fwd_item(P, it);
+        first_pv[0] = first_pv[1] = true;
+        ready[0] = false;
+        ready[1] = !w.has1;
+        int pend1 = -1;  // stage whose PV1 is still to be issued
+        int li = 0;      // key-tile step within the item
+        // issue order S0(j), PV1(j-1), S1(j), PV0(j): each softmax group works
+        // while the tensor core runs the other group's products
+        for (int kt = w.kt_lo; kt <= w.kt_hi && ok; ++kt, ++li, ++ks) {
+          const int s = ks % kStages;
+          ok = wait_or_abort(&sm.kv_full[s], (ks / kStages) & 1, P, abort_flag, 313);
+          if (!ok) break;
+          ptx::tc_fence_after();
+          const bool in0 = kt >= w.lo[0] && kt <= w.hi[0], in1 = kt >= w.lo[1] && kt <= w.hi[1];
+          if (in0 && !(ok = issue_s(0, s))) break;
+          if (pend1 >= 0) {
+            if (!(ok = issue_pv(1, pend1))) break;
+            pend1 = -1;
+          }
+          if (li > 0) ptx::mma_commit(&sm.kv_empty[(ks - 1) % kStages]);
+          if (in1 && !(ok = issue_s(1, s))) break;
+          if (in0) {
+            if (!(ok = issue_pv(0, s))) break;
+            if (kt == w.hi[0]) ptx::mma_commit(&sm.o_full[0]);  // O0 complete
+          }
+          if (in1) pend1 = s;
+        }
+        if (ok && pend1 >= 0) {
           ok = issue_pv(1, pend1);
-          if (!ok) break;
-          pend1 = -1;
+          if (ok) ptx::mma_commit(&sm.o_full[1]);
         }
-        if (it > 0) ptx::mma_commit(&sm.kv_empty[(it - 1) % kStages]);
-        if (in1) issue_s(1, s);
-        if (in0) {
-          ok = issue_pv(0, s);
-          if (!ok) break;
-        }
-        if (in1) pend1 = s;
-      }
-      if (ok && pend1 >= 0) ok = issue_pv(1, pend1);
-      if (ok) {
-        ptx::mma_commit(&sm.kv_empty[(it - 1) % kStages]);
-        ptx::mma_commit(&sm.o_full);
+        if (ok) ptx::mma_commit(&sm.kv_empty[(ks - 1) % kStages]);
+        ++nq[0];
+        if (w.has1) ++nq[1];
       }
       // every issued MMA must finish before TMEM is released
       ptx::mma_commit(&sm.drain);
@@ -225,135 +279,133 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ softmax
     const int t = (warp - 4) >> 2;
     const int r = tid & 127;
-    const int lo_t = t ? lo1 : lo0, hi_t = t ? hi1 : hi0;
-    const bool tile_exists = t == 0 || has1;
-    const int i = (qt0 + t) * kTile + r;
-    const bool row_valid = tile_exists && i < P.T;
-    const int lo = row_valid ? __ldg(P.row_lo + i) : 1;
-    const int hi = row_valid ? i : 0;
     const float sl2 = P.scale * kLog2e;
     const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
     const uint32_t t_s = tmem + 128 * t + lane_off, t_o = tmem + 256 + HD * t + lane_off;
-    float m = -INFINITY, l = 0.f, s0 = 0.f;
-    // RoPE fused into the Q tile load: rotate this group's tile in shared
-    // memory (table reads issued before the copy lands)
-    const bool rot = P.layout != 2;
-    RopeUnits<HD, 128> rq;
-    if (tile_exists && rot) rq.begin((qt0 + t) * kTile, P.T, P.pos_id, false, P.rope_hi, P.rope_lo, r);
-    bool ok = tile_exists;
-    if (ok) ok = wait_or_abort(&sm.q_full, 0, P, abort_flag, 321);
-    if (ok && rot) rope_smem_tile<HD, 128>(rq, sm.q[t][0], P.layout, P.rope_hi, P.rope_lo, P.rope_step, r);
-    // every row of the tile is rotated before the MMA or the anchor dot reads it
-    if (t == 0) asm volatile("bar.sync 1, 128;" ::: "memory");
-    else asm volatile("bar.sync 2, 128;" ::: "memory");
-    if (ok) {
-      ptx::fence_proxy_async_smem();
-      ptx::mbar_arrive(&sm.q_ready[t]);
-    }
-    if (ok && P.anchor) {
-      // s_i0 = q~_i . k~_0 with the rotated anchor key from the workspace
-      const uint4* k0 = reinterpret_cast<const uint4*>(P.kr + (size_t)g * HD);
-      float acc = 0.f;
-#pragma unroll 4
-      for (int c8 = 0; c8 < HD / 8; ++c8) {
-        const uint4 kq = __ldg(k0 + c8);
-        const uint4 qq = *reinterpret_cast<const uint4*>(sm.q[t][0] + (c8 >> 3) * 16384 + sw128_chunk(r, c8 & 7));
-        const uint32_t ka[4] = {kq.x, kq.y, kq.z, kq.w}, qa[4] = {qq.x, qq.y, qq.z, qq.w};
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float2 kf = ptx::unpack_bf16x2(ka[e]), qf = ptx::unpack_bf16x2(qa[e]);
-          acc = fmaf(qf.x, kf.x, acc);
-          acc = fmaf(qf.y, kf.y, acc);
-        }
-      }
-      s0 = acc * sl2;
-      m = s0;
-      l = 1.f;
-    }
     uint32_t ph_s = 0;
-    for (int kt = lo_t; kt <= hi_t && ok; ++kt) {
-      ok = wait_or_abort(&sm.s_full[t], ph_s, P, abort_flag, 322);
-      if (!ok) break;
-      ph_s ^= 1;
-      ptx::tc_fence_after();
-      const int j0 = kt * kTile;
-      // tiles every row of the warp sees entirely skip the per-element mask
-      const bool full = __all_sync(0xffffffffu, lo <= j0 && j0 + kTile - 1 <= hi);
-      // the row's logits, read from TMEM once (one wait) and kept in registers
-      // for both passes
-      float sv[128];
+    int nq = 0;
+    bool ok = true;
+    for (int it = it_begin; it < it_end && ok; ++it) {
+      const FwdItem w = load_fwd_item(P, it);
+      if (t == 1 && !w.has1) continue;
+      const int h = w.h, g = h / P.group;
+      const int lo_t = w.lo[t], hi_t = w.hi[t];
+      const int i = (w.qt0 + t) * kTile + r;
+      const bool row_valid = i < P.T;
+      const int lo = row_valid ? __ldg(P.row_lo + i) : 1;
+      const int hi = row_valid ? i : 0;
+      float m = -INFINITY, l = 0.f, s0 = 0.f;
+      if (P.anchor) {
+        ok = __all_sync(0xffffffffu, wait_or_abort(&sm.q_full[t], nq & 1, P, abort_flag, 324));
+        if (!ok) break;
+        // s_i0 = q~_i . k~_0 with the rotated anchor key from the workspace
+        const uint4* k0 = reinterpret_cast<const uint4*>(P.kr + (size_t)g * HD);
+        float acc = 0.f;
+#pragma unroll 4
+        for (int c8 = 0; c8 < HD / 8; ++c8) {
+          const uint4 kq = __ldg(k0 + c8);
+          const uint4 qq = *reinterpret_cast<const uint4*>(sm.q[t][0] + (c8 >> 3) * 16384 + sw128_chunk(r, c8 & 7));
+          const uint32_t ka[4] = {kq.x, kq.y, kq.z, kq.w}, qa[4] = {qq.x, qq.y, qq.z, qq.w};
 #pragma unroll
-      for (int c = 0; c < 4; ++c) ptx::tmem_ld32(t_s + c * 32, sv + c * 32);
-      ptx::tmem_wait_ld();
-      // pass 1: row max of the visible logits (scaled once at the end)
-      float mt = -INFINITY;
-      if (full) {
-#pragma unroll
-        for (int e = 0; e < 128; e += 2) mt = fmaxf(mt, fmaxf(sv[e], sv[e + 1]));
-      } else {
-#pragma unroll
-        for (int e = 0; e < 128; ++e) {
-          const int j = j0 + e;
-          if (j >= lo && j <= hi) mt = fmaxf(mt, sv[e]);
-        }
-      }
-      mt *= sl2;
-      // TMEM access is warp-collective, so a rescale of O is decided per warp
-      const bool need = (mt > m + kRescaleThreshold) || (m == -INFINITY && mt > -INFINITY);
-      if (__any_sync(0xffffffffu, need)) {
-        const float mn = fmaxf(m, mt);
-        const float f = (m == -INFINITY) ? 0.f : exp2f(m - mn);
-        l *= f;
-        if (kt > lo_t) {  // O holds earlier tiles: S(kt) done implies their PV is done
-#pragma unroll 1
-          for (int c = 0; c < HD / 16; ++c) {
-            float ov[16];
-            ptx::tmem_ld16(t_o + c * 16, ov);
-            ptx::tmem_wait_ld();
-#pragma unroll
-            for (int e = 0; e < 16; ++e) ov[e] *= f;
-            ptx::tmem_st16f(t_o + c * 16, ov);
+          for (int e = 0; e < 4; ++e) {
+            const float2 kf = ptx::unpack_bf16x2(ka[e]), qf = ptx::unpack_bf16x2(qa[e]);
+            acc = fmaf(qf.x, kf.x, acc);
+            acc = fmaf(qf.y, kf.y, acc);
           }
         }
-        m = mn;
+        s0 = acc * sl2;
+        m = s0;
+        l = 1.f;
       }
-      // pass 2: P = exp2(s - m) as packed bf16 over the first 64 columns of S
-      float rs = 0.f;
-      const float mm = (m == -INFINITY) ? 0.f : m;
+      for (int kt = lo_t; kt <= hi_t && ok; ++kt) {
+        ok = __all_sync(0xffffffffu, wait_or_abort(&sm.s_full[t], ph_s, P, abort_flag, 322));
+        if (!ok) break;
+        ph_s ^= 1;
+        ptx::tc_fence_after();
+        // the item's last S product for this tile is done and the anchor dot
+        // read Q long before: the producer may refill the Q buffer
+        if (kt == hi_t) ptx::mbar_arrive(&sm.q_free[t]);
+        const int j0 = kt * kTile;
+        // tiles every row of the warp sees entirely skip the per-element mask
+        const bool full = __all_sync(0xffffffffu, lo <= j0 && j0 + kTile - 1 <= hi);
+        // the row's logits, read from TMEM once (one wait) and kept in registers
+        // for both passes
+        float sv[128];
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        const float* sc = sv + c * 32;
-        uint32_t w[16];
+        for (int c = 0; c < 4; ++c) ptx::tmem_ld32(t_s + c * 32, sv + c * 32);
+        ptx::tmem_wait_ld();
+        // pass 1: row max of the visible logits (scaled once at the end)
+        float mt = -INFINITY;
         if (full) {
-          const float2 sl22 = make_float2(sl2, sl2), nm2 = make_float2(-mm, -mm);
-          float2 rs2 = make_float2(0.f, 0.f);
 #pragma unroll
-          for (int e = 0; e < 16; ++e) {
-            const float2 a = __ffma2_rn(make_float2(sc[2 * e], sc[2 * e + 1]), sl22, nm2);
-            const float2 pp = make_float2(ptx::ex2(a.x), ptx::ex2(a.y));
-            rs2 = __fadd2_rn(rs2, pp);
-            w[e] = ptx::pack_bf16x2(pp.x, pp.y);
-          }
-          rs += rs2.x + rs2.y;
+          for (int e = 0; e < 128; e += 2) mt = fmaxf(mt, fmaxf(sv[e], sv[e + 1]));
         } else {
 #pragma unroll
-          for (int e = 0; e < 16; ++e) {
-            const int j = j0 + c * 32 + 2 * e;
-            const float p0 = (j >= lo && j <= hi) ? ptx::ex2(fmaf(sc[2 * e], sl2, -mm)) : 0.f;
-            const float p1 = (j + 1 >= lo && j + 1 <= hi) ? ptx::ex2(fmaf(sc[2 * e + 1], sl2, -mm)) : 0.f;
-            rs += p0 + p1;
-            w[e] = ptx::pack_bf16x2(p0, p1);
+          for (int e = 0; e < 128; ++e) {
+            const int j = j0 + e;
+            if (j >= lo && j <= hi) mt = fmaxf(mt, sv[e]);
           }
         }
-        ptx::tmem_st16(t_s + c * 16, w);
+        mt *= sl2;
+        // TMEM access is warp-collective, so a rescale of O is decided per warp
+        const bool need = (mt > m + kRescaleThreshold) || (m == -INFINITY && mt > -INFINITY);
+        if (__any_sync(0xffffffffu, need)) {
+          const float mn = fmaxf(m, mt);
+          const float f = (m == -INFINITY) ? 0.f : exp2f(m - mn);
+          l *= f;
+          if (kt > lo_t) {  // O holds earlier tiles: S(kt) done implies their PV is done
+#pragma unroll 1
+            for (int c = 0; c < HD / 16; ++c) {
+              float ov[16];
+              ptx::tmem_ld16(t_o + c * 16, ov);
+              ptx::tmem_wait_ld();
+#pragma unroll
+              for (int e = 0; e < 16; ++e) ov[e] *= f;
+              ptx::tmem_st16f(t_o + c * 16, ov);
+            }
+          }
+          m = mn;
+        }
+        // pass 2: P = exp2(s - m) as packed bf16 over the first 64 columns of S
+        float rs = 0.f;
+        const float mm = (m == -INFINITY) ? 0.f : m;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const float* sc = sv + c * 32;
+          uint32_t pw[16];
+          if (full) {
+            const float2 sl22 = make_float2(sl2, sl2), nm2 = make_float2(-mm, -mm);
+            float2 rs2 = make_float2(0.f, 0.f);
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+              const float2 a = __ffma2_rn(make_float2(sc[2 * e], sc[2 * e + 1]), sl22, nm2);
+              const float2 pp = make_float2(ptx::ex2(a.x), ptx::ex2(a.y));
+              rs2 = __fadd2_rn(rs2, pp);
+              pw[e] = ptx::pack_bf16x2(pp.x, pp.y);
+            }
+            rs += rs2.x + rs2.y;
+          } else {
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+              const int j = j0 + c * 32 + 2 * e;
+              const float p0 = (j >= lo && j <= hi) ? ptx::ex2(fmaf(sc[2 * e], sl2, -mm)) : 0.f;
+              const float p1 = (j + 1 >= lo && j + 1 <= hi) ? ptx::ex2(fmaf(sc[2 * e + 1], sl2, -mm)) : 0.f;
+              rs += p0 + p1;
+              pw[e] = ptx::pack_bf16x2(p0, p1);
+            }
+          }
+          ptx::tmem_st16(t_s + c * 16, pw);
+        }
+        l += rs;
+        ptx::tmem_wait_st();
+        ptx::tc_fence_before();
+        ptx::mbar_arrive(&sm.p_full[t]);
       }
-      l += rs;
-      ptx::tmem_wait_st();
-      ptx::tc_fence_before();
-      ptx::mbar_arrive(&sm.p_full[t]);
-    }
-    if (ok) ok = wait_or_abort(&sm.o_full, 0, P, abort_flag, 323);
-    if (ok) {
+      if (ok) ok = __all_sync(0xffffffffu, wait_or_abort(&sm.o_full[t], nq & 1, P, abort_flag, 323));
+      if (!ok) break;
+      // ---- epilogue. Its TMEM reads complete (tmem_wait_ld) before this
+      // thread's next p_full arrival, which the next item's first PV of this
+      // tile (overwriting O) waits for.
       ptx::tc_fence_after();
       const float w0 = P.anchor ? exp2f(s0 - m) : 0.f;
       const float inv_l = 1.f / l;
@@ -364,21 +416,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::tmem_ld32(t_o + c * 32, ov);
         ptx::tmem_wait_ld();
         if (row_valid) {
-          uint32_t w[16];
+          uint32_t ow[16];
 #pragma unroll
           for (int e = 0; e < 16; ++e) {
             float2 v0 = make_float2(0.f, 0.f);
-            if (P.anchor) v0 = ptx::unpack_bf16x2(__ldg(reinterpret_cast<const uint32_t*>(P.v + (size_t)g * HD + c * 32) + e));
+            if (P.anchor)
+              v0 = ptx::unpack_bf16x2(__ldg(reinterpret_cast<const uint32_t*>(P.v + (size_t)g * HD + c * 32) + e));
             const float a = (ov[2 * e] + w0 * v0.x) * inv_l;
             const float b = (ov[2 * e + 1] + w0 * v0.y) * inv_l;
-            w[e] = ptx::pack_bf16x2(a, b);
+            ow[e] = ptx::pack_bf16x2(a, b);
           }
           uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
 #pragma unroll
-          for (int e = 0; e < 4; ++e) dst[e] = make_uint4(w[4 * e], w[4 * e + 1], w[4 * e + 2], w[4 * e + 3]);
+          for (int e = 0; e < 4; ++e) dst[e] = make_uint4(ow[4 * e], ow[4 * e + 1], ow[4 * e + 2], ow[4 * e + 3]);
         }
       }
       if (row_valid) P.lse[(size_t)h * P.T + i] = (m + log2f(l)) * 0.69314718055994531f;
+      ++nq;
     }
   }
 
@@ -387,17 +441,23 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 1) ptx::tmem_dealloc(tmem, kTmemCols);
 }
 
+size_t fwd_k_bytes(const aa_plan_s* p) { return ((size_t)p->T * p->Hkv * p->D * 2 + 255) & ~size_t(255); }
+
 template <int HD>
 aa_status launch_fwd(aa_plan_s* p, const void* q, const void* k, const void* v, void* o, float* lse,
                      void* workspace, cudaStream_t s) {
   CUtensorMap tq, tk, tv;
   aa_status st;
+  const void* qr = q;
   const void* kr = k;
   if (p->cfg.rope_layout != AA_ROPE_NONE) {
-    if ((st = launch_rope(p, k, workspace, p->Hkv, 0, s)) != AA_OK) return st;
+    // workspace: rotated K, then rotated Q
     kr = workspace;
+    qr = static_cast<uint8_t*>(workspace) + fwd_k_bytes(p);
+    if ((st = launch_rope(p, k, workspace, p->Hkv, 0, s)) != AA_OK) return st;
+    if ((st = launch_rope(p, q, const_cast<void*>(qr), p->Hq, 0, s)) != AA_OK) return st;
   }
-  if ((st = make_tile_map(&tq, q, p->T, p->Hq, HD)) != AA_OK) return st;
+  if ((st = make_tile_map(&tq, qr, p->T, p->Hq, HD)) != AA_OK) return st;
   if ((st = make_tile_map(&tk, kr, p->T, p->Hkv, HD)) != AA_OK) return st;
   if ((st = make_tile_map(&tv, v, p->T, p->Hkv, HD)) != AA_OK) return st;
   FwdParams P;
@@ -409,6 +469,7 @@ aa_status launch_fwd(aa_plan_s* p, const void* q, const void* k, const void* v, 
   P.row_lo = p->dev.row_lo;
   P.qtile_klo = p->dev.qtile_klo;
   P.items = p->dev.fwd_items;
+  P.cta_start = p->dev.fwd_cta_start;
   P.rope_hi = p->dev.rope_hi;
   P.rope_lo = p->dev.rope_lo;
   P.rope_step = p->dev.rope_step;
@@ -425,8 +486,10 @@ aa_status launch_fwd(aa_plan_s* p, const void* q, const void* k, const void* v, 
   const size_t smem = sizeof(FwdSmem<HD>);
   cudaError_t e = cudaFuncSetAttribute(attn_fwd_kernel<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return cuda_fail(e, "attn_fwd_kernel smem attribute");
-  const unsigned n_items = (unsigned)p->fwd_items.size();
-  attn_fwd_kernel<HD><<<n_items, kThreads, smem, s>>>(tq, tk, tv, P);
+  // persistent: one CTA per list of the planner's schedule (at most one per SM)
+  if (p->fwd_items.empty()) return AA_OK;
+  const unsigned n_cta = (unsigned)(p->fwd_cta_start.size() - 1);
+  attn_fwd_kernel<HD><<<n_cta, kThreads, smem, s>>>(tq, tk, tv, P);
   e = cudaGetLastError();
   return e == cudaSuccess ? AA_OK : cuda_fail(e, "attn_fwd_kernel launch");
 }
@@ -435,7 +498,7 @@ aa_status launch_fwd(aa_plan_s* p, const void* q, const void* k, const void* v, 
 
 size_t fwd_base_workspace_bytes(const aa_plan_s* p) {
   if (!p || p->cfg.rope_layout == AA_ROPE_NONE) return 0;
-  return ((size_t)p->T * p->Hkv * p->D * 2 + 255) & ~size_t(255);
+  return fwd_k_bytes(p) + (((size_t)p->T * p->Hq * p->D * 2 + 255) & ~size_t(255));
 }
 
 aa_status launch_fwd_with_workspace(aa_plan_s* p, const void* q, const void* k, const void* v, void* o, float* lse,
