@@ -1,9 +1,12 @@
 """Benchmark: fused RoPE + AnchorAttention forward + backward on one GB300.
 
-A step is one aa_fwd + one aa_bwd over one synthetic packing (the 64K
-long-context training shape by default: T = 65536, 32 heads MHA, head_dim
-128, RoPE base 5e6, log-normal document lengths with median 1500). Inputs
-(Q, K, V, dO: 2 GiB) are far larger than L2, so no flush runs between steps.
+A step is one aa_fwd + one aa_bwd_from_fwd over one synthetic packing (the
+64K long-context training shape by default: T = 65536, 32 heads MHA, head_dim
+128, RoPE base 5e6, log-normal document lengths with median 1500): the
+forward rotates Q and K once and the backward reads them from the forward's
+workspace, as a training step that keeps that workspace for the backward
+does (--bwd recompute times aa_bwd, which rotates them again). Inputs (Q, K,
+V, dO: 2 GiB) are far larger than L2, so no flush runs between steps.
 
 Metric: effective TFLOP/s = 14 * D * Hq * P / (t_fwd + t_bwd), where P counts
 the visible (query, key) pairs of the mask, anchor pairs included (4*D flops
@@ -166,15 +169,16 @@ def run_ours(args):
     o = torch.empty_like(q)
     lse = torch.empty(Hq, T, device=dev, dtype=torch.float32)
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
-    ws = plan.alloc_workspace(dev)
     fws = plan.alloc_fwd_workspace(dev)
     stream = torch.cuda.current_stream()
-    # fwd: K rotation + attention; bwd: Q rotation, prep, tile kernel, dq finalize (+ anchor)
-    n_launch_per_step = 2 + 4 + (1 if mask == aa.MASK_ANCHOR else 0)
+    bwd = _bwd_call(plan, args.bwd, q, k, v, o, lse, do, dq, dk, dv, fws, dev)
+    # fwd: K and Q rotation + attention; bwd: (K and Q rotation,) prep, tile
+    # kernel, dq finalize (+ anchor)
+    n_launch_per_step = 3 + 3 + (2 if args.bwd == "recompute" else 0) + (1 if mask == aa.MASK_ANCHOR else 0)
 
     def step():
         plan.fwd(q, k, v, o, lse, fws)
-        plan.bwd(q, k, v, o, lse, do, dq, dk, dv, ws)
+        bwd()
 
     for _ in range(args.warmup):
         step()
@@ -198,7 +202,7 @@ def run_ours(args):
         plan.fwd(q, k, v, o, lse, fws)
         e[1].record(stream)
         plan.set_bwd_timing_events(e[2], e[3])
-        plan.bwd(q, k, v, o, lse, do, dq, dk, dv, ws)
+        bwd()
         e[4].record(stream)
     t_stop.record(stream)
     _barrier(world)
@@ -243,6 +247,7 @@ def run_ours(args):
                    "head_dim": D, "rope_base": w.rope_base, "mask": args.mask, "pos": args.pos,
                    "documents": int(len(cu) - 1), "unmasked_pairs_per_head": P,
                    "l2": "inputs (2 GiB) larger than L2; no flush", "parallelism": f"replicas x{world}"},
+        "bwd_entry": "aa_bwd_from_fwd" if args.bwd == "from_fwd" else "aa_bwd",
         "fwd_ms": round(fwd_ms, 4), "bwd_ms": round(bwd_ms, 4), "bwd_main_kernel_ms": round(bwd_main_ms, 4),
         "fwd_tflops": round(flops_fwd / (fwd_ms * 1e-3) / 1e12, 2),
         "bwd_tflops": round(flops_bwd / (bwd_ms * 1e-3) / 1e12, 2),
@@ -270,6 +275,17 @@ def run_ours(args):
         torch.distributed.destroy_process_group()
 
 
+def _bwd_call(plan, kind, q, k, v, o, lse, do, dq, dk, dv, fws, dev):
+    """The step's backward call with its workspace: aa_bwd_from_fwd reading the
+    rotated Q and K from the forward workspace `fws`, or aa_bwd (recompute)."""
+    import torch
+    if kind == "from_fwd":
+        ws = torch.empty(max(plan.bwd_from_fwd_workspace_bytes(), 256), device=dev, dtype=torch.uint8)
+        return lambda: plan.bwd_from_fwd(fws, v, o, lse, do, dq, dk, dv, ws)
+    ws = plan.alloc_workspace(dev)
+    return lambda: plan.bwd(q, k, v, o, lse, do, dq, dk, dv, ws)
+
+
 def _causal_speedup(aa, w, q, k, v, do, dev, ms_anchor, args):
     import torch
     T, Hq, Hkv, D = w.total_tokens, w.num_q_heads, w.num_kv_heads, w.head_dim
@@ -277,23 +293,23 @@ def _causal_speedup(aa, w, q, k, v, do, dev, ms_anchor, args):
         o = torch.empty_like(q)
         lse = torch.empty(Hq, T, device=dev, dtype=torch.float32)
         dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
-        ws = pc.alloc_workspace(dev)
         fws = pc.alloc_fwd_workspace(dev)
+        bwd = _bwd_call(pc, args.bwd, q, k, v, o, lse, do, dq, dk, dv, fws, dev)
         for _ in range(1):
             pc.fwd(q, k, v, o, lse, fws)
-            pc.bwd(q, k, v, o, lse, do, dq, dk, dv, ws)
+            bwd()
         torch.cuda.synchronize()
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         n = 2
         a.record()
         for _ in range(n):
             pc.fwd(q, k, v, o, lse, fws)
-            pc.bwd(q, k, v, o, lse, do, dq, dk, dv, ws)
+            bwd()
         b.record()
         torch.cuda.synchronize()
         pc.check_device_error()
         ms_causal = a.elapsed_time(b) / n
-        del ws
+        del bwd
     return {"causal_ms_per_step": round(ms_causal, 3), "speedup": round(ms_causal / ms_anchor, 3)}
 
 
@@ -310,8 +326,8 @@ def _e2e(aa, plan, w, dev, args, flops, world):
     o = torch.empty_like(q)
     lse = torch.empty(Hq, T, device=dev, dtype=torch.float32)
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
-    ws = plan.alloc_workspace(dev)
     fws = plan.alloc_fwd_workspace(dev)
+    bwd = _bwd_call(plan, args.bwd, q, k, v, o, lse, do, dq, dk, dv, fws, dev)
     h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hdo))
     d2h = sum(t.numel() * t.element_size() for t in (out_o, out_l, out_dq, out_dk, out_dv))
 
@@ -319,7 +335,7 @@ def _e2e(aa, plan, w, dev, args, flops, world):
         for d_, h_ in ((q, hq), (k, hk), (v, hv), (do, hdo)):
             d_.copy_(h_, non_blocking=True)
         plan.fwd(q, k, v, o, lse, fws)
-        plan.bwd(q, k, v, o, lse, do, dq, dk, dv, ws)
+        bwd()
         for h_, d_ in ((out_o, o), (out_l, lse), (out_dq, dq), (out_dk, dk), (out_dv, dv)):
             h_.copy_(d_, non_blocking=True)
 
@@ -409,6 +425,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--compare-causal", action=argparse.BooleanOptionalAction, default=True)
     ap.add_argument("--cpu-budget", type=float, default=15.0)
+    ap.add_argument("--bwd", choices=["from_fwd", "recompute"], default="from_fwd",
+                    help="backward entry point: aa_bwd_from_fwd (default) or aa_bwd")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         print("warning: fewer than 3 warm-up steps", file=sys.stderr)

@@ -180,7 +180,8 @@ aa_status aa_fwd(aa_plan_t plan, const void* q, const void* k, const void* v, vo
                  float* lse, void* workspace, size_t workspace_bytes, aa_stream_t stream);
 
 /* Bytes of device scratch aa_fwd needs (the rotated K and Q, T*(Hkv+Hq)*D
- * bf16; 0 with AA_ROPE_NONE; segment plans add their grouped copies). */
+ * bf16, which it leaves there for aa_bwd_from_fwd; 0 with AA_ROPE_NONE;
+ * segment plans add their grouped copies). */
 size_t aa_fwd_workspace_bytes(aa_plan_t plan);
 
 /* Bytes of device scratch aa_bwd needs (rotated Q and K, fp32 dQ
@@ -199,6 +200,31 @@ size_t aa_bwd_workspace_bytes(aa_plan_t plan);
 aa_status aa_bwd(aa_plan_t plan, const void* q, const void* k, const void* v, const void* o,
                  const float* lse, const void* dout, void* dq, void* dk, void* dv,
                  void* workspace, size_t workspace_bytes, aa_stream_t stream);
+
+/* aa_bwd from the forward's rotated operands (no counterpart in the paper:
+ * an interface addition of this library) [ARCH §3.4 Anchor, §3.4 RoPE].
+ * aa_fwd leaves the rotated Q and K (R_i q_i, R_j k_j, rounded to bf16) in
+ * its workspace; a training step that keeps that workspace until the
+ * backward pass, instead of q and k, passes it here as fwd_workspace and the
+ * backward skips its own rotation of Q and K (two passes over them).
+ *  - fwd_workspace: the workspace of an aa_fwd call with this plan and the
+ *    q, k whose gradients are wanted, unchanged since that call (the library
+ *    cannot check this; it is the caller's contract). Read only.
+ *  - v, o, lse, dout, dq, dk, dv: as for aa_bwd; the results are the same
+ *    (gradients with respect to the UN-ROTATED q, k and v): dk, dv bit for
+ *    bit, dq up to the order of its fp32 atomic additions.
+ *  - workspace: at least aa_bwd_from_fwd_workspace_bytes(plan) bytes,
+ *    256-byte aligned, contents ignored (smaller than aa_bwd's: no rotated
+ *    copies).
+ *  - AA_ERR_UNSUPPORTED with AA_ROPE_NONE (aa_fwd rotates nothing; call
+ *    aa_bwd); AA_ERR_INVALID_ARG for NULL or misaligned pointers or a short
+ *    workspace, with nothing launched. */
+aa_status aa_bwd_from_fwd(aa_plan_t plan, const void* fwd_workspace, const void* v, const void* o,
+                          const float* lse, const void* dout, void* dq, void* dk, void* dv,
+                          void* workspace, size_t workspace_bytes, aa_stream_t stream);
+
+/* Bytes of device scratch aa_bwd_from_fwd needs. */
+size_t aa_bwd_from_fwd_workspace_bytes(aa_plan_t plan);
 
 /* aa_bwd without a caller-provided workspace (no counterpart in the paper:
  * an interface addition of this library).

@@ -22,7 +22,8 @@ STATUS = {0: "AA_OK", 1: "AA_ERR_INVALID_ARG", 2: "AA_ERR_UNSUPPORTED", 3: "AA_E
 
 # every symbol include/anchorattn.h declares
 EXPORTS = ["aa_plan", "aa_plan_with_theta", "aa_plan_segments", "aa_plan_destroy", "aa_plan_metadata", "aa_plan_stats", "aa_plan_work",
-           "aa_rope_apply", "aa_fwd", "aa_fwd_workspace_bytes", "aa_bwd_workspace_bytes", "aa_bwd", "aa_bwd_static_workspace", "aa_check_device_error",
+           "aa_rope_apply", "aa_fwd", "aa_fwd_workspace_bytes", "aa_bwd_workspace_bytes", "aa_bwd", "aa_bwd_from_fwd",
+           "aa_bwd_from_fwd_workspace_bytes", "aa_bwd_static_workspace", "aa_check_device_error",
            "aa_set_wait_limit", "aa_set_bwd_timing_events", "aa_selftest_bounded_wait", "aa_status_string",
            "aa_last_error", "aa_shift_diag_workspace_bytes", "aa_shift_diag"]
 
@@ -68,6 +69,8 @@ def lib():
             "aa_fwd_workspace_bytes": ([vp], ctypes.c_size_t),
             "aa_bwd_workspace_bytes": ([vp], ctypes.c_size_t),
             "aa_bwd": ([vp] + [vp] * 9 + [vp, ctypes.c_size_t, vp], ctypes.c_int),
+            "aa_bwd_from_fwd": ([vp] + [vp] * 8 + [vp, ctypes.c_size_t, vp], ctypes.c_int),
+            "aa_bwd_from_fwd_workspace_bytes": ([vp], ctypes.c_size_t),
             "aa_bwd_static_workspace": ([vp] + [vp] * 9 + [vp], ctypes.c_int),
             "aa_check_device_error": ([vp, vp], ctypes.c_int),
             "aa_set_wait_limit": ([vp, ctypes.c_uint64], ctypes.c_int),
@@ -241,6 +244,26 @@ class Plan:
         _check(lib().aa_bwd(self._h, _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout),
                             _ptr(dq), _ptr(dk), _ptr(dv), _ptr(ws), ctypes.c_size_t(ws.numel()),
                             _stream(stream)))
+        return dq, dk, dv
+
+    def bwd_from_fwd_workspace_bytes(self):
+        return int(lib().aa_bwd_from_fwd_workspace_bytes(self._h))
+
+    def bwd_from_fwd(self, fwd_workspace, v, o, lse, dout, dq=None, dk=None, dv=None, workspace=None,
+                     stream=None):
+        """aa_bwd_from_fwd: the backward pass reading the rotated Q and K that
+        aa_fwd left in ``fwd_workspace`` (the tensor passed to fwd(); q and k
+        are not needed). Same results as bwd()."""
+        import torch
+        dq = torch.empty_like(o) if dq is None else dq
+        dk = torch.empty_like(v) if dk is None else dk
+        dv = torch.empty_like(v) if dv is None else dv
+        if workspace is None:
+            workspace = torch.empty(max(self.bwd_from_fwd_workspace_bytes(), 256), device=v.device,
+                                    dtype=torch.uint8)
+        _check(lib().aa_bwd_from_fwd(self._h, _ptr(fwd_workspace), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout),
+                                     _ptr(dq), _ptr(dk), _ptr(dv), _ptr(workspace),
+                                     ctypes.c_size_t(workspace.numel()), _stream(stream)))
         return dq, dk, dv
 
     def shift_diag(self, other, q, k, workspace=None, stream=None):

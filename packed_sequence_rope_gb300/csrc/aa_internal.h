@@ -82,17 +82,26 @@ aa_status launch_rope(const aa_plan_s* p, const void* x, void* y, int H, int inv
 aa_status launch_fwd_with_workspace(aa_plan_s* p, const void* q, const void* k, const void* v, void* o, float* lse,
                                     void* workspace, cudaStream_t s);
 size_t fwd_base_workspace_bytes(const aa_plan_s* p);
-size_t bwd_base_workspace_bytes(const aa_plan_s* p);
+// Where a forward workspace keeps the rotated Q and K (kernel token order);
+// only meaningful when the plan rotates (rope_layout != AA_ROPE_NONE).
+void fwd_rotated_operands(const aa_plan_s* p, const void* fwd_workspace, const void** qr, const void** kr);
+// with_rot = false: the caller supplies the rotated Q and K (aa_bwd_from_fwd)
+size_t bwd_base_workspace_bytes(const aa_plan_s* p, bool with_rot = true);
 // Segment plans: extra workspace behind the base one, and the gather / run /
 // scatter wrappers (segments.cu).
 size_t seg_fwd_extra_bytes(const aa_plan_s* p);
-size_t seg_bwd_extra_bytes(const aa_plan_s* p);
+size_t seg_bwd_extra_bytes(const aa_plan_s* p, bool with_qk = true);
 aa_status seg_fwd(aa_plan_s* p, const void* q, const void* k, const void* v, void* o, float* lse, void* workspace,
                   cudaStream_t s);
+// qr / kr (both or neither): rotated Q and K already in the kernels' token
+// order, replacing q and k (which may then be NULL).
 aa_status seg_bwd(aa_plan_s* p, const void* q, const void* k, const void* v, const void* o, const float* lse,
-                  const void* dout, void* dq, void* dk, void* dv, void* workspace, cudaStream_t s);
-// Launch the backward kernels with an already-validated workspace pointer.
+                  const void* dout, void* dq, void* dk, void* dv, void* workspace, cudaStream_t s,
+                  const void* qr = nullptr, const void* kr = nullptr);
+// Launch the backward kernels with an already-validated workspace pointer;
+// qr / kr as for seg_bwd.
 aa_status launch_bwd_with_workspace(aa_plan_s* p, const void* q, const void* k, const void* v, const void* o,
                                     const float* lse, const void* dout, void* dq, void* dk, void* dv,
-                                    void* workspace, cudaStream_t s);
+                                    void* workspace, cudaStream_t s, const void* qr = nullptr,
+                                    const void* kr = nullptr);
 }  // namespace aa

@@ -43,14 +43,17 @@ struct Workspace {
 
 inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
-Workspace carve(void* base, const aa_plan_s* p, size_t* total) {
+// with_rot = false: the rotated Q and K come from the caller (a forward
+// workspace), so the workspace holds no copies of them
+Workspace carve(void* base, const aa_plan_s* p, size_t* total, bool with_rot = true) {
   Workspace w;
   size_t off = 0;
   uint8_t* b = static_cast<uint8_t*>(base);
+  const bool rot = with_rot && p->cfg.rope_layout != AA_ROPE_NONE;
   w.qr = reinterpret_cast<__nv_bfloat16*>(b + off);
-  if (p->cfg.rope_layout != AA_ROPE_NONE) off = align256(off + (size_t)p->T * p->Hq * p->D * 2);
+  if (rot) off = align256(off + (size_t)p->T * p->Hq * p->D * 2);
   w.kr = reinterpret_cast<__nv_bfloat16*>(b + off);
-  if (p->cfg.rope_layout != AA_ROPE_NONE) off = align256(off + (size_t)p->T * p->Hkv * p->D * 2);
+  if (rot) off = align256(off + (size_t)p->T * p->Hkv * p->D * 2);
   w.dq_acc = reinterpret_cast<float*>(b + off);
   off = align256(off + (size_t)p->T * p->Hq * p->D * 4);
   w.dsum = reinterpret_cast<float*>(b + off);
@@ -829,16 +832,18 @@ __global__ void anchor_finalize_kernel(Workspace ws, __nv_bfloat16* __restrict__
 
 template <int HD>
 aa_status launch_bwd(aa_plan_s* p, const void* q, const void* k, const void* v, const void* o, const float* lse,
-                     const void* dout, void* dq, void* dk, void* dv, void* workspace, cudaStream_t s) {
+                     const void* dout, void* dq, void* dk, void* dv, void* workspace, cudaStream_t s,
+                     const void* qr_in, const void* kr_in) {
   size_t need = 0;
-  Workspace ws = carve(workspace, p, &need);
+  const bool given = qr_in != nullptr;  // rotated Q and K from a forward workspace
+  Workspace ws = carve(workspace, p, &need, !given);
   cudaError_t e;
   const int rope_layout = p->cfg.rope_layout;
   // Q is the streaming operand of the key-stationary tile loop: rotate it
-  // once here rather than on every visit
-  const void* qr = q;
-  const void* kr = k;
-  if (rope_layout != AA_ROPE_NONE) {
+  // once here rather than on every visit (or take the forward's rotation)
+  const void* qr = given ? qr_in : q;
+  const void* kr = given ? kr_in : k;
+  if (rope_layout != AA_ROPE_NONE && !given) {
     aa_status rs = launch_rope(p, q, ws.qr, p->Hq, 0, s);
     if (rs == AA_OK) rs = launch_rope(p, k, ws.kr, p->Hkv, 0, s);
     if (rs != AA_OK) return rs;
@@ -918,15 +923,15 @@ aa_status launch_bwd(aa_plan_s* p, const void* q, const void* k, const void* v, 
 
 aa_status launch_bwd_with_workspace(aa_plan_s* p, const void* q, const void* k, const void* v, const void* o,
                                     const float* lse, const void* dout, void* dq, void* dk, void* dv,
-                                    void* workspace, cudaStream_t s) {
-  return p->D == 128 ? launch_bwd<128>(p, q, k, v, o, lse, dout, dq, dk, dv, workspace, s)
-                     : launch_bwd<64>(p, q, k, v, o, lse, dout, dq, dk, dv, workspace, s);
+                                    void* workspace, cudaStream_t s, const void* qr, const void* kr) {
+  return p->D == 128 ? launch_bwd<128>(p, q, k, v, o, lse, dout, dq, dk, dv, workspace, s, qr, kr)
+                     : launch_bwd<64>(p, q, k, v, o, lse, dout, dq, dk, dv, workspace, s, qr, kr);
 }
 
-size_t bwd_base_workspace_bytes(const aa_plan_s* p) {
+size_t bwd_base_workspace_bytes(const aa_plan_s* p, bool with_rot) {
   if (!p) return 0;
   size_t total = 0;
-  carve(nullptr, p, &total);
+  carve(nullptr, p, &total, with_rot);
   return total;
 }
 
@@ -956,4 +961,34 @@ extern "C" aa_status aa_bwd(aa_plan_t p, const void* q, const void* k, const voi
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (p->segmented) return seg_bwd(p, q, k, v, o, lse, dout, dq, dk, dv, workspace, s);
   return launch_bwd_with_workspace(p, q, k, v, o, lse, dout, dq, dk, dv, workspace, s);
+}
+
+extern "C" size_t aa_bwd_from_fwd_workspace_bytes(aa_plan_t p) {
+  if (!p) return 0;
+  return bwd_base_workspace_bytes(p, false) + (p->segmented ? seg_bwd_extra_bytes(p, false) : 0);
+}
+
+extern "C" aa_status aa_bwd_from_fwd(aa_plan_t p, const void* fwd_workspace, const void* v, const void* o,
+                                     const float* lse, const void* dout, void* dq, void* dk, void* dv,
+                                     void* workspace, size_t workspace_bytes, aa_stream_t stream) {
+  aa_status st = check_compute_plan(p);
+  if (st != AA_OK) return st;
+  if (p->cfg.rope_layout == AA_ROPE_NONE)
+    return fail(AA_ERR_UNSUPPORTED, "with AA_ROPE_NONE aa_fwd keeps no rotated operands: call aa_bwd");
+  const void* ptrs[] = {v, o, lse, dout, dq, dk, dv};
+  for (const void* x : ptrs) {
+    if (!x) return fail(AA_ERR_INVALID_ARG, "NULL tensor pointer");
+    if (!aligned16(x)) return fail(AA_ERR_INVALID_ARG, "tensors must be 16-byte aligned");
+  }
+  if (!fwd_workspace || (reinterpret_cast<uintptr_t>(fwd_workspace) & 255u))
+    return fail(AA_ERR_INVALID_ARG, "fwd_workspace must be the 256-byte aligned workspace of an aa_fwd call");
+  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+    return fail(AA_ERR_INVALID_ARG, "workspace must be a 256-byte aligned device pointer");
+  if (workspace_bytes < aa_bwd_from_fwd_workspace_bytes(p))
+    return fail(AA_ERR_INVALID_ARG, "workspace is smaller than aa_bwd_from_fwd_workspace_bytes()");
+  const void *qr = nullptr, *kr = nullptr;
+  fwd_rotated_operands(p, fwd_workspace, &qr, &kr);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (p->segmented) return seg_bwd(p, nullptr, nullptr, v, o, lse, dout, dq, dk, dv, workspace, s, qr, kr);
+  return launch_bwd_with_workspace(p, nullptr, nullptr, v, o, lse, dout, dq, dk, dv, workspace, s, qr, kr);
 }

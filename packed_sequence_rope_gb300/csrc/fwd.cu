@@ -451,9 +451,7 @@ aa_status launch_fwd(aa_plan_s* p, const void* q, const void* k, const void* v, 
   const void* qr = q;
   const void* kr = k;
   if (p->cfg.rope_layout != AA_ROPE_NONE) {
-    // workspace: rotated K, then rotated Q
-    kr = workspace;
-    qr = static_cast<uint8_t*>(workspace) + fwd_k_bytes(p);
+    fwd_rotated_operands(p, workspace, &qr, &kr);  // they stay there for aa_bwd_from_fwd
     if ((st = launch_rope(p, k, workspace, p->Hkv, 0, s)) != AA_OK) return st;
     if ((st = launch_rope(p, q, const_cast<void*>(qr), p->Hq, 0, s)) != AA_OK) return st;
   }
@@ -495,6 +493,11 @@ aa_status launch_fwd(aa_plan_s* p, const void* q, const void* k, const void* v, 
 }
 
 }  // namespace
+
+void fwd_rotated_operands(const aa_plan_s* p, const void* fwd_workspace, const void** qr, const void** kr) {
+  *kr = fwd_workspace;
+  *qr = static_cast<const uint8_t*>(fwd_workspace) + fwd_k_bytes(p);
+}
 
 size_t fwd_base_workspace_bytes(const aa_plan_s* p) {
   if (!p || p->cfg.rope_layout == AA_ROPE_NONE) return 0;

@@ -76,9 +76,11 @@ size_t seg_fwd_extra_bytes(const aa_plan_s* p) {
   return 2 * tensor_bytes(p, p->Hq) + 2 * tensor_bytes(p, p->Hkv) + lse_bytes(p);
 }
 
-// Backward extras: grouped Q, K, V, O, dO, LSE and dQ, dK, dV.
-size_t seg_bwd_extra_bytes(const aa_plan_s* p) {
-  return 4 * tensor_bytes(p, p->Hq) + 4 * tensor_bytes(p, p->Hkv) + lse_bytes(p);
+// Backward extras: grouped Q, K (unless the rotated ones are given), V, O,
+// dO, LSE and dQ, dK, dV.
+size_t seg_bwd_extra_bytes(const aa_plan_s* p, bool with_qk) {
+  const int n = with_qk ? 4 : 3;
+  return n * tensor_bytes(p, p->Hq) + n * tensor_bytes(p, p->Hkv) + lse_bytes(p);
 }
 
 aa_status seg_fwd(aa_plan_s* p, const void* q, const void* k, const void* v, void* o, float* lse, void* workspace,
@@ -100,24 +102,31 @@ aa_status seg_fwd(aa_plan_s* p, const void* q, const void* k, const void* v, voi
 }
 
 aa_status seg_bwd(aa_plan_s* p, const void* q, const void* k, const void* v, const void* o, const float* lse,
-                  const void* dout, void* dq, void* dk, void* dv, void* workspace, cudaStream_t s) {
-  uint8_t* w = static_cast<uint8_t*>(workspace) + bwd_base_workspace_bytes(p);
+                  const void* dout, void* dq, void* dk, void* dv, void* workspace, cudaStream_t s, const void* qr,
+                  const void* kr) {
+  // qr / kr: the forward's rotated Q and K, already in the grouped order
+  const bool given = qr != nullptr;
+  uint8_t* w = static_cast<uint8_t*>(workspace) + bwd_base_workspace_bytes(p, !given);
   const size_t tq = tensor_bytes(p, p->Hq), tk = tensor_bytes(p, p->Hkv);
-  void* qg = w;
-  void* og = w + tq;
-  void* dog = w + 2 * tq;
-  void* dqg = w + 3 * tq;
-  void* kg = w + 4 * tq;
-  void* vg = w + 4 * tq + tk;
-  void* dkg = w + 4 * tq + 2 * tk;
-  void* dvg = w + 4 * tq + 3 * tk;
-  float* lg = reinterpret_cast<float*>(w + 4 * tq + 4 * tk);
+  void* og = w;
+  void* dog = w + tq;
+  void* dqg = w + 2 * tq;
+  void* vg = w + 3 * tq;
+  void* dkg = w + 3 * tq + tk;
+  void* dvg = w + 3 * tq + 2 * tk;
+  float* lg = reinterpret_cast<float*>(w + 3 * tq + 3 * tk);
+  void* qg = w + 3 * tq + 3 * tk + lse_bytes(p);  // only without qr / kr
+  void* kg = static_cast<uint8_t*>(qg) + tq;
   aa_status st;
-  if ((st = permute_rows(p, q, qg, p->Hq, 0, s)) != AA_OK || (st = permute_rows(p, k, kg, p->Hkv, 0, s)) != AA_OK ||
-      (st = permute_rows(p, v, vg, p->Hkv, 0, s)) != AA_OK || (st = permute_rows(p, o, og, p->Hq, 0, s)) != AA_OK ||
+  if (!given &&
+      ((st = permute_rows(p, q, qg, p->Hq, 0, s)) != AA_OK || (st = permute_rows(p, k, kg, p->Hkv, 0, s)) != AA_OK))
+    return st;
+  if ((st = permute_rows(p, v, vg, p->Hkv, 0, s)) != AA_OK || (st = permute_rows(p, o, og, p->Hq, 0, s)) != AA_OK ||
       (st = permute_rows(p, dout, dog, p->Hq, 0, s)) != AA_OK || (st = permute_cols(p, lse, lg, 0, s)) != AA_OK)
     return st;
-  if ((st = launch_bwd_with_workspace(p, qg, kg, vg, og, lg, dog, dqg, dkg, dvg, workspace, s)) != AA_OK) return st;
+  st = given ? launch_bwd_with_workspace(p, nullptr, nullptr, vg, og, lg, dog, dqg, dkg, dvg, workspace, s, qr, kr)
+             : launch_bwd_with_workspace(p, qg, kg, vg, og, lg, dog, dqg, dkg, dvg, workspace, s);
+  if (st != AA_OK) return st;
   if ((st = permute_rows(p, dqg, dq, p->Hq, 1, s)) != AA_OK || (st = permute_rows(p, dkg, dk, p->Hkv, 1, s)) != AA_OK)
     return st;
   return permute_rows(p, dvg, dv, p->Hkv, 1, s);
