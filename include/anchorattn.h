@@ -98,7 +98,8 @@ typedef struct aa_plan_s* aa_plan_t;
  * §3.4 Index]: per-token document and position IDs, each query row's visible
  * key interval, the live 128x128 tile lists (fully cross-document tiles are
  * dropped; the anchor column is folded in separately), longest-first work
- * order, and the two-level fp32 cos/sin tables of Eq. 6 built in fp64.
+ * order dealt out to one list per SM (the attention kernels are persistent),
+ * and the two-level fp32 cos/sin tables of Eq. 6 built in fp64.
  * cu_doclens: host int32[num_docs + 1] (see conventions). Device metadata is
  * uploaded with copies ordered on `stream`. On success *out owns everything;
  * release it with aa_plan_destroy. */

@@ -45,9 +45,9 @@ __device__ __forceinline__ uint32_t sw128_chunk(int r, int c8) {
 // the two-level tables; the other rows advance each pair's angle by one
 // theta_p with an exact complex product by (cos theta_p, sin theta_p). Over at
 // most 15 steps the drift stays near 1e-6 of the pair's magnitude, far below
-// the bf16 rounding of the result. Every kernel that rotates a tile (and
-// aa_rope_apply) runs this same unit decomposition and arithmetic, so fused
-// and standalone rotation agree bit for bit.
+// the bf16 rounding of the result. Any kernel that rotates a tile runs this
+// same unit decomposition and arithmetic, so all rotations of a tile agree bit
+// for bit.
 //
 // Usage: RopeUnits<HD, NT> st; st.begin(...) loads the positions and the
 // group-start (cos, sin) values (issue it before waiting for the tile's data
@@ -189,54 +189,6 @@ __device__ __forceinline__ QuadRaw quad_pack(int layout, const float* x, const f
                      ptx::pack_bf16x2(y[2], y[3]));
   return q;
 }
-
-// Tile accessor over a [128][HD] bf16 tile in shared memory (HD/64 swizzled
-// 16 KB blocks). layout 0: pair p = elements (2p, 2p+1); layout 1: (p, p+HD/2).
-// The layout is a template parameter of the unpack/pack pair through `L`.
-template <int HD, int L>
-struct SmemTile {
-  using Raw = QuadRaw;
-  uint8_t* base;
-  __device__ __forceinline__ static uint32_t elem_off(int r, int e) {
-    return (uint32_t)((e >> 6) * 16384) + sw128_chunk(r, (e & 63) >> 3) + (uint32_t)((e & 7) * 2);
-  }
-  __device__ __forceinline__ QuadRaw load_raw(int r, int qd) const {
-    QuadRaw q;
-    if (L == 0) {
-      q.w = *reinterpret_cast<const uint4*>(base + (qd >> 3) * 16384 + sw128_chunk(r, qd & 7));
-    } else {
-      const uint2 a = *reinterpret_cast<const uint2*>(base + elem_off(r, 4 * qd));
-      const uint2 b = *reinterpret_cast<const uint2*>(base + elem_off(r, HD / 2 + 4 * qd));
-      q.w = make_uint4(a.x, a.y, b.x, b.y);
-    }
-    return q;
-  }
-  __device__ __forceinline__ void store_raw(int r, int qd, const QuadRaw& q) const {
-    if (L == 0) {
-      *reinterpret_cast<uint4*>(base + (qd >> 3) * 16384 + sw128_chunk(r, qd & 7)) = q.w;
-    } else {
-      *reinterpret_cast<uint2*>(base + elem_off(r, 4 * qd)) = make_uint2(q.w.x, q.w.y);
-      *reinterpret_cast<uint2*>(base + elem_off(r, HD / 2 + 4 * qd)) = make_uint2(q.w.z, q.w.w);
-    }
-  }
-  __device__ __forceinline__ static void unpack(const QuadRaw& q, float* x, float* y) { quad_unpack(L, q, x, y); }
-  __device__ __forceinline__ static QuadRaw pack(const float* x, const float* y) { return quad_pack(L, x, y); }
-};
-
-// Rotate a [128][HD] shared-memory tile with the layout chosen at run time.
-template <int HD, int NT>
-__device__ __forceinline__ void rope_smem_tile(const RopeUnits<HD, NT>& st, uint8_t* base, int layout,
-                                               const float2* hi_tab, const float2* lo_tab,
-                                               const float2* step_tab, int t) {
-  if (layout == 0) {
-    SmemTile<HD, 0> tile{base};
-    st.run(tile, false, hi_tab, lo_tab, step_tab, t);
-  } else if (layout == 1) {
-    SmemTile<HD, 1> tile{base};
-    st.run(tile, false, hi_tab, lo_tab, step_tab, t);
-  }
-}
-
 
 // Host: tensor map over x [T, H, D] bf16 with a {64, 1, 128} box and the
 // 128-byte swizzle (one 16 KB tile block per load).

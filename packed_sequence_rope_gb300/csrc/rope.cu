@@ -3,9 +3,10 @@
 // fp32 rotation then a cast to bf16 as in §3.2 "Big-Picture Architecture")
 // and the host-side TMA descriptor helper.
 //
-// HBM-bound: one read and one write of x, one CTA per (128-row tile, head),
-// with the same per-tile arithmetic as the rotation fused into the attention
-// kernels' tile loads (so the two agree bit for bit).
+// HBM-bound: one read and one write of x, one CTA per (128-row tile, head).
+// The attention entry points run the same kernel once per call on Q and K,
+// so aa_rope_apply and the operands the attention kernels read agree bit for
+// bit.
 #include <cudaTypedefs.h>
 
 #include <mutex>
