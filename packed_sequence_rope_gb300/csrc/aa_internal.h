@@ -28,8 +28,7 @@ struct DevicePlan {
   int32_t* key_hi = nullptr;   // [T] last query row that sees key j in the tile path
   WorkItem* fwd_items = nullptr;  // in the persistent schedule's order (CTA-major)
   int32_t* fwd_cta_start = nullptr;  // [fwd CTAs + 1] first item of each CTA's list
-  WorkItem* bwd_items = nullptr;  // in the persistent schedule's order (CTA-major)
-  int32_t* bwd_cta_start = nullptr;  // [bwd CTAs + 1] first item of each CTA's list
+  WorkItem* bwd_items = nullptr;  // in work-list order (claimed by the CTAs in that order)
   int32_t* qtile_klo = nullptr;  // [n_tiles] first live key tile of each query tile
   float2* rope_hi = nullptr;   // [n_hi][D/2]  cos/sin((32*h) * theta_p)
   float2* rope_lo = nullptr;   // [D/2][32]    cos/sin(l * theta_p), p-major
@@ -55,7 +54,7 @@ struct aa_plan_s {
   bool segmented = false;
   std::vector<int32_t> perm, seg_doc, seg_pos;  // seg_*: the caller's order
   std::vector<aa::WorkItem> fwd_items, bwd_items;  // fwd: one item per (query-tile pair, head)
-  std::vector<int32_t> fwd_cta_start, bwd_cta_start;  // persistent kernels: CTA c runs items[start[c], start[c+1])
+  std::vector<int32_t> fwd_cta_start;  // persistent forward: CTA c runs fwd_items[start[c], start[c+1])
   std::vector<int32_t> qtile_klo;
   std::vector<double> theta;    // [D/2] rotation frequency of each pair (Eq. 6's theta_p)
   std::vector<float2> rope_hi, rope_lo, rope_step;

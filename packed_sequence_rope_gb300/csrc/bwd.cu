@@ -15,9 +15,9 @@
 //      fp32 dQ accumulator is initialised with scale*dS_i0*k~_0 (so it needs
 //      no separate clearing pass) and per-chunk partial sums of dv_0, dk~_0
 //      are written.
-//   2. attn_bwd: persistent, one CTA per SM walking a list of (key tile, kv
-//      head) items; per item K~/V stay in shared memory while it loops over
-//      the group's query heads and the live query tiles. Five tcgen05 MMAs per tile (S^T, dP^T, dV, dK, dQ) with fp32
+//   2. attn_bwd: persistent, one CTA per SM claiming (key tile, kv head)
+//      items in work-list order; per item K~/V stay in shared memory while it
+//      loops over the group's query heads and the live query tiles. Five tcgen05 MMAs per tile (S^T, dP^T, dV, dK, dQ) with fp32
 //      TMEM accumulators; dQ~ is added into the fp32 accumulator (TMA bulk
 //      reductions for D = 128, vector atomics for D = 64); dK/dV are rotated
 //      back and written once.
@@ -39,6 +39,7 @@ struct Workspace {
   float* dsum;     // [Hq, T] fp32 (D_i)
   float* part_dv;  // [kPrepChunks, Hq, D]
   float* part_dk;  // [kPrepChunks, Hq, D]
+  int32_t* next_item;  // the attention kernel's work counter (reset by bwd_prep)
 };
 
 inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -62,6 +63,8 @@ Workspace carve(void* base, const aa_plan_s* p, size_t* total, bool with_rot = t
   off = align256(off + (size_t)kPrepChunks * p->Hq * p->D * 4);
   w.part_dk = reinterpret_cast<float*>(b + off);
   off = align256(off + (size_t)kPrepChunks * p->Hq * p->D * 4);
+  w.next_item = reinterpret_cast<int32_t*>(b + off);
+  off = align256(off + sizeof(int32_t));
   if (total) *total = off;
   return w;
 }
@@ -87,6 +90,8 @@ __global__ void __launch_bounds__(kPrepThreads) bwd_prep_kernel(const __nv_bfloa
   // [Hq, D] token rows rather than one head's rows at a stride
   const int h = blockIdx.x, g = h / group;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // the attention kernel, next in stream order, claims its items from here
+  if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) *ws.next_item = 0;
   const int sub = lane / LPR, c0 = (lane % LPR) * 8;
   const int rows_per_chunk = (T + kPrepChunks - 1) / kPrepChunks;
   const int r_begin = blockIdx.y * rows_per_chunk;
@@ -212,12 +217,16 @@ __global__ void __launch_bounds__(kPrepThreads) bwd_prep_kernel(const __nv_bfloa
 }
 
 // ---------------------------------------------------------------- 2. main
-// Persistent: one CTA per SM, each walking its own list of (key tile, kv
-// head) items (the planner's schedule). An item keeps K~/V stationary in
+// Persistent: one CTA per SM. The CTAs claim (key tile, kv head) items from a
+// global counter in work-list order, so the items in flight at any moment are
+// neighbours in the planner's (document, head) grouping and share their Q~/dO
+// tiles and dQ accumulator rows in L2. An item keeps K~/V stationary in
 // shared memory and loops over the group's query heads and live query tiles.
 // 512 threads:
-//   warp 0      TMA producer: an item's K, V once it may overwrite them; Q_i,
-//               dO_i through a 2-stage ring that runs on across items
+//   warp 0      claims the next item (published to the other roles through
+//               a 2-slot ring in shared memory) and is the TMA producer: an
+//               item's K, V once it may overwrite them; Q_i, dO_i through a
+//               2-stage ring that runs on across items
 //   warp 1      TMEM owner and MMA issuer (one thread)
 //   warps 2-3   staging of each query tile's -LSE*log2(e) and -D rows into
 //               shared memory (Q and K arrive rotated from the workspace: a
@@ -253,6 +262,8 @@ struct BwdSmem {
   float lse2[2][128];                   // -LSE * log2(e) of each stage's query rows
   float dsum[2][128];                   // -D of each stage's query rows
   uint64_t kv_full, kv_free;
+  uint64_t item_full[2], item_empty[2];
+  int item_slot[2];  // claimed work-list index (-1: none left)
   uint64_t qd_full[2], q_ready[2], qd_empty[2];
   uint64_t st_full, p_full, dq_full, dq_free, o_full, drain;
   uint32_t tmem_base;
@@ -266,8 +277,9 @@ struct BwdParams {
   Workspace ws;
   const int32_t* pos_id;
   const int32_t* key_hi;
-  const WorkItem* items;      // all CTAs' lists, CTA-major
-  const int32_t* cta_start;   // CTA c runs items[cta_start[c], cta_start[c + 1])
+  const WorkItem* items;      // the work list, in the planner's order
+  int32_t* next_item;         // next unclaimed index (zeroed by bwd_prep)
+  int n_items;
   const float2* rope_hi;
   const float2* rope_lo;
   const float2* rope_step;
@@ -307,9 +319,33 @@ __device__ __forceinline__ bool bwd_wait(uint64_t* bar, uint32_t parity, const B
   }
 }
 
+// The li-th item this CTA runs (its work-list index, or -1 when the list is
+// exhausted or the CTA aborted), as the producer published it in slot li & 1.
+// warp_read: the whole (converged) warp reads it and lane 0 frees the slot;
+// otherwise the calling thread alone. Slot readers: the MMA thread and the
+// 14 warps of the P/dS, staging and drain roles.
+constexpr int kItemReaders = 15;
+
+template <class Smem>
+__device__ __forceinline__ int read_item(Smem& sm, int li, const BwdParams& P, volatile int* abort_flag,
+                                         bool warp_read, int site) {
+  const int slot = li & 1;
+  bool ok = bwd_wait(&sm.item_full[slot], (li >> 1) & 1, P, abort_flag, site);
+  if (warp_read) ok = __all_sync(0xffffffffu, ok);
+  if (!ok) return -1;
+  const int it = *reinterpret_cast<volatile int*>(&sm.item_slot[slot]);
+  if (warp_read) {
+    __syncwarp();
+    if ((threadIdx.x & 31) == 0) ptx::mbar_arrive(&sm.item_empty[slot]);
+  } else {
+    ptx::mbar_arrive(&sm.item_empty[slot]);
+  }
+  return it;
+}
+
 // Barrier phases: per-step barriers count the CTA's steps across all its
-// items (gs); per-item barriers (kv_full, kv_free, o_full) count its items
-// (li). Every wait is bounded; a timeout records the site in the error word
+// items (gs); per-item barriers (item_full, item_empty, kv_full, kv_free,
+// o_full) count its items (li). Every wait is bounded; a timeout records the site in the error word
 // and stops every role of the CTA. Waits followed by warp-collective steps
 // are made warp-uniform by a vote (the drain group by a barrier reduction).
 template <int HD>
@@ -328,7 +364,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   constexpr int kTmemCols = 512;
   constexpr uint32_t kTileBytes = 128 * HD * 2;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int it_begin = __ldg(P.cta_start + blockIdx.x), it_end = __ldg(P.cta_start + blockIdx.x + 1);
   volatile int* abort_flag = &sm.abort_flag;
 
   if (tid == 0) {
@@ -338,6 +373,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     ptx::tma_prefetch_desc(&tmDO);
     ptx::mbar_init(&sm.kv_full, 1);
     ptx::mbar_init(&sm.kv_free, 1);
+    for (int s = 0; s < 2; ++s) {
+      ptx::mbar_init(&sm.item_full[s], 1);
+      ptx::mbar_init(&sm.item_empty[s], kItemReaders);
+    }
     for (int s = 0; s < 2; ++s) {
       ptx::mbar_init(&sm.qd_full[s], 1);
       ptx::mbar_init(&sm.q_ready[s], 64);
@@ -364,8 +403,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     if (lane == 0) {
       int gs = 0, n_issued = 0, li_loaded = -1;
       bool ok = true;
-      for (int it = it_begin; it < it_end && ok; ++it) {
-        const int li = it - it_begin;
+      for (int li = 0; ok; ++li) {
+        // claim the next work-list item once every role has read slot li & 1
+        const int slot = li & 1;
+        if (li >= 2) ok = bwd_wait(&sm.item_empty[slot], ((li >> 1) - 1) & 1, P, abort_flag, 402);
+        if (!ok) break;
+        int it = atomicAdd(P.next_item, 1);
+        if (it >= P.n_items) it = -1;
+        sm.item_slot[slot] = it;
+        ptx::mbar_arrive(&sm.item_full[slot]);  // release: the slot is written
+        if (it < 0) break;
         const BwdItem w = load_item(P, it);
         // the previous item's last MMA has read K~/V
         if (li > 0) ok = bwd_wait(&sm.kv_free, (li - 1) & 1, P, abort_flag, 400);
@@ -406,8 +453,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const uint32_t sds = ptx::smem_u32(sm.dst[0]);
       int gs = 0;
       bool ok = true;
-      for (int it = it_begin; it < it_end && ok; ++it) {
-        const int li = it - it_begin;
+      for (int li = 0; ok; ++li) {
+        const int it = read_item(sm, li, P, abort_flag, false, 410);
+        if (it < 0) break;
         const int n_steps = load_item(P, it).n_steps;
         ok = bwd_wait(&sm.kv_full, li & 1, P, abort_flag, 411);
         for (int step = 0; step < n_steps && ok; ++step, ++gs) {
@@ -479,8 +527,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
     int gs = 0;
     bool ok = true;
-    for (int it = it_begin; it < it_end && ok; ++it) {
-      const int li = it - it_begin;
+    for (int li = 0; ok; ++li) {
+      const int it = read_item(sm, li, P, abort_flag, true, 424);
+      if (it < 0) break;
       const BwdItem w = load_item(P, it);
       const int j = w.kt * kTile + r;
       const bool key_valid = j < P.T;
@@ -631,7 +680,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
     int gs = 0;
     bool ok = true;
-    for (int it = it_begin; it < it_end && ok; ++it) {
+    for (int li = 0; ok; ++li) {
+      int it = read_item(sm, li, P, abort_flag, true, 430);
+      if (!ptx::bar_and(3, 128, it >= 0)) break;  // the drain group moves on (or stops) as one
       const BwdItem w = load_item(P, it);
       for (int step = 0; step < w.n_steps && ok; ++step, ++gs) {
         const int h = w.head(step, P.group), i0 = w.qtile(step) * kTile;
@@ -699,7 +750,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const int t = tid - 64;
     int gs = 0;
     bool ok = true;
-    for (int it = it_begin; it < it_end && ok; ++it) {
+    for (int li = 0; ok; ++li) {
+      const int it = read_item(sm, li, P, abort_flag, true, 440);
+      if (it < 0) break;
       const BwdItem w = load_item(P, it);
       for (int step = 0; step < w.n_steps && ok; ++step, ++gs) {
         const int s = gs & 1;
@@ -872,7 +925,8 @@ aa_status launch_bwd(aa_plan_s* p, const void* q, const void* k, const void* v, 
   P.pos_id = p->dev.pos_id;
   P.key_hi = p->dev.key_hi;
   P.items = p->dev.bwd_items;
-  P.cta_start = p->dev.bwd_cta_start;
+  P.next_item = ws.next_item;
+  P.n_items = (int)p->bwd_items.size();
   P.rope_hi = p->dev.rope_hi;
   P.rope_lo = p->dev.rope_lo;
   P.rope_step = p->dev.rope_step;
@@ -889,8 +943,8 @@ aa_status launch_bwd(aa_plan_s* p, const void* q, const void* k, const void* v, 
   if (e != cudaSuccess) return cuda_fail(e, "attn_bwd_kernel smem attribute");
   if (p->bwd_ev_start && (e = cudaEventRecord(p->bwd_ev_start, s)) != cudaSuccess)
     return cuda_fail(e, "recording the bwd start event");
-  // persistent: one CTA per list of the planner's schedule (at most one per SM)
-  const unsigned n_cta = (unsigned)(p->bwd_cta_start.size() - 1);
+  // persistent: one CTA per SM (fewer for short work lists)
+  const unsigned n_cta = (unsigned)std::min<size_t>(p->bwd_items.size(), (size_t)std::max(p->num_sms, 1));
   if (!p->bwd_items.empty()) {
     attn_bwd_kernel<HD><<<n_cta, kBwdThreads, smem, s>>>(tq, tk, tv, tdo, tdq, P);
     if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(e, "attn_bwd_kernel launch");

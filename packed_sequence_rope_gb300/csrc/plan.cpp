@@ -170,14 +170,15 @@ static void build_stats_and_work(aa_plan_s* p) {
   for (auto& w : p->bwd_items) p->bwd_tiles += (int64_t)(w.hi - w.lo + 1) * p->group;
 }
 
-// Persistent schedules: the attention kernels run one CTA per SM, each walking
-// its own list of items. Items are dealt out in work-list order, each to the
-// CTA with the least estimated work so far (list scheduling; cost = the
-// item's tile steps plus `overhead` for its loads and epilogue, which mostly
-// overlap the neighbouring items), so the CTAs busy at any moment hold
-// neighbouring items of the list (the backward's (document, head) grouping
-// keeps its L2 reuse) and all CTAs finish close together. Ties go to the
-// lower CTA index. `items` is rewritten CTA-major; start[c] is CTA c's first.
+// Persistent forward schedule: the forward kernel runs one CTA per SM, each
+// walking its own list of items. Items are dealt out in work-list order, each
+// to the CTA with the least estimated work so far (list scheduling; cost =
+// the item's tile steps plus an allowance for its loads and epilogue, which
+// mostly overlap the neighbouring items), so all CTAs finish close together.
+// Ties go to the lower CTA index. `items` is rewritten CTA-major; start[c] is
+// CTA c's first. (The backward kernel claims its items from a device counter
+// in work-list order instead: its L2 reuse needs the CTAs to stay together
+// in the list, which a static deal does not keep.)
 template <class Cost>
 static void build_schedule(std::vector<WorkItem>& items, std::vector<int32_t>& start, int num_sms, Cost cost) {
   const int n = (int)items.size();
@@ -203,11 +204,8 @@ static void build_schedule(std::vector<WorkItem>& items, std::vector<int32_t>& s
 }
 
 static void build_schedules(aa_plan_s* p) {
-  // backward: one step per (query head of the group, query tile)
-  build_schedule(p->bwd_items, p->bwd_cta_start, p->num_sms,
-                 [&](const WorkItem& w) { return 1 + (int64_t)(w.hi - w.lo + 1) * p->group; });
-  // forward: one step per key tile of the pair's range (both query tiles
-  // share it), plus the second tile's Q rotation and epilogue
+  // one step per key tile of the pair's range (both query tiles share it),
+  // plus two for the loads and epilogues
   build_schedule(p->fwd_items, p->fwd_cta_start, p->num_sms,
                  [&](const WorkItem& w) { return 2 + (int64_t)(w.hi - w.lo + 1); });
 }
@@ -259,8 +257,8 @@ static aa_status upload(T** dst, const std::vector<T>& src, cudaStream_t s, cons
 
 static void free_device(aa_plan_s* p) {
   DevicePlan& d = p->dev;
-  void* ptrs[] = {d.pos_id,    d.row_lo,  d.key_hi,    d.fwd_items, d.bwd_items, d.fwd_cta_start, d.bwd_cta_start,
-                  d.qtile_klo, d.rope_hi, d.rope_lo, d.rope_step, d.err,       d.perm,          d.pos_orig};
+  void* ptrs[] = {d.pos_id,    d.row_lo,  d.key_hi,    d.fwd_items, d.bwd_items, d.fwd_cta_start,
+                  d.qtile_klo, d.rope_hi, d.rope_lo, d.rope_step, d.err,       d.perm,     d.pos_orig};
   for (void* q : ptrs)
     if (q) cudaFree(q);
   d = DevicePlan{};
@@ -403,7 +401,6 @@ static aa_status make_plan(const aa_config* cfg, const int32_t* cu_doclens_host,
       (st = upload(&d.key_hi, p->key_hi, s, "key_hi")) != AA_OK ||
       (st = upload(&d.fwd_items, p->fwd_items, s, "fwd work list")) != AA_OK ||
       (st = upload(&d.bwd_items, p->bwd_items, s, "bwd work list")) != AA_OK ||
-      (st = upload(&d.bwd_cta_start, p->bwd_cta_start, s, "bwd schedule")) != AA_OK ||
       (st = upload(&d.fwd_cta_start, p->fwd_cta_start, s, "fwd schedule")) != AA_OK ||
       (st = upload(&d.qtile_klo, p->qtile_klo, s, "query-tile key ranges")) != AA_OK ||
       (st = upload(&d.rope_hi, p->rope_hi, s, "rope table (hi)")) != AA_OK ||
