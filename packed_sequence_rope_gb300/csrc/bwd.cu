@@ -850,36 +850,58 @@ __global__ void __launch_bounds__(256) dq_finalize_kernel(const float* __restric
 }
 
 // ---------------------------------------------------------------- 4. anchor
-__global__ void anchor_finalize_kernel(Workspace ws, __nv_bfloat16* __restrict__ dk, __nv_bfloat16* __restrict__ dv,
-                                       const int32_t* __restrict__ pos_id, const float2* __restrict__ hi_tab,
-                                       const float2* __restrict__ lo_tab, int Hq, int Hkv, int D, int layout) {
+// One block per kv head. The 256 row chunks are split into runs of
+// consecutive chunks, each summed by its own thread (many loads in flight
+// instead of one long dependent walk), and the runs are combined in run
+// order, so the sums are run-to-run deterministic.
+constexpr int kAnchorThreads = 512;
+
+__global__ void __launch_bounds__(kAnchorThreads)
+    anchor_finalize_kernel(Workspace ws, __nv_bfloat16* __restrict__ dk, __nv_bfloat16* __restrict__ dv,
+                           const int32_t* __restrict__ pos_id, const float2* __restrict__ hi_tab,
+                           const float2* __restrict__ lo_tab, int Hq, int Hkv, int D, int layout) {
   const int g = blockIdx.x, group = Hq / Hkv;
-  extern __shared__ float sh[];  // [2][D]
-  for (int c = threadIdx.x; c < D; c += blockDim.x) {
-    float sdv = 0.f, sdk = 0.f;
-    for (int hh = 0; hh < group; ++hh) {
-      const int h = g * group + hh;
-      for (int b = 0; b < kPrepChunks; ++b) {
-        sdv += ws.part_dv[((size_t)b * Hq + h) * D + c];
-        sdk += ws.part_dk[((size_t)b * Hq + h) * D + c];
-      }
+  const int runs = kAnchorThreads / D;  // 4 at D = 128, 8 at D = 64
+  const int per = kPrepChunks / runs;
+  const int c = threadIdx.x % D, run = threadIdx.x / D;
+  extern __shared__ float sh[];  // [2][runs][D] run sums, then [2][D] totals (dv, dk)
+  float sdv = 0.f, sdk = 0.f;
+  const size_t stride = (size_t)Hq * D;
+  for (int hh = 0; hh < group; ++hh) {
+    const float* pv = ws.part_dv + (size_t)(g * group + hh) * D + c;
+    const float* pk = ws.part_dk + (size_t)(g * group + hh) * D + c;
+#pragma unroll 8
+    for (int b = run * per; b < (run + 1) * per; ++b) {
+      sdv += pv[b * stride];
+      sdk += pk[b * stride];
     }
-    sh[c] = sdv;
-    sh[D + c] = sdk;
+  }
+  sh[run * D + c] = sdv;
+  sh[(runs + run) * D + c] = sdk;
+  __syncthreads();
+  float* tot = sh + 2 * runs * D;
+  if (threadIdx.x < D) {
+    float a = 0.f, b = 0.f;
+    for (int q = 0; q < runs; ++q) {
+      a += sh[q * D + c];
+      b += sh[(runs + q) * D + c];
+    }
+    tot[c] = a;
+    tot[D + c] = b;
   }
   __syncthreads();
   const int pos = __ldg(pos_id);
   for (int p = threadIdx.x; p < D / 2; p += blockDim.x) {
     const int ia = layout == 1 ? p : 2 * p, ib = layout == 1 ? p + D / 2 : 2 * p + 1;
-    float a = sh[D + ia], b = sh[D + ib];
+    float a = tot[D + ia], b = tot[D + ib];
     if (layout != 2) {
       const float2 cs = rope_cs(hi_tab, lo_tab, pos, p, D / 2);
       rope_pair(a, b, cs.x, -cs.y);
     }
     dk[(size_t)g * D + ia] = __float2bfloat16_rn(a);
     dk[(size_t)g * D + ib] = __float2bfloat16_rn(b);
-    dv[(size_t)g * D + ia] = __float2bfloat16_rn(sh[ia]);
-    dv[(size_t)g * D + ib] = __float2bfloat16_rn(sh[ib]);
+    dv[(size_t)g * D + ia] = __float2bfloat16_rn(tot[ia]);
+    dv[(size_t)g * D + ib] = __float2bfloat16_rn(tot[ib]);
   }
 }
 
@@ -965,7 +987,7 @@ aa_status launch_bwd(aa_plan_s* p, const void* q, const void* k, const void* v, 
                                                           p->Hq, rope_layout);
   if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(e, "dq_finalize_kernel launch");
   if (p->anchor) {
-    anchor_finalize_kernel<<<p->Hkv, 128, 2 * HD * sizeof(float), s>>>(
+    anchor_finalize_kernel<<<p->Hkv, kAnchorThreads, (2 * kAnchorThreads + 2 * HD) * sizeof(float), s>>>(
         ws, static_cast<__nv_bfloat16*>(dk), static_cast<__nv_bfloat16*>(dv), p->dev.pos_id, p->dev.rope_hi,
         p->dev.rope_lo, p->Hq, p->Hkv, HD, rope_layout);
     if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(e, "anchor_finalize_kernel launch");

@@ -100,7 +100,33 @@ def test_compute_on_host_only_plan_is_refused(aa):
         L = aa.lib()
         assert L.aa_fwd(p._h, None, None, None, None, None, None, 0, None) == 1
         assert "host_only" in L.aa_last_error().decode()
+        assert L.aa_bwd_from_fwd(p._h, *([None] * 8), None, 0, None) == 1
+        assert "host_only" in L.aa_last_error().decode()
         assert L.aa_check_device_error(p._h, None) == 1
+
+
+@pytest.mark.parametrize("layout", [orc.ROPE_ADJACENT, orc.ROPE_NONE])
+@pytest.mark.parametrize("segmented", [False, True])
+def test_workspace_sizes(aa, layout, segmented):
+    # Forward: rotated K then rotated Q (bf16), nothing without RoPE; the
+    # backward from the forward's rotated operands needs no copies of them,
+    # and segment plans add grouped copies of their tensors.
+    T, Hq, Hkv, D = 1000, 4, 2, 128
+    al = lambda n: (n + 255) // 256 * 256
+    doc = np.repeat(np.arange(1, 5, dtype=np.int32), [250, 250, 250, 249]) if segmented else None
+    doc = None if doc is None else np.concatenate([[0], doc]).astype(np.int32)
+    cu = None if segmented else [1, 300, 700, T]
+    with aa.Plan(cu, T, Hq, Hkv, D, 1e4, rope_layout=layout, host_only=True, doc_of_token=doc) as p:
+        L = aa.lib()
+        fwd, bwd, from_fwd = (int(L.aa_fwd_workspace_bytes(p._h)), int(L.aa_bwd_workspace_bytes(p._h)),
+                              int(L.aa_bwd_from_fwd_workspace_bytes(p._h)))
+    rot = al(T * Hkv * D * 2) + al(T * Hq * D * 2) if layout != orc.ROPE_NONE else 0
+    seg_fwd = 2 * al(T * Hq * D * 2) + 2 * al(T * Hkv * D * 2) + al(Hq * T * 4) if segmented else 0
+    assert fwd == rot + seg_fwd
+    # the two backward entry points differ by the rotated copies (and, for
+    # segment plans, by the grouped copies of q and k)
+    seg_qk = al(T * Hq * D * 2) + al(T * Hkv * D * 2) if segmented else 0
+    assert bwd - from_fwd == rot + seg_qk
 
 
 def test_status_strings(aa):
