@@ -26,14 +26,14 @@ struct DevicePlan {
   int32_t* pos_id = nullptr;   // [T] rotation index (shift included)
   int32_t* row_lo = nullptr;   // [T] first key of row i's tile-path interval [row_lo, i]
   int32_t* key_hi = nullptr;   // [T] last query row that sees key j in the tile path
-  WorkItem* fwd_items = nullptr;  // in the persistent schedule's order (CTA-major)
-  int32_t* fwd_cta_start = nullptr;  // [fwd CTAs + 1] first item of each CTA's list
+  WorkItem* fwd_items = nullptr;  // longest first (claimed by the CTAs in that order)
   WorkItem* bwd_items = nullptr;  // in work-list order (claimed by the CTAs in that order)
   int32_t* qtile_klo = nullptr;  // [n_tiles] first live key tile of each query tile
   float2* rope_hi = nullptr;   // [n_hi][D/2]  cos/sin((32*h) * theta_p)
   float2* rope_lo = nullptr;   // [D/2][32]    cos/sin(l * theta_p), p-major
   float2* rope_step = nullptr; // [D/2]        cos/sin(theta_p)
   int32_t* err = nullptr;      // device error word (0 = ok)
+  int32_t* fwd_next = nullptr; // the forward kernel's work counter (reset before each launch)
   int32_t* perm = nullptr;     // segment plans: [T] caller token of each grouped position
   int32_t* pos_orig = nullptr; // segment plans: [T] rotation index in the caller's token order
 };
@@ -54,7 +54,6 @@ struct aa_plan_s {
   bool segmented = false;
   std::vector<int32_t> perm, seg_doc, seg_pos;  // seg_*: the caller's order
   std::vector<aa::WorkItem> fwd_items, bwd_items;  // fwd: one item per (query-tile pair, head)
-  std::vector<int32_t> fwd_cta_start;  // persistent forward: CTA c runs fwd_items[start[c], start[c+1])
   std::vector<int32_t> qtile_klo;
   std::vector<double> theta;    // [D/2] rotation frequency of each pair (Eq. 6's theta_p)
   std::vector<float2> rope_hi, rope_lo, rope_step;

@@ -12,12 +12,13 @@
 // the workspace: every query tile of a document re-reads K, and a Q tile
 // rotated inside the attention kernel would put the rotation between one
 // item's last products and the next item's first. The attention kernel is
-// persistent: one CTA per SM walks its list of (pair of 128-row query tiles,
-// head) items, 384 threads:
-//   warp 0      TMA producer: each item's rotated Q0/Q1 as soon as the
-//               previous item's last S product of that tile has run, and the
-//               rotated K / V tiles through a 2-stage ring that runs on
-//               across items
+// persistent: one CTA per SM; the CTAs claim (pair of 128-row query tiles,
+// head) items longest first from a counter, 384 threads:
+//   warp 0      claims the next item (published to the other roles through a
+//               2-slot shared-memory ring) and is the TMA producer: each
+//               item's rotated Q0/Q1 as soon as the previous item's last S
+//               product of that tile has run, and the rotated K / V tiles
+//               through a 2-stage ring that runs on across items
 //   warp 1      TMEM owner and MMA issuer (one thread)
 //   warps 4-7   query tile 0: online softmax (thread = query row = TMEM lane)
 //               and epilogue
@@ -51,6 +52,8 @@ struct FwdSmem {
   alignas(1024) uint8_t k[kStages][kB][16384];
   alignas(1024) uint8_t v[kStages][kB][16384];
   uint64_t q_full[2], q_free[2];
+  uint64_t item_full[2], item_empty[2];
+  int item_slot[2];  // claimed work-list index (-1: none left)
   uint64_t kv_full[kStages], kv_empty[kStages];
   uint64_t s_full[2], p_full[2], o_full[2], drain;
   uint32_t tmem_base;
@@ -65,8 +68,9 @@ struct FwdParams {
   const int32_t* pos_id;
   const int32_t* row_lo;
   const int32_t* qtile_klo;
-  const WorkItem* items;     // all CTAs' lists, CTA-major
-  const int32_t* cta_start;  // CTA c runs items[cta_start[c], cta_start[c + 1])
+  const WorkItem* items;     // the work list, longest first
+  int32_t* next_item;        // next unclaimed index (zeroed before the launch)
+  int n_items;
   const float2* rope_hi;
   const float2* rope_lo;
   const float2* rope_step;
@@ -115,8 +119,32 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, co
   }
 }
 
-// Barrier phases: the K/V ring counts the CTA's key-tile steps across its
-// items; s_full / p_full count each query tile's softmax steps; q_full,
+// The li-th item this CTA runs (its work-list index, or -1 when the list is
+// exhausted or the CTA aborted), as the producer published it in slot li & 1.
+// warp_read: the whole (converged) warp reads it and lane 0 frees the slot;
+// otherwise the calling thread alone. Slot readers: the MMA thread and the 8
+// softmax warps.
+constexpr int kFwdItemReaders = 9;
+
+template <class Smem>
+__device__ __forceinline__ int read_fwd_item(Smem& sm, int li, const FwdParams& P, volatile int* abort_flag,
+                                             bool warp_read, int site) {
+  const int slot = li & 1;
+  bool ok = wait_or_abort(&sm.item_full[slot], (li >> 1) & 1, P, abort_flag, site);
+  if (warp_read) ok = __all_sync(0xffffffffu, ok);
+  if (!ok) return -1;
+  const int it = *reinterpret_cast<volatile int*>(&sm.item_slot[slot]);
+  if (warp_read) {
+    __syncwarp();
+    if ((threadIdx.x & 31) == 0) ptx::mbar_arrive(&sm.item_empty[slot]);
+  } else {
+    ptx::mbar_arrive(&sm.item_empty[slot]);
+  }
+  return it;
+}
+
+// Barrier phases: the item ring counts the CTA's items; the K/V ring counts
+// the CTA's key-tile steps across its items; s_full / p_full count each query tile's softmax steps; q_full,
 // q_free and o_full count the items in which the query tile exists.
 // The roles synchronise through mbarriers only (every wait bounded), so an
 // abort in one role never strands another at a named barrier; inside a warp
@@ -135,7 +163,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr uint32_t kTileBytes = 128 * HD * 2;
   constexpr int kTmemCols = 512;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int it_begin = __ldg(P.cta_start + blockIdx.x), it_end = __ldg(P.cta_start + blockIdx.x + 1);
   volatile int* abort_flag = &sm.abort_flag;
 
   if (tid == 0) {
@@ -153,6 +180,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::mbar_init(&sm.kv_full[s], 1);
       ptx::mbar_init(&sm.kv_empty[s], 1);
     }
+    for (int s = 0; s < 2; ++s) {
+      ptx::mbar_init(&sm.item_full[s], 1);
+      ptx::mbar_init(&sm.item_empty[s], kFwdItemReaders);
+    }
     ptx::mbar_init(&sm.drain, 1);
     sm.abort_flag = 0;
     ptx::fence_mbar_init();
@@ -168,7 +199,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       int nq[2] = {0, 0}, ks = 0;
       bool ok = true;
-      for (int it = it_begin; it < it_end && ok; ++it) {
+      for (int li = 0; ok; ++li) {
+        // claim the next work-list item once every reader has taken slot li & 1
+        const int slot = li & 1;
+        if (li >= 2) ok = wait_or_abort(&sm.item_empty[slot], ((li >> 1) - 1) & 1, P, abort_flag, 302);
+        if (!ok) break;
+        int it = atomicAdd(P.next_item, 1);
+        if (it >= P.n_items) it = -1;
+        sm.item_slot[slot] = it;
+        ptx::mbar_arrive(&sm.item_full[slot]);  // release: the slot is written
+        if (it < 0) break;
         const FwdItem w = load_fwd_item(P, it);
         const int g = w.h / P.group;
         for (int t = 0; t < (w.has1 ? 2 : 1) && ok; ++t) {
@@ -235,16 +275,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         return true;
       };
       bool ok = true;
-      for (int it = it_begin; it < it_end && ok; ++it) {
+      for (int li = 0; ok; ++li) {
+        const int it = read_fwd_item(sm, li, P, abort_flag, false, 310);
+        if (it < 0) break;
         const FwdItem w = load_fwd_item(P, it);
         first_pv[0] = first_pv[1] = true;
         ready[0] = false;
         ready[1] = !w.has1;
         int pend1 = -1;  // stage whose PV1 is still to be issued
-        int li = 0;      // key-tile step within the item
+        int kstep = 0;   // key-tile step within the item
         // issue order S0(j), PV1(j-1), S1(j), PV0(j): each softmax group works
         // while the tensor core runs the other group's products
-        for (int kt = w.kt_lo; kt <= w.kt_hi && ok; ++kt, ++li, ++ks) {
+        for (int kt = w.kt_lo; kt <= w.kt_hi && ok; ++kt, ++kstep, ++ks) {
           const int s = ks % kStages;
           ok = wait_or_abort(&sm.kv_full[s], (ks / kStages) & 1, P, abort_flag, 313);
           if (!ok) break;
@@ -255,7 +297,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!(ok = issue_pv(1, pend1))) break;
             pend1 = -1;
           }
-          if (li > 0) ptx::mma_commit(&sm.kv_empty[(ks - 1) % kStages]);
+          if (kstep > 0) ptx::mma_commit(&sm.kv_empty[(ks - 1) % kStages]);
           if (in1 && !(ok = issue_s(1, s))) break;
           if (in0) {
             if (!(ok = issue_pv(0, s))) break;
@@ -285,7 +327,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t ph_s = 0;
     int nq = 0;
     bool ok = true;
-    for (int it = it_begin; it < it_end && ok; ++it) {
+    for (int li = 0; ok; ++li) {
+      const int it = read_fwd_item(sm, li, P, abort_flag, true, 320);
+      if (it < 0) break;
       const FwdItem w = load_fwd_item(P, it);
       if (t == 1 && !w.has1) continue;
       const int h = w.h, g = h / P.group;
@@ -467,7 +511,8 @@ aa_status launch_fwd(aa_plan_s* p, const void* q, const void* k, const void* v, 
   P.row_lo = p->dev.row_lo;
   P.qtile_klo = p->dev.qtile_klo;
   P.items = p->dev.fwd_items;
-  P.cta_start = p->dev.fwd_cta_start;
+  P.next_item = p->dev.fwd_next;
+  P.n_items = (int)p->fwd_items.size();
   P.rope_hi = p->dev.rope_hi;
   P.rope_lo = p->dev.rope_lo;
   P.rope_step = p->dev.rope_step;
@@ -484,9 +529,12 @@ aa_status launch_fwd(aa_plan_s* p, const void* q, const void* k, const void* v, 
   const size_t smem = sizeof(FwdSmem<HD>);
   cudaError_t e = cudaFuncSetAttribute(attn_fwd_kernel<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return cuda_fail(e, "attn_fwd_kernel smem attribute");
-  // persistent: one CTA per list of the planner's schedule (at most one per SM)
+  // persistent: one CTA per SM (fewer for short work lists), claiming the
+  // items longest first from the plan's counter
   if (p->fwd_items.empty()) return AA_OK;
-  const unsigned n_cta = (unsigned)(p->fwd_cta_start.size() - 1);
+  if ((e = cudaMemsetAsync(p->dev.fwd_next, 0, sizeof(int32_t), s)) != cudaSuccess)
+    return cuda_fail(e, "resetting the forward work counter");
+  const unsigned n_cta = (unsigned)std::min<size_t>(p->fwd_items.size(), (size_t)std::max(p->num_sms, 1));
   attn_fwd_kernel<HD><<<n_cta, kThreads, smem, s>>>(tq, tk, tv, P);
   e = cudaGetLastError();
   return e == cudaSuccess ? AA_OK : cuda_fail(e, "attn_fwd_kernel launch");

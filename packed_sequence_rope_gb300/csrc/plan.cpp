@@ -13,7 +13,6 @@
 #include <algorithm>
 #include <map>
 #include <new>
-#include <queue>
 #include <string>
 
 #include "aa_internal.h"
@@ -170,46 +169,6 @@ static void build_stats_and_work(aa_plan_s* p) {
   for (auto& w : p->bwd_items) p->bwd_tiles += (int64_t)(w.hi - w.lo + 1) * p->group;
 }
 
-// Persistent forward schedule: the forward kernel runs one CTA per SM, each
-// walking its own list of items. Items are dealt out in work-list order, each
-// to the CTA with the least estimated work so far (list scheduling; cost =
-// the item's tile steps plus an allowance for its loads and epilogue, which
-// mostly overlap the neighbouring items), so all CTAs finish close together.
-// Ties go to the lower CTA index. `items` is rewritten CTA-major; start[c] is
-// CTA c's first. (The backward kernel claims its items from a device counter
-// in work-list order instead: its L2 reuse needs the CTAs to stay together
-// in the list, which a static deal does not keep.)
-template <class Cost>
-static void build_schedule(std::vector<WorkItem>& items, std::vector<int32_t>& start, int num_sms, Cost cost) {
-  const int n = (int)items.size();
-  const int ncta = std::max(1, std::min(n, num_sms));
-  std::vector<std::vector<WorkItem>> lists(ncta);
-  using Load = std::pair<int64_t, int>;
-  std::priority_queue<Load, std::vector<Load>, std::greater<Load>> least;
-  for (int c = 0; c < ncta; ++c) least.push({0, c});
-  for (const WorkItem& w : items) {
-    const Load top = least.top();
-    least.pop();
-    lists[top.second].push_back(w);
-    least.push({top.first + cost(w), top.second});
-  }
-  std::vector<WorkItem> flat;
-  flat.reserve(n);
-  start.assign(1, 0);
-  for (const auto& l : lists) {
-    flat.insert(flat.end(), l.begin(), l.end());
-    start.push_back((int32_t)flat.size());
-  }
-  items.swap(flat);
-}
-
-static void build_schedules(aa_plan_s* p) {
-  // one step per key tile of the pair's range (both query tiles share it),
-  // plus two for the loads and epilogues
-  build_schedule(p->fwd_items, p->fwd_cta_start, p->num_sms,
-                 [&](const WorkItem& w) { return 2 + (int64_t)(w.hi - w.lo + 1); });
-}
-
 // Two-level cos/sin tables for Eq. 6: pos = 32*h + l, so
 // (cos, sin)(pos*theta_p) is the complex product of rope_hi[h][p] and
 // rope_lo[p][l]. Entries are computed in fp64 and rounded once to fp32.
@@ -257,8 +216,8 @@ static aa_status upload(T** dst, const std::vector<T>& src, cudaStream_t s, cons
 
 static void free_device(aa_plan_s* p) {
   DevicePlan& d = p->dev;
-  void* ptrs[] = {d.pos_id,    d.row_lo,  d.key_hi,    d.fwd_items, d.bwd_items, d.fwd_cta_start,
-                  d.qtile_klo, d.rope_hi, d.rope_lo, d.rope_step, d.err,       d.perm,     d.pos_orig};
+  void* ptrs[] = {d.pos_id,  d.row_lo,  d.key_hi,    d.fwd_items, d.bwd_items, d.qtile_klo, d.rope_hi,
+                  d.rope_lo, d.rope_step, d.err, d.fwd_next,  d.perm,      d.pos_orig};
   for (void* q : ptrs)
     if (q) cudaFree(q);
   d = DevicePlan{};
@@ -392,7 +351,6 @@ static aa_status make_plan(const aa_config* cfg, const int32_t* cu_doclens_host,
     delete p;
     return cuda_fail(e, "device query");
   }
-  build_schedules(p);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   std::vector<int32_t> zero(1, 0);
   DevicePlan& d = p->dev;
@@ -401,12 +359,12 @@ static aa_status make_plan(const aa_config* cfg, const int32_t* cu_doclens_host,
       (st = upload(&d.key_hi, p->key_hi, s, "key_hi")) != AA_OK ||
       (st = upload(&d.fwd_items, p->fwd_items, s, "fwd work list")) != AA_OK ||
       (st = upload(&d.bwd_items, p->bwd_items, s, "bwd work list")) != AA_OK ||
-      (st = upload(&d.fwd_cta_start, p->fwd_cta_start, s, "fwd schedule")) != AA_OK ||
       (st = upload(&d.qtile_klo, p->qtile_klo, s, "query-tile key ranges")) != AA_OK ||
       (st = upload(&d.rope_hi, p->rope_hi, s, "rope table (hi)")) != AA_OK ||
       (st = upload(&d.rope_lo, p->rope_lo, s, "rope table (lo)")) != AA_OK ||
       (st = upload(&d.rope_step, p->rope_step, s, "rope step table")) != AA_OK ||
       (st = upload(&d.err, zero, s, "error word")) != AA_OK ||
+      (st = upload(&d.fwd_next, zero, s, "forward work counter")) != AA_OK ||
       (p->segmented && ((st = upload(&d.perm, p->perm, s, "segment permutation")) != AA_OK ||
                         (st = upload(&d.pos_orig, p->seg_pos, s, "segment positions")) != AA_OK))) {
     cudaStreamSynchronize(s);
