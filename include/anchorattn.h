@@ -23,8 +23,9 @@
  *    head, channel), 16-byte aligned device pointers. LSE/D-style per-row
  *    values are fp32 [H, T].
  *  - Q and K are passed UN-ROTATED: the library rotates them (RoPE in fp32,
- *    rounded to bf16) inside its kernels; gradients are returned with respect
- *    to the un-rotated inputs.
+ *    rounded to bf16) once per call in its own kernels; gradients are returned
+ *    with respect to the un-rotated inputs (aa_bwd_from_fwd takes the
+ *    forward's rotated copies instead of q and k).
  *  - Token 0 is the anchor. cu_doclens (host int32[num_docs + 1]) gives the
  *    document boundaries after it: document k occupies tokens
  *    [cu[k-1], cu[k]), with cu[0] == 1, cu[num_docs] == T, strictly increasing.
@@ -37,6 +38,9 @@
  *  - aa_fwd / aa_bwd / aa_rope_apply allocate no memory (scratch comes from
  *    caller workspaces sized by aa_*_workspace_bytes). aa_plan allocates the
  *    plan's device metadata; aa_plan_destroy frees it.
+ *  - A plan's compute calls must not overlap on the GPU: they share the
+ *    plan's device error word and the forward's work counter. Issue them on
+ *    one stream, or order them with events. Separate plans are independent.
  *  - A thread-local message describing the last failure is available from
  *    aa_last_error().
  */
