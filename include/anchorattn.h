@@ -38,9 +38,10 @@
  *  - aa_fwd / aa_bwd / aa_rope_apply allocate no memory (scratch comes from
  *    caller workspaces sized by aa_*_workspace_bytes). aa_plan allocates the
  *    plan's device metadata; aa_plan_destroy frees it.
- *  - A plan's compute calls must not overlap on the GPU: they share the
- *    plan's device error word and the forward's work counter. Issue them on
- *    one stream, or order them with events. Separate plans are independent.
+ *  - Compute calls may overlap on the GPU when each has its own workspace
+ *    (the persistent kernels keep their work counters there); calls with one
+ *    plan share its device error word, so aa_check_device_error() reports a
+ *    timeout from any of them.
  *  - A thread-local message describing the last failure is available from
  *    aa_last_error().
  */
@@ -179,14 +180,16 @@ aa_status aa_rope_apply(aa_plan_t plan, const void* x, void* y, int32_t num_head
  * q [T,Hq,D], k/v [T,Hkv,D] bf16 in; o [T,Hq,D] bf16, lse [Hq,T] fp32 out.
  * Query head h reads kv head h / (Hq / Hkv). Q and K are rotated once per
  * call into `workspace` (caller-owned device memory of at least
- * aa_fwd_workspace_bytes(plan) bytes, 256-byte aligned, contents ignored;
- * NULL allowed when that size is 0), which the attention kernel then reads. */
+ * aa_fwd_workspace_bytes(plan) bytes, 256-byte aligned, contents ignored),
+ * which the attention kernel then reads; it also holds the kernel's work
+ * counter, so forward calls with separate workspaces may overlap. */
 aa_status aa_fwd(aa_plan_t plan, const void* q, const void* k, const void* v, void* o,
                  float* lse, void* workspace, size_t workspace_bytes, aa_stream_t stream);
 
-/* Bytes of device scratch aa_fwd needs (the rotated K and Q, T*(Hkv+Hq)*D
- * bf16, which it leaves there for aa_bwd_from_fwd; 0 with AA_ROPE_NONE;
- * segment plans add their grouped copies). */
+/* Bytes of device scratch aa_fwd needs: the rotated K and Q, T*(Hkv+Hq)*D
+ * bf16, which it leaves there for aa_bwd_from_fwd (none with AA_ROPE_NONE),
+ * plus 256 bytes for the work counter; segment plans add their grouped
+ * copies. */
 size_t aa_fwd_workspace_bytes(aa_plan_t plan);
 
 /* Bytes of device scratch aa_bwd needs (rotated Q and K, fp32 dQ

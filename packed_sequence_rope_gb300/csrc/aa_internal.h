@@ -33,7 +33,6 @@ struct DevicePlan {
   float2* rope_lo = nullptr;   // [D/2][32]    cos/sin(l * theta_p), p-major
   float2* rope_step = nullptr; // [D/2]        cos/sin(theta_p)
   int32_t* err = nullptr;      // device error word (0 = ok)
-  int32_t* fwd_next = nullptr; // the forward kernel's work counter (reset before each launch)
   int32_t* perm = nullptr;     // segment plans: [T] caller token of each grouped position
   int32_t* pos_orig = nullptr; // segment plans: [T] rotation index in the caller's token order
 };

@@ -485,7 +485,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 1) ptx::tmem_dealloc(tmem, kTmemCols);
 }
 
+// Forward workspace: [rotated K][rotated Q] (with RoPE), then 256 bytes
+// holding the attention kernel's work counter.
 size_t fwd_k_bytes(const aa_plan_s* p) { return ((size_t)p->T * p->Hkv * p->D * 2 + 255) & ~size_t(255); }
+size_t fwd_rot_bytes(const aa_plan_s* p) {
+  if (p->cfg.rope_layout == AA_ROPE_NONE) return 0;
+  return fwd_k_bytes(p) + (((size_t)p->T * p->Hq * p->D * 2 + 255) & ~size_t(255));
+}
+int32_t* fwd_counter(const aa_plan_s* p, void* workspace) {
+  return reinterpret_cast<int32_t*>(static_cast<uint8_t*>(workspace) + fwd_rot_bytes(p));
+}
 
 template <int HD>
 aa_status launch_fwd(aa_plan_s* p, const void* q, const void* k, const void* v, void* o, float* lse,
@@ -511,7 +520,7 @@ aa_status launch_fwd(aa_plan_s* p, const void* q, const void* k, const void* v, 
   P.row_lo = p->dev.row_lo;
   P.qtile_klo = p->dev.qtile_klo;
   P.items = p->dev.fwd_items;
-  P.next_item = p->dev.fwd_next;
+  P.next_item = fwd_counter(p, workspace);
   P.n_items = (int)p->fwd_items.size();
   P.rope_hi = p->dev.rope_hi;
   P.rope_lo = p->dev.rope_lo;
@@ -530,9 +539,9 @@ aa_status launch_fwd(aa_plan_s* p, const void* q, const void* k, const void* v, 
   cudaError_t e = cudaFuncSetAttribute(attn_fwd_kernel<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return cuda_fail(e, "attn_fwd_kernel smem attribute");
   // persistent: one CTA per SM (fewer for short work lists), claiming the
-  // items longest first from the plan's counter
+  // items longest first from the counter in this call's workspace
   if (p->fwd_items.empty()) return AA_OK;
-  if ((e = cudaMemsetAsync(p->dev.fwd_next, 0, sizeof(int32_t), s)) != cudaSuccess)
+  if ((e = cudaMemsetAsync(P.next_item, 0, sizeof(int32_t), s)) != cudaSuccess)
     return cuda_fail(e, "resetting the forward work counter");
   const unsigned n_cta = (unsigned)std::min<size_t>(p->fwd_items.size(), (size_t)std::max(p->num_sms, 1));
   attn_fwd_kernel<HD><<<n_cta, kThreads, smem, s>>>(tq, tk, tv, P);
@@ -548,8 +557,8 @@ void fwd_rotated_operands(const aa_plan_s* p, const void* fwd_workspace, const v
 }
 
 size_t fwd_base_workspace_bytes(const aa_plan_s* p) {
-  if (!p || p->cfg.rope_layout == AA_ROPE_NONE) return 0;
-  return fwd_k_bytes(p) + (((size_t)p->T * p->Hq * p->D * 2 + 255) & ~size_t(255));
+  if (!p) return 0;
+  return fwd_rot_bytes(p) + 256;
 }
 
 aa_status launch_fwd_with_workspace(aa_plan_s* p, const void* q, const void* k, const void* v, void* o, float* lse,
@@ -574,12 +583,10 @@ extern "C" aa_status aa_fwd(aa_plan_t p, const void* q, const void* k, const voi
   if (!q || !k || !v || !o || !lse) return fail(AA_ERR_INVALID_ARG, "NULL tensor pointer");
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
     return fail(AA_ERR_INVALID_ARG, "tensors must be 16-byte aligned");
-  const size_t need = aa_fwd_workspace_bytes(p);
-  if (need > 0) {
-    if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u))
-      return fail(AA_ERR_INVALID_ARG, "workspace must be a 256-byte aligned device pointer");
-    if (workspace_bytes < need) return fail(AA_ERR_INVALID_ARG, "workspace is smaller than aa_fwd_workspace_bytes()");
-  }
+  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+    return fail(AA_ERR_INVALID_ARG, "workspace must be a 256-byte aligned device pointer");
+  if (workspace_bytes < aa_fwd_workspace_bytes(p))
+    return fail(AA_ERR_INVALID_ARG, "workspace is smaller than aa_fwd_workspace_bytes()");
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (p->segmented) return seg_fwd(p, q, k, v, o, lse, workspace, s);
   return launch_fwd_with_workspace(p, q, k, v, o, lse, workspace, s);

@@ -216,8 +216,8 @@ static aa_status upload(T** dst, const std::vector<T>& src, cudaStream_t s, cons
 
 static void free_device(aa_plan_s* p) {
   DevicePlan& d = p->dev;
-  void* ptrs[] = {d.pos_id,  d.row_lo,  d.key_hi,    d.fwd_items, d.bwd_items, d.qtile_klo, d.rope_hi,
-                  d.rope_lo, d.rope_step, d.err, d.fwd_next,  d.perm,      d.pos_orig};
+  void* ptrs[] = {d.pos_id,    d.row_lo, d.key_hi, d.fwd_items, d.bwd_items, d.qtile_klo,
+                  d.rope_hi,   d.rope_lo, d.rope_step, d.err,   d.perm,      d.pos_orig};
   for (void* q : ptrs)
     if (q) cudaFree(q);
   d = DevicePlan{};
@@ -364,7 +364,6 @@ static aa_status make_plan(const aa_config* cfg, const int32_t* cu_doclens_host,
       (st = upload(&d.rope_lo, p->rope_lo, s, "rope table (lo)")) != AA_OK ||
       (st = upload(&d.rope_step, p->rope_step, s, "rope step table")) != AA_OK ||
       (st = upload(&d.err, zero, s, "error word")) != AA_OK ||
-      (st = upload(&d.fwd_next, zero, s, "forward work counter")) != AA_OK ||
       (p->segmented && ((st = upload(&d.perm, p->perm, s, "segment permutation")) != AA_OK ||
                         (st = upload(&d.pos_orig, p->seg_pos, s, "segment positions")) != AA_OK))) {
     cudaStreamSynchronize(s);

@@ -108,7 +108,8 @@ def test_compute_on_host_only_plan_is_refused(aa):
 @pytest.mark.parametrize("layout", [orc.ROPE_ADJACENT, orc.ROPE_NONE])
 @pytest.mark.parametrize("segmented", [False, True])
 def test_workspace_sizes(aa, layout, segmented):
-    # Forward: rotated K then rotated Q (bf16), nothing without RoPE; the
+    # Forward: rotated K then rotated Q (bf16), nothing without RoPE, then a
+    # 256-byte work counter; the
     # backward from the forward's rotated operands needs no copies of them,
     # and segment plans add grouped copies of their tensors.
     T, Hq, Hkv, D = 1000, 4, 2, 128
@@ -122,7 +123,7 @@ def test_workspace_sizes(aa, layout, segmented):
                               int(L.aa_bwd_from_fwd_workspace_bytes(p._h)))
     rot = al(T * Hkv * D * 2) + al(T * Hq * D * 2) if layout != orc.ROPE_NONE else 0
     seg_fwd = 2 * al(T * Hq * D * 2) + 2 * al(T * Hkv * D * 2) + al(Hq * T * 4) if segmented else 0
-    assert fwd == rot + seg_fwd
+    assert fwd == rot + 256 + seg_fwd
     # the two backward entry points differ by the rotated copies (and, for
     # segment plans, by the grouped copies of q and k)
     seg_qk = al(T * Hq * D * 2) + al(T * Hkv * D * 2) if segmented else 0
