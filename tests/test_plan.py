@@ -198,3 +198,28 @@ def test_segment_plan_rejects_bad_maps(aa):
         aa.Plan(None, 5, 1, 1, 64, 1e4, host_only=True, doc_of_token=np.array([1, 1, 2, 1, 2]))
     with pytest.raises(aa.AAError, match="doc_of_token\\[3\\]"):
         aa.Plan(None, 5, 1, 1, 64, 1e4, host_only=True, doc_of_token=np.array([0, 1, 2, 0, 2]))
+
+
+@pytest.mark.parametrize("seed", range(12))
+def test_random_packings_vs_oracle(aa, seed):
+    # documents of awkward lengths (1, tile-edge, random), T from 2 tokens up:
+    # metadata, pair and tile counts against the oracle, and the forward and
+    # backward work lists covering the same (query tile, key tile) pairs
+    rng = np.random.default_rng(100 + seed)
+    T = int(rng.integers(2, 3000))
+    lens, rem = [], T - 1
+    while rem > 0:
+        n = min(int(rng.choice([1, 2, 127, 128, 129, 255, 256, 257, int(rng.integers(1, 600))])), rem)
+        lens.append(n)
+        rem -= n
+    cu = np.concatenate([[1], 1 + np.cumsum(lens)]).astype(np.int32)
+    for mode in (orc.MASK_ANCHOR, orc.MASK_INTRA_DOC, orc.MASK_CAUSAL):
+        c = None if mode == orc.MASK_CAUSAL else cu
+        with aa.Plan(c, T, 4, 2, 64, 1e4, mode, host_only=True) as p:
+            doc, pos = p.metadata()
+            assert np.array_equal(doc, orc.document_ids(c, T, mode))
+            assert np.array_equal(pos, orc.position_ids(c, T, mode, orc.POS_RESET, 0))
+            st, w = p.stats(), p.work()
+        assert st["unmasked_pairs"] == orc.unmasked_pairs(c, T, mode)
+        assert (st["live_tiles"], st["causal_tiles"]) == orc.tile_counts(c, T, mode)
+        assert w["fwd_tiles"] == w["bwd_tiles"]
