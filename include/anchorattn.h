@@ -102,9 +102,10 @@ typedef struct aa_plan_s* aa_plan_t;
 /* Build the plan for one packing [ARCH §3.4 Anchor "Mask construction",
  * §3.4 Index]: per-token document and position IDs, each query row's visible
  * key interval, the live 128x128 tile lists (fully cross-document tiles are
- * dropped; the anchor column is folded in separately), longest-first work
- * order dealt out to one list per SM (the attention kernels are persistent),
- * and the two-level fp32 cos/sin tables of Eq. 6 built in fp64.
+ * dropped; the anchor column is folded in separately) in the order the
+ * persistent attention kernels claim them (longest first; the backward's
+ * grouped by document and head), and the two-level fp32 cos/sin tables of
+ * Eq. 6 built in fp64.
  * cu_doclens: host int32[num_docs + 1] (see conventions). Device metadata is
  * uploaded with copies ordered on `stream`. On success *out owns everything;
  * release it with aa_plan_destroy. */
@@ -135,8 +136,8 @@ aa_status aa_plan_with_theta(const aa_config* cfg, const int32_t* cu_doclens_hos
  * j <= i of its own document. Positions: RESET counts 1, 2, ... through the
  * document's tokens in order, CONTINUOUS is the token index; pos_shift adds.
  * cfg->mask_mode must be ANCHOR or INTRA_DOC. aa_fwd / aa_bwd /
- * aa_bwd_static_workspace / aa_rope_apply take and return tensors in the
- * caller's token order (the library groups the tokens by document, runs its
+ * aa_bwd_from_fwd / aa_bwd_static_workspace / aa_rope_apply take and return
+ * tensors in the caller's token order (the library groups the tokens by document, runs its
  * kernels and scatters the results back; the workspace sizes include the
  * grouped copies); aa_plan_metadata returns the caller's document ids and
  * positions; aa_plan_stats / aa_plan_work count the grouped layout's tiles.
@@ -273,8 +274,8 @@ aa_status aa_check_device_error(aa_plan_t plan, aa_stream_t stream);
 aa_status aa_set_wait_limit(aa_plan_t plan, uint64_t nanoseconds);
 
 /* Measurement hook: when both are non-NULL CUDA events (cudaEvent_t),
- * aa_bwd records `start` immediately before and `stop` immediately after the
- * launch of its main tile kernel, on the call's stream, so that kernel can be
+ * aa_bwd and aa_bwd_from_fwd record `start` immediately before and `stop`
+ * immediately after the launch of their main tile kernel, on the call's stream, so that kernel can be
  * timed on its own. NULL, NULL (the default) disables the recording. The
  * events are caller-owned and must outlive the calls that record them. */
 aa_status aa_set_bwd_timing_events(aa_plan_t plan, void* start, void* stop);
