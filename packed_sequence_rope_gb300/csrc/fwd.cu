@@ -125,6 +125,7 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, co
 // otherwise the calling thread alone. Slot readers: the MMA thread and the 8
 // softmax warps.
 constexpr int kFwdItemReaders = 9;
+static_assert(kFwdItemReaders == 1 + (kThreads / 32 - 4), "item readers: the MMA thread and warps 4-11");
 
 template <class Smem>
 __device__ __forceinline__ int read_fwd_item(Smem& sm, int li, const FwdParams& P, volatile int* abort_flag,
