@@ -12,6 +12,11 @@ Metric: effective TFLOP/s = 14 * D * Hq * P / (t_fwd + t_bwd), where P counts
 the visible (query, key) pairs of the mask, anchor pairs included (4*D flops
 per pair forward, 10*D backward); masked or padded work is not credited.
 
+The default line also carries `other_configs`: GQA 128K and the 64K
+mask-paradigm sweep (a few steps each, after the main timed region).
+--chunks N times the same documents cut into N chunks each and interleaved
+(a segment plan, documents given per token).
+
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 Under torchrun (N > 1) every rank runs the same workload on its own GPU
 (independent replicas, weak scaling); rank 0 prints one JSON line.
@@ -160,7 +165,16 @@ def run_ours(args):
     mask = {"anchor": aa.MASK_ANCHOR, "intra_doc": aa.MASK_INTRA_DOC, "causal": aa.MASK_CAUSAL}[args.mask]
     pos = {"reset": aa.POS_RESET, "continuous": aa.POS_CONTINUOUS}[args.pos]
     q, k, v, do = make_qkv(w, device=dev)
-    plan = aa.Plan(cu, T, Hq, Hkv, D, w.rope_base, mask, pos)
+    layout = "contiguous"
+    if args.chunks > 0:
+        # the same documents cut into chunks and interleaved (a segment plan:
+        # documents given per token); the visible pairs are unchanged
+        from aa_synth import interleaved_chunks
+        doc = interleaved_chunks(np.diff(cu), args.chunks, np.random.default_rng(0))
+        plan = aa.Plan(None, T, Hq, Hkv, D, w.rope_base, mask, pos, doc_of_token=doc)
+        layout = f"interleaved chunks x{args.chunks}"
+    else:
+        plan = aa.Plan(cu, T, Hq, Hkv, D, w.rope_base, mask, pos)
     st = plan.stats()
     work = plan.work()
     P = st["unmasked_pairs"]
@@ -175,6 +189,10 @@ def run_ours(args):
     # fwd: K and Q rotation + attention; bwd: (K and Q rotation,) prep, tile
     # kernel, dq finalize (+ anchor)
     n_launch_per_step = 3 + 3 + (2 if args.bwd == "recompute" else 0) + (1 if mask == aa.MASK_ANCHOR else 0)
+    if args.chunks > 0:
+        # gathers of q, k, v (fwd), scatters of o, lse; backward gathers of
+        # v, o, lse, dout and scatters of dq, dk, dv
+        n_launch_per_step += 5 + (7 if args.bwd == "from_fwd" else 9)
 
     def step():
         plan.fwd(q, k, v, o, lse, fws)
@@ -232,6 +250,13 @@ def run_ours(args):
     extra = {}
     if args.compare_causal and mask != aa.MASK_CAUSAL and rank == 0:
         extra["speedup_vs_causal"] = _causal_speedup(aa, w, q, k, v, do, dev, ms_step, args)
+    if args.other_configs and rank == 0 and world == 1 and args.chunks == 0 and w.name == "llama7b_64k":
+        causal = extra.get("speedup_vs_causal", {}).get("causal_ms_per_step")
+        del q, k, v, do, o, lse, dq, dk, dv, fws, bwd
+        torch.cuda.empty_cache()
+        t0 = time.perf_counter()
+        extra["other_configs"] = _other_configs(aa, dev, args, causal)
+        extra["other_configs"]["wall_s"] = round(time.perf_counter() - t0, 1)
 
     e2e = _e2e(aa, plan, w, dev, args, flops_fwd + flops_bwd, world) if not args.no_e2e else None
     cpu = None
@@ -243,7 +268,7 @@ def run_ours(args):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded N(0,1) bf16 Q/K/V/dO, seeded log-normal document lengths)",
-        "config": {"workload": w.name, "total_tokens": T, "num_q_heads": Hq, "num_kv_heads": Hkv,
+        "config": {"workload": w.name, "layout": layout, "total_tokens": T, "num_q_heads": Hq, "num_kv_heads": Hkv,
                    "head_dim": D, "rope_base": w.rope_base, "mask": args.mask, "pos": args.pos,
                    "documents": int(len(cu) - 1), "unmasked_pairs_per_head": P,
                    "l2": "inputs (2 GiB) larger than L2; no flush", "parallelism": f"replicas x{world}"},
@@ -257,9 +282,13 @@ def run_ours(args):
         "tiles": {"live": st["live_tiles"], "causal": st["causal_tiles"], "fwd_tiles": work["fwd_tiles"],
                   "bwd_tiles": work["bwd_tiles"]},
         "roofline": {"bound": "tensor", "kernel": dom_name, "achieved": round(achieved, 2),
-                     "peak": sustained, "unit": "TFLOP/s", "frac": round(achieved / sustained, 4),
-                     "peak_kind": f"bf16 sustained ({peak_src})", "frac_of_burst": round(achieved / burst, 4),
-                     "traffic": traffic},
+                     "peak": burst, "unit": "TFLOP/s", "frac": round(achieved / burst, 4),
+                     "peak_kind": f"bf16 burst ({peak_src}): the timed region is short and runs at the "
+                                  f"maximum clock", "frac_of_sustained": round(achieved / sustained, 4),
+                     "traffic": traffic,
+                     "traffic_source": "DRAM bytes per launch from the committed ncu capture of this kernel "
+                                       "(profiles/traffic.json, checked against the kernel source's hash; "
+                                       "null once the source changed), not measured in this run"},
         "cpu_baseline": cpu,
         "e2e": e2e,
         "gpu_launches": n_launch_per_step * args.steps,
@@ -273,6 +302,71 @@ def run_ours(args):
     plan.close()
     if world > 1:
         torch.distributed.destroy_process_group()
+
+
+def _time_steps(plan, fwd, bwd, steps, warmup):
+    """Mean ms per fwd+bwd step (CUDA events on the current stream) after
+    `warmup` untimed steps; the library's error word is checked after both."""
+    import torch
+    for _ in range(warmup):
+        fwd()
+        bwd()
+    plan.check_device_error()
+    a, z = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    a.record()
+    for _ in range(steps):
+        fwd()
+        bwd()
+    z.record()
+    torch.cuda.synchronize()
+    plan.check_device_error()
+    return a.elapsed_time(z) / steps
+
+
+def _other_configs(aa, dev, args, causal_ms_64k):
+    """The secondary configurations, a few timed steps each: GQA 128K, and the
+    mask-paradigm sweep at 64K (document-length medians 512 / 4096 / one
+    document under CAUSAL, INTRA_DOC + RESET and ANCHOR + RESET) with the
+    skipped-tile fraction and the speedup over the same kernels on the causal
+    mask. The causal step ignores the documents, so one causal timing (the
+    main workload's, same shape) serves every 64K sweep point."""
+    import torch
+    out = {}
+    runs = [("gqa_128k", "anchor")] + [(w, m) for w in ("sweep_64k_m512", "sweep_64k_m4096", "sweep_64k_single")
+                                       for m in ("intra_doc", "anchor")]
+    for name, mname in runs:
+        w = WORKLOADS[name]
+        cu = workload_cu_doclens(w)
+        T, Hq, Hkv, D = w.total_tokens, w.num_q_heads, w.num_kv_heads, w.head_dim
+        mask = {"anchor": aa.MASK_ANCHOR, "intra_doc": aa.MASK_INTRA_DOC}[mname]
+        q, k, v, do = make_qkv(w, device=dev)
+        with aa.Plan(cu, T, Hq, Hkv, D, w.rope_base, mask, aa.POS_RESET) as p:
+            st = p.stats()
+            o = torch.empty_like(q)
+            lse = torch.empty(Hq, T, device=dev, dtype=torch.float32)
+            dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+            fws = p.alloc_fwd_workspace(dev)
+            bwd = _bwd_call(p, args.bwd, q, k, v, o, lse, do, dq, dk, dv, fws, dev)
+            ms = _time_steps(p, lambda: p.fwd(q, k, v, o, lse, fws), bwd, args.other_steps, 2)
+            flops = 14.0 * D * Hq * st["unmasked_pairs"]
+            rec = {"mask": mname, "pos": "reset", "documents": int(len(cu) - 1), "ms_per_step": round(ms, 3),
+                   "tflops": round(flops / (ms * 1e-3) / 1e12, 2),
+                   "skipped_tile_fraction": round(1 - st["live_tiles"] / st["causal_tiles"], 4)}
+            if name.startswith("sweep_64k") and causal_ms_64k:
+                rec["speedup_vs_causal"] = round(causal_ms_64k / ms, 3)
+            out[f"{name}:{mname}"] = rec
+            del bwd, fws, o, lse, dq, dk, dv
+        del q, k, v, do
+        torch.cuda.empty_cache()
+    if causal_ms_64k:
+        w = WORKLOADS["llama7b_64k"]
+        out["sweep_64k:causal"] = {"mask": "causal", "ms_per_step": round(causal_ms_64k, 3),
+                                   "tflops": round(14.0 * w.head_dim * w.num_q_heads * w.total_tokens
+                                                   * (w.total_tokens + 1) / 2 / (causal_ms_64k * 1e-3) / 1e12, 2),
+                                   "skipped_tile_fraction": 0.0, "speedup_vs_causal": 1.0,
+                                   "note": "the causal mask ignores the documents: one timing for every 64K point"}
+    return out
 
 
 def _bwd_call(plan, kind, q, k, v, o, lse, do, dq, dk, dv, fws, dev):
@@ -460,6 +554,11 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--bwd", choices=["from_fwd", "recompute"], default="from_fwd",
                     help="backward entry point: aa_bwd_from_fwd (default) or aa_bwd")
+    ap.add_argument("--chunks", type=int, default=0,
+                    help="cut every document into this many chunks and interleave them (a segment plan)")
+    ap.add_argument("--other-configs", action=argparse.BooleanOptionalAction, default=True,
+                    help="also time GQA 128K and the 64K mask sweep (default workload, one GPU)")
+    ap.add_argument("--other-steps", type=int, default=3)
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         print("warning: fewer than 3 warm-up steps", file=sys.stderr)

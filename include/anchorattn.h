@@ -247,12 +247,19 @@ size_t aa_bwd_from_fwd_workspace_bytes(aa_plan_t plan);
  *  - Arguments and results are those of aa_bwd minus the workspace pair.
  *  - Plans whose aa_bwd_workspace_bytes() exceeds 64 MiB are rejected with
  *    AA_ERR_INVALID_ARG and a message giving both sizes; nothing is launched.
- *    With RoPE at D = 128 a query row needs about 1 KB (rotated Q and K and
- *    the fp32 dQ accumulator) and each query head 0.25 MiB of anchor
- *    partials, so T * Hq up to about 55K query rows fit.
+ *    aa_bwd_workspace_bytes() is the exact test. As a guide, for plans built
+ *    from cu_doclens with RoPE at D = 128 a query row needs about 1 KB
+ *    (rotated Q and K and the fp32 dQ accumulator) and each query head
+ *    0.25 MiB of anchor partials, so T * Hq up to about 55K query rows fit.
+ *    Segment plans (aa_plan_segments) also need grouped copies of q, k, v,
+ *    o, lse, dout and of the gradients, about twice as much per row, so
+ *    roughly half as many rows fit.
  *  - The plan's device must be current. The first call on a device looks up
- *    the array's device address (cudaGetSymbolAddress) once; make that first
- *    call before any stream capture on that device.
+ *    the array's device address (cudaGetSymbolAddress) once and keeps it for
+ *    the life of the process; make that first call before any stream capture
+ *    on that device. The kept address does not survive a reset of the
+ *    device's primary context (cudaDeviceReset): do not call this entry point
+ *    after one.
  *  - Every call on a device shares the one array, and the array keeps the
  *    last call's contents; the call overwrites all the scratch it reads, so
  *    nothing needs clearing. Calls whose executions overlap on the GPU (for

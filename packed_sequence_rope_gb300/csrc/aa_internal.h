@@ -4,6 +4,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <mutex>
 #include <string>
 #include <vector>
 
@@ -66,6 +67,19 @@ struct aa_plan_s {
 };
 
 namespace aa {
+constexpr int kMaxDevices = 64;
+
+// Per-device one-time host set-up (a kernel attribute, an occupancy query):
+// `fn` runs once for each device ordinal, thread-safely, and every later call
+// returns its first result. Ordinals outside [0, kMaxDevices) run `fn` every
+// time.
+template <class R, class Fn>
+R once_per_device(std::once_flag (&flags)[kMaxDevices], R (&results)[kMaxDevices], int device, Fn fn) {
+  if (device < 0 || device >= kMaxDevices) return fn();
+  std::call_once(flags[device], [&] { results[device] = fn(); });
+  return results[device];
+}
+
 // Record a failure message for aa_last_error() and return `s`.
 aa_status fail(aa_status s, const std::string& msg);
 aa_status cuda_fail(cudaError_t e, const char* what);

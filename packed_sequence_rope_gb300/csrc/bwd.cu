@@ -961,7 +961,11 @@ aa_status launch_bwd(aa_plan_s* p, const void* q, const void* k, const void* v, 
   P.layout = rope_layout;
   P.scale = p->scale;
   const size_t smem = sizeof(BwdSmem<HD>);
-  e = cudaFuncSetAttribute(attn_bwd_kernel<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  static std::once_flag attr_once[kMaxDevices];
+  static cudaError_t attr_result[kMaxDevices];
+  e = once_per_device(attr_once, attr_result, p->device, [&] {
+    return cudaFuncSetAttribute(attn_bwd_kernel<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  });
   if (e != cudaSuccess) return cuda_fail(e, "attn_bwd_kernel smem attribute");
   if (p->bwd_ev_start && (e = cudaEventRecord(p->bwd_ev_start, s)) != cudaSuccess)
     return cuda_fail(e, "recording the bwd start event");
@@ -975,10 +979,14 @@ aa_status launch_bwd(aa_plan_s* p, const void* q, const void* k, const void* v, 
     return cuda_fail(e, "recording the bwd stop event");
 
   // one full wave of resident blocks, grid-striding over the rows
-  static int fin_occ[2] = {0, 0};
-  int& occ = fin_occ[HD == 128];
-  if (occ == 0 && cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, dq_finalize_kernel<HD>, 256, 0) != cudaSuccess)
-    occ = 4;
+  static std::once_flag occ_once[kMaxDevices];
+  static int occ_result[kMaxDevices];
+  const int occ = once_per_device(occ_once, occ_result, p->device, [] {
+    int n = 0;
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, dq_finalize_kernel<HD>, 256, 0) == cudaSuccess && n > 0
+               ? n
+               : 4;
+  });
   const int rows = p->T * p->Hq;  // below 2^31: the plan checks T * Hq
   const int per_block = kFinNB * (256 / (HD / 8));
   const int64_t blocks = std::min<int64_t>((rows + per_block - 1) / per_block, (int64_t)p->num_sms * std::max(occ, 1));

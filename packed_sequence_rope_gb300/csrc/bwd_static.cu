@@ -16,12 +16,13 @@ constexpr size_t kStaticWorkspaceBytes = size_t(64) << 20;  // 64 MiB per device
 // comes from cudaGetSymbolAddress below.
 static __device__ __align__(256) unsigned char g_static_workspace[kStaticWorkspaceBytes];
 
-constexpr int kMaxDevices = 64;
 std::mutex g_mu;
 void* g_addr[kMaxDevices] = {};
 
-// Device address of the array on `device`, looked up once per device. The
-// caller has made `device` current.
+// Device address of the array on `device`, looked up once per device and
+// kept for the life of the process (a reset of the device's primary context
+// would invalidate it; the header tells callers not to reset). The caller has
+// made `device` current.
 aa_status static_workspace_address(int device, void** out) {
   if (device < 0 || device >= kMaxDevices) return fail(AA_ERR_UNSUPPORTED, "device ordinal out of range");
   std::lock_guard<std::mutex> lock(g_mu);
@@ -55,8 +56,8 @@ extern "C" aa_status aa_bwd_static_workspace(aa_plan_t p, const void* q, const v
     char buf[200];
     std::snprintf(buf, sizeof buf,
                   "this plan needs %zu bytes of backward scratch; the static workspace holds %zu bytes "
-                  "(64 MiB): use aa_bwd with a caller-provided workspace",
-                  need, kStaticWorkspaceBytes);
+                  "(%zu MiB): use aa_bwd with a caller-provided workspace",
+                  need, kStaticWorkspaceBytes, kStaticWorkspaceBytes >> 20);
     return fail(AA_ERR_INVALID_ARG, buf);
   }
   int current = -1;

@@ -537,7 +537,11 @@ aa_status launch_fwd(aa_plan_s* p, const void* q, const void* k, const void* v, 
   P.n_tiles = p->n_tiles;
   P.scale = p->scale;
   const size_t smem = sizeof(FwdSmem<HD>);
-  cudaError_t e = cudaFuncSetAttribute(attn_fwd_kernel<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  static std::once_flag attr_once[kMaxDevices];
+  static cudaError_t attr_result[kMaxDevices];
+  cudaError_t e = once_per_device(attr_once, attr_result, p->device, [&] {
+    return cudaFuncSetAttribute(attn_fwd_kernel<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  });
   if (e != cudaSuccess) return cuda_fail(e, "attn_fwd_kernel smem attribute");
   // persistent: one CTA per SM (fewer for short work lists), claiming the
   // items longest first from the counter in this call's workspace

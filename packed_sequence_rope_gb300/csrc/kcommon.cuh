@@ -43,9 +43,12 @@ __device__ __forceinline__ uint32_t sw128_chunk(int r, int c8) {
 // pairs, 16-row group g). The group's first row, and any row whose position
 // does not follow its predecessor's (a document start), take (cos, sin) from
 // the two-level tables; the other rows advance each pair's angle by one
-// theta_p with an exact complex product by (cos theta_p, sin theta_p). Over at
-// most 15 steps the drift stays near 1e-6 of the pair's magnitude, far below
-// the bf16 rounding of the result. Any kernel that rotates a tile runs this
+// theta_p with a complex product by (cos theta_p, sin theta_p) in fp32. A
+// table value is off by at most 3 fp32 units in the last place (u = 2^-24) per
+// component, each step adds at most 4.3u, and a unit takes at most 15 steps,
+// so with the rotation's own roundings the result is within 72u (4.3e-6) of
+// the pair's magnitude of the exact rotation: far below the bf16 rounding of
+// the result (2^-9 relative). Any kernel that rotates a tile runs this
 // same unit decomposition and arithmetic, so all rotations of a tile agree bit
 // for bit.
 //

@@ -46,3 +46,38 @@ def check_forward(o, lse, O_ref, L_ref, rows=None, tag=""):
 def rel_l2(got, ref):
     got = f64(got) if isinstance(got, torch.Tensor) else got
     return float(np.linalg.norm(got - ref) / max(np.linalg.norm(ref), 1e-30))
+
+
+# Error of the library's fp32 rotation before its bf16 rounding, in units of
+# u = 2^-24 times the pair's magnitude. A tile row's (cos, sin) is either a
+# two-level table value (two fp64 -> fp32 roundings and one fp32 angle
+# addition: at most 3u per component, 3*sqrt(2)u for the pair) or the previous
+# row's value advanced by one complex step (cos theta_p, sin theta_p): the
+# step's own fp32 rounding (sqrt(2)u/2) plus the product's roundings (2*sqrt(2)u)
+# add at most 4.3u per step, and a 16-row unit takes at most 15 steps from its
+# table value. The rotation itself adds at most 3u. Total < 4.3 + 15 * 4.3 + 3
+# = 72u; the bound takes 96u (a third of margin).
+ROT_U = 96 * 2.0 ** -24
+
+
+def bf16_ulp(x):
+    """Spacing of bfloat16 numbers at |x| (8 significant bits)."""
+    ax = np.maximum(np.abs(x), 1e-30)
+    return 2.0 ** (np.floor(np.log2(ax)) - 7)
+
+
+def pair_norm(x, layout=orc.ROPE_ADJACENT):
+    """|(a, b)| of the rotated pair each element of x [..., d] belongs to."""
+    d = x.shape[-1]
+    if layout == orc.ROPE_ADJACENT:
+        n = np.sqrt(x[..., 0::2] ** 2 + x[..., 1::2] ** 2)
+        return np.repeat(n, 2, axis=-1)
+    n = np.sqrt(x[..., : d // 2] ** 2 + x[..., d // 2:] ** 2)
+    return np.concatenate([n, n], axis=-1)
+
+
+def rope_bound(ref, x, layout=orc.ROPE_ADJACENT):
+    """Bound on |library rotation (bf16) - exact rotation| elementwise: the fp32
+    rotation's error plus one bf16 rounding of its result (a full ulp of the
+    reference covers a result that crosses a binade boundary)."""
+    return bf16_ulp(ref) + ROT_U * pair_norm(x, layout)

@@ -11,7 +11,7 @@ import torch
 
 import oracle as orc
 from aa_synth import WORKLOADS, make_qkv, workload_cu_doclens
-from gpu_common import (REL_L2, check_forward, f64, inputs, problem, rel_l2)
+from gpu_common import (REL_L2, check_forward, f64, inputs, problem, rel_l2, rope_bound)
 
 pytestmark = pytest.mark.gpu
 
@@ -24,28 +24,6 @@ def aa():
     __graft_entry__.build()
     import packed_sequence_rope_gb300 as pkg
     return pkg
-
-
-def _bf16_ulp(x):
-    ax = np.maximum(np.abs(x), 1e-30)
-    return 2.0 ** (np.floor(np.log2(ax)) - 7)
-
-
-def _pair_norm(x, layout):
-    """|(a, b)| of the rotated pair each element belongs to."""
-    d = x.shape[-1]
-    if layout == orc.ROPE_ADJACENT:
-        n = np.sqrt(x[..., 0::2] ** 2 + x[..., 1::2] ** 2)
-        return np.repeat(n, 2, axis=-1)
-    n = np.sqrt(x[..., : d // 2] ** 2 + x[..., d // 2:] ** 2)
-    return np.concatenate([n, n], axis=-1)
-
-
-def _rope_bound(ref, x, layout):
-    # one bf16 rounding of an fp32 rotation whose angle is advanced by at most
-    # 31 exact complex steps from a table value: the fp32 part stays below
-    # 1e-5 of the pair's magnitude
-    return _bf16_ulp(ref) + 1e-5 * _pair_norm(x, layout)
 
 
 # --------------------------------------------------------------------------- RoPE
@@ -62,9 +40,9 @@ def test_rope_apply_matches_oracle(aa, D, layout, shift):
         torch.cuda.synchronize()
     pos = orc.position_ids(cu, T, orc.MASK_ANCHOR, orc.POS_CONTINUOUS, shift)
     ref = orc.rotate(f64(x), pos, 5e5, layout)
-    assert (np.abs(f64(y) - ref) <= _rope_bound(ref, f64(x), layout)).all()
+    assert (np.abs(f64(y) - ref) <= rope_bound(ref, f64(x), layout)).all()
     ref_back = orc.rotate(f64(y), pos, 5e5, layout, inverse=True)
-    assert (np.abs(f64(back) - ref_back) <= _rope_bound(ref_back, f64(y), layout)).all()
+    assert (np.abs(f64(back) - ref_back) <= rope_bound(ref_back, f64(y), layout)).all()
 
 
 def test_rope_none_is_copy(aa):
@@ -208,7 +186,7 @@ def test_rope_apply_custom_theta_matches_oracle(aa, layout):
         torch.cuda.synchronize()
     pos = orc.position_ids(cu, T, orc.MASK_ANCHOR, orc.POS_CONTINUOUS, 3000)
     ref = orc.rotate(f64(x), pos, 1e4, layout, theta=theta)
-    assert (np.abs(f64(y) - ref) <= _rope_bound(ref, f64(x), layout)).all()
+    assert (np.abs(f64(y) - ref) <= rope_bound(ref, f64(x), layout)).all()
 
 
 def test_fwd_bwd_custom_theta_elementwise(aa):

@@ -8,7 +8,7 @@ import torch
 
 import oracle as orc
 from aa_synth import interleaved_chunks
-from gpu_common import REL_L2, check_forward, f64, inputs, rel_l2
+from gpu_common import REL_L2, check_forward, f64, inputs, rel_l2, rope_bound
 
 pytestmark = pytest.mark.gpu
 
@@ -62,9 +62,7 @@ def test_segments_rope_apply_uses_caller_positions(aa):
         torch.cuda.synchronize()
     pos = orc.segment_position_ids(doc, orc.POS_RESET, 9)
     ref = orc.rotate(f64(x), pos, 1e4)
-    pair = np.repeat(np.sqrt(f64(x)[..., 0::2] ** 2 + f64(x)[..., 1::2] ** 2), 2, axis=-1)
-    ulp = 2.0 ** (np.floor(np.log2(np.maximum(np.abs(ref), 1e-30))) - 7)
-    assert (np.abs(f64(y) - ref) <= ulp + 1e-5 * pair).all()
+    assert (np.abs(f64(y) - ref) <= rope_bound(ref, f64(x))).all()
 
 
 def test_contiguous_segments_bit_identical_to_cu_plan(aa):
