@@ -52,6 +52,38 @@ def column_counts(prob: Problem) -> np.ndarray:
     return mask_rows(np.arange(prob.T), prob.doc, prob.mask_mode).sum(axis=0)
 
 
+def attention_under_shift(prob: Problem, qr, kr, h: int, allowed):
+    """Logits A [T, T] (scale * q~_i . k~_j, every pair) and the masked softmax
+    ATTN [T, T] of query head h for rotated operands qr [T, Hq, d], kr
+    [T, Hkv, d]: the two matrices Eq. 4 and Eq. 5 compare across shifts.
+    Masked entries of ATTN are exactly 0 and every row of ATTN sums to 1."""
+    g = prob.kv_head(h)
+    a = prob.scale * (qr[:, h, :] @ kr[:, g, :].T)
+    s = np.where(allowed, a, -np.inf)
+    p = np.exp(s - s.max(axis=1, keepdims=True))
+    return a, p / p.sum(axis=1, keepdims=True)
+
+
+def eq4_column_sums(attn1, attn2) -> np.ndarray:
+    """Eq. 4's inner sum: for every key column j, sum over the query rows i of
+    |ATTN_ij(Δ1) - ATTN_ij(Δ2)|."""
+    return np.abs(np.asarray(attn1) - np.asarray(attn2)).sum(axis=0)
+
+
+def eq4_weighted_total(C, count) -> float:
+    """Eq. 4's outer sum for one head: sum_j n_j C_j with n_j = 1 / count_j
+    (count_j = rows that may attend to key j); columns nobody sees add 0."""
+    C, count = np.asarray(C, np.float64), np.asarray(count)
+    seen = count > 0
+    return float((C[seen] / count[seen]).sum())
+
+
+def eq5_first_logit(a1, a2, allowed) -> np.ndarray:
+    """Eq. 5's per-row term |A_{i,first}(Δ1) - A_{i,first}(Δ2)| for the first
+    token (index 0), 0 for rows that may not attend to it."""
+    return np.where(allowed[:, 0], np.abs(np.asarray(a1)[:, 0] - np.asarray(a2)[:, 0]), 0.0)
+
+
 def shift_diagnostic(prob1: Problem, prob2: Problem, q, k, bf16_operands: bool = True):
     """Eq. 4 and Eq. 5 for one input under the two problems' position shifts.
 
@@ -70,18 +102,12 @@ def shift_diagnostic(prob1: Problem, prob2: Problem, q, k, bf16_operands: bool =
     count = allowed.sum(axis=0)
     C = np.zeros((Hq, T))
     E = np.zeros((Hq, T))
+    D = 0.0
     for h in range(Hq):
-        g = prob1.kv_head(h)
-        attn = []
-        for qr, kr in ((q1, k1), (q2, k2)):
-            a = prob1.scale * (qr[:, h, :] @ kr[:, g, :].T)      # logits A_ij
-            s = np.where(allowed, a, -np.inf)
-            p = np.exp(s - s.max(axis=1, keepdims=True))
-            attn.append((a, p / p.sum(axis=1, keepdims=True)))
-        (a1, p1), (a2, p2) = attn
-        C[h] = np.abs(p1 - p2).sum(axis=0)
-        E[h] = np.where(allowed[:, 0], np.abs(a1[:, 0] - a2[:, 0]), 0.0)
-    seen = count > 0
-    D = float((C[:, seen] / count[seen]).sum())
+        a1, p1 = attention_under_shift(prob1, q1, k1, h, allowed)
+        a2, p2 = attention_under_shift(prob2, q2, k2, h, allowed)
+        C[h] = eq4_column_sums(p1, p2)
+        E[h] = eq5_first_logit(a1, a2, allowed)
+        D += eq4_weighted_total(C[h], count)
     D_logit = float(E.sum() / T)
     return {"C": C, "E": E, "count": count, "D": D, "D_logit": D_logit}

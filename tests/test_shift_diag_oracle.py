@@ -104,3 +104,78 @@ def test_first_token_logits_closed_form():
     want = [abs(logit(i, d1) - logit(i, d2)) for i in range(T)]
     assert np.allclose(r["E"][0], want, rtol=0, atol=1e-15)
     assert r["D_logit"] == pytest.approx(sum(want) / T, abs=1e-15)
+
+
+# ---------------------------------------------------------------- Eq. 4 by hand
+def test_eq4_hand_computed_three_by_three():
+    # Eq. 4 for one head, causal L = 3, with two attention matrices written out
+    # (rows i = queries, columns j = keys; each row sums to 1, zeros above the
+    # diagonal):
+    #   ATTN(Δ1) = [[1, 0, 0], [3/4, 1/4, 0], [1/2, 1/4, 1/4]]
+    #   ATTN(Δ2) = [[1, 0, 0], [1/2, 1/2, 0], [1/4, 1/4, 1/2]]
+    #   |diff|   = [[0, 0, 0], [1/4, 1/4, 0], [1/4, 0, 1/4]]
+    # summed over the rows of each column: C = [1/2, 1/4, 1/4]; the causal
+    # weights n = [1/L, 1/(L-1), 1] = [1/3, 1/2, 1], so
+    #   D = (1/2)(1/3) + (1/4)(1/2) + (1/4)(1) = 13/24.
+    # Summing over the wrong axis (row sums [0, 1/2, 1/2]) would give 3/4;
+    # weighting by 1/(j+1) instead would give 17/24.
+    from oracle.shift_diag import eq4_column_sums, eq4_weighted_total
+    p1 = np.array([[1, 0, 0], [0.75, 0.25, 0], [0.5, 0.25, 0.25]])
+    p2 = np.array([[1, 0, 0], [0.5, 0.5, 0], [0.25, 0.25, 0.5]])
+    C = eq4_column_sums(p1, p2)
+    assert np.array_equal(C, [0.5, 0.25, 0.25])
+    p, _ = _problems(None, 3, 1, 2, 1e4, orc.MASK_CAUSAL, 0, 0)
+    count = column_counts(p)
+    assert np.array_equal(count, [3, 2, 1])
+    assert eq4_weighted_total(C, count) == pytest.approx(13 / 24, abs=1e-15)
+
+
+def test_eq4_one_hot_flip_worked_example():
+    # End to end with d = 2 (one pair, theta_0 = 1 rad per position), causal
+    # L = 3, every q_i = (1, 0) and every k_j = (cos 1/2, sin 1/2). In exact
+    # arithmetic the logit of (i, j) is scale * cos(j - i + 1/2): row 1 ties
+    # keys 0 and 1 (cos(-1/2) = cos(1/2)) and row 2 ties keys 1 and 2, key 0
+    # far below (cos(-3/2) = 0.07). The shift cancels (Eq. 3); the bfloat16
+    # rounding of the rotated operands breaks the ties. Rounded by hand (8
+    # significant bits, to nearest):
+    #   Δ = 0: q~_2 = (cos 2, sin 2) -> (-0.416015625, 0.91015625)
+    #          k~_1 = (cos 1.5, sin 1.5) -> (0.07080078125, 0.99609375)
+    #          k~_2 = (cos 2.5, sin 2.5) -> (-0.80078125, 0.59765625)
+    #          row 2: key 1 0.877146721 > key 2 0.877098083 -> key 1
+    #          row 1: key 0 0.875663757 > key 1 0.874729156 -> key 0
+    #   Δ = 1: row 2: key 2 0.876731873 > key 1 0.876026154 -> key 2
+    #          row 1: key 0 0.877146721 > key 1 0.877098083 -> key 0
+    # With scale = 1e6 the smallest gap (4.9e-5) is 49 in the exponent, so
+    # every softmax row is one-hot to within e^-49. Row 2 moves from key 1 to
+    # key 2, rows 0 and 1 do not move: C = [0, 1, 1] and, with the weights
+    # [1/3, 1/2, 1], D = 1/2 + 1 = 3/2.
+    T = 3
+    q = np.zeros((T, 1, 2)); q[:, 0, 0] = 1.0
+    k = np.zeros((T, 1, 2)); k[:, 0, 0] = math.cos(0.5); k[:, 0, 1] = math.sin(0.5)
+    mk = lambda s: orc.Problem(None, T, 1, 1, 2, 1e4, orc.MASK_CAUSAL, orc.POS_RESET, orc.ROPE_ADJACENT,
+                               softmax_scale=1e6, pos_shift=s)
+    r = shift_diagnostic(mk(0), mk(1), q, k)
+    assert np.allclose(r["C"][0], [0.0, 1.0, 1.0], rtol=0, atol=1e-18)
+    assert r["D"] == pytest.approx(1.5, abs=1e-18)
+
+
+def test_attention_under_shift_equals_the_forward_oracle():
+    # the per-shift attention is the forward oracle's softmax: ATTN @ v equals
+    # forward()'s output for the same (already rotated, bf16) operands with
+    # rotation off, and ATTN's rows sum to 1 with exact zeros where masked
+    from oracle.shift_diag import attention_under_shift
+    cu, T, H, Hkv, d = [1, 20, 21, 64], 64, 2, 1, 16
+    q, k = _qk(T, H, d, 9)
+    k = k[:, :Hkv]
+    v = np.random.default_rng(9).standard_normal((T, Hkv, d))
+    p = orc.Problem(cu, T, H, Hkv, d, 1e4, orc.MASK_ANCHOR, orc.POS_RESET, pos_shift=40)
+    qr = round_to_bf16(orc.rotate(q, p.pos, 1e4))
+    kr = round_to_bf16(orc.rotate(k, p.pos, 1e4))
+    allowed = orc.mask_rows(np.arange(T), p.doc, orc.MASK_ANCHOR)
+    none = orc.Problem(cu, T, H, Hkv, d, 1e4, orc.MASK_ANCHOR, orc.POS_RESET, orc.ROPE_NONE)
+    O, _ = orc.forward(none, qr, kr, v)
+    for h in range(H):
+        _, attn = attention_under_shift(p, qr, kr, h, allowed)
+        assert np.allclose(attn @ v[:, 0, :], O[:, h, :], rtol=0, atol=1e-12)
+        assert np.allclose(attn.sum(axis=1), 1.0, rtol=0, atol=1e-14)
+        assert not attn[~allowed].any()
