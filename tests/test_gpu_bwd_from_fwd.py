@@ -103,3 +103,65 @@ def test_short_workspace_is_refused(aa):
         small = torch.empty(256, device="cuda", dtype=torch.uint8)
         with pytest.raises(aa.AAError, match="smaller than aa_bwd_from_fwd_workspace_bytes"):
             p.bwd_from_fwd(fws, v, o, lse, do, workspace=small)
+
+
+# --------------------------------------------------------------------------- full size, the timed path
+FULL = [
+    # workload, query heads checked (all of their kv groups' query heads, so
+    # the kv heads' dk / dv are complete)
+    ("llama7b_64k", [0, 17]),
+    ("gqa_128k", [4, 5, 6, 7]),   # kv head 1 and its whole query group
+]
+
+
+@pytest.mark.parametrize("name, heads", FULL, ids=[f[0] for f in FULL])
+def test_full_size_training_step(aa, name, heads):
+    # The benchmark's step at full size: aa_fwd, then aa_bwd_from_fwd on the
+    # forward's workspace. Documents are independent apart from the anchor
+    # (architecture page, §3.4 "AnchorAttention", "Mask construction": every
+    # row sees column 0, nothing crosses documents), so
+    #  - the longest document's dq, dk, dv equal the oracle's on [anchor + that
+    #    document] alone (its key ranges span the most tiles), and
+    #  - the anchor's dk_0, dv_0 are the sum, over every document, of the
+    #    oracle's anchor gradients from that document's rows, plus the anchor
+    #    row's own term (counted once): the full reduction over all T rows.
+    from aa_synth import WORKLOADS, make_qkv, workload_cu_doclens
+    w = WORKLOADS[name]
+    cu = workload_cu_doclens(w)
+    T, Hq, Hkv, D = w.total_tokens, w.num_q_heads, w.num_kv_heads, w.head_dim
+    group = Hq // Hkv
+    kv = sorted({h // group for h in heads})
+    assert sorted(heads) == [h for g in kv for h in range(g * group, (g + 1) * group)]
+    q, k, v, do = make_qkv(w, device="cuda")
+    with aa.Plan(cu, T, Hq, Hkv, D, w.rope_base) as p:
+        fws = p.alloc_fwd_workspace(q.device)
+        o, lse = p.fwd(q, k, v, workspace=fws)
+        dq, dk, dv = p.bwd_from_fwd(fws, v, o, lse, do)
+        torch.cuda.synchronize()
+        p.check_device_error()
+        del fws
+    hq = torch.tensor(heads)
+    hk = torch.tensor(kv)
+    host = (q.cpu()[:, hq], k.cpu()[:, hk], v.cpu()[:, hk], do.cpu()[:, hq])
+    dq, dk, dv = dq.cpu()[:, hq], dk.cpu()[:, hk], dv.cpu()[:, hk]
+    del q, k, v, do, o, lse
+    torch.cuda.empty_cache()
+    lens = np.diff(cu)
+    longest = int(np.argmax(lens))
+    gk0 = np.zeros((len(kv), D))
+    gv0 = np.zeros((len(kv), D))
+    for d in range(len(lens)):
+        a, b = int(cu[d]), int(cu[d + 1])
+        idx = torch.from_numpy(np.concatenate([[0], np.arange(a, b)]))
+        sub = orc.Problem([1, b - a + 1], b - a + 1, len(heads), len(kv), D, w.rope_base)
+        rows = np.arange(0 if d == 0 else 1, b - a + 1)   # the anchor row once, with the first document
+        gq, gk, gv = orc.backward(sub, *(t[idx] for t in host), rows=rows)
+        gk0 += gk[0]
+        gv0 += gv[0]
+        if d == longest:
+            for nm, got, ref in (("dq", dq[a:b], gq[1:]), ("dk", dk[a:b], gk[1:]), ("dv", dv[a:b], gv[1:])):
+                e = rel_l2(got, ref)
+                assert e <= REL_L2, f"{name} longest document ({b - a} tokens) {nm} rel-L2 {e:.3e}"
+    for nm, got, ref in (("dk_0", dk[0], gk0), ("dv_0", dv[0], gv0)):
+        e = rel_l2(got, ref)
+        assert e <= REL_L2, f"{name} anchor {nm} over all {T} rows: rel-L2 {e:.3e}"
