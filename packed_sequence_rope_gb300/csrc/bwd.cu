@@ -234,8 +234,11 @@ __global__ void __launch_bounds__(kPrepThreads) bwd_prep_kernel(const __nv_bfloa
 //               pass, since most items run only a handful of tiles)
 //   warps 4-11  P/dS: two groups (query columns 0-63 and 64-127), thread = key
 //               row = TMEM lane; P^T packed bf16 into TMEM for the dV product,
-//               dS^T bf16 into shared memory; at the end of an item they read
-//               dV and dK~ out of TMEM and write dv, dk
+//               dS^T bf16 into shared memory, each group in two 32-column
+//               chunks: the first chunks of both groups release half of the
+//               dV / dK~ products while the second chunks are computed; at
+//               the end of an item they read dV and dK~ out of TMEM and write
+//               dv, dk
 //   warps 12-15 dQ drain: dQ~ from TMEM into the fp32 accumulator. For
 //               D = 128 the MMA produces dQ~^T (lane = channel); the drain
 //               copies it into the step's dead Q~/dO stage buffers, releases
@@ -265,7 +268,7 @@ struct BwdSmem {
   uint64_t item_full[2], item_empty[2];
   int item_slot[2];  // claimed work-list index (-1: none left)
   uint64_t qd_full[2], q_ready[2], qd_empty[2];
-  uint64_t st_full, p_full, dq_full, dq_free, o_full, drain;
+  uint64_t st_full, p_full[2], dq_full, dq_free, o_full, drain;
   uint32_t tmem_base;
   int abort_flag;
 };
@@ -383,7 +386,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       ptx::mbar_init(&sm.qd_empty[s], 1);
     }
     ptx::mbar_init(&sm.st_full, 1);
-    ptx::mbar_init(&sm.p_full, 256);
+    ptx::mbar_init(&sm.p_full[0], 256);
+    ptx::mbar_init(&sm.p_full[1], 256);
     ptx::mbar_init(&sm.dq_full, 1);
     ptx::mbar_init(&sm.dq_free, 128);
     ptx::mbar_init(&sm.o_full, 1);
@@ -465,49 +469,49 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           ok = bwd_wait(&sm.qd_full[s], (gs >> 1) & 1, P, abort_flag, 412);
           if (!ok) break;
           ptx::tc_fence_after();
-          for (int kk = 0; kk < HD / 16; ++kk) {
-            const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-            ptx::mma_bf16(t_s, ptx::smem_desc_sw128(sk + off, 16, 1024), ptx::smem_desc_sw128(sq + off, 16, 1024),
-                          idesc_kt, kk > 0);
-          }
+          if constexpr (HD == 128)
+            ptx::mma8_ss_kk(t_s, ptx::smem_desc_sw128(sk, 16, 1024), ptx::smem_desc_sw128(sq, 16, 1024), idesc_kt, 0);
+          else
+            ptx::mma4_ss_kk(t_s, ptx::smem_desc_sw128(sk, 16, 1024), ptx::smem_desc_sw128(sq, 16, 1024), idesc_kt, 0);
           if (gs > 0) {
             // dQ~ of the previous tile must be drained before dP^T overwrites it
             ok = bwd_wait(&sm.dq_free, (gs - 1) & 1, P, abort_flag, 413);
             if (!ok) break;
             ptx::tc_fence_after();
           }
-          for (int kk = 0; kk < HD / 16; ++kk) {
-            const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-            ptx::mma_bf16(t_dp, ptx::smem_desc_sw128(sv + off, 16, 1024),
-                          ptx::smem_desc_sw128(sdo + off, 16, 1024), idesc_kt, kk > 0);
-          }
+          if constexpr (HD == 128)
+            ptx::mma8_ss_kk(t_dp, ptx::smem_desc_sw128(sv, 16, 1024), ptx::smem_desc_sw128(sdo, 16, 1024), idesc_kt, 0);
+          else
+            ptx::mma4_ss_kk(t_dp, ptx::smem_desc_sw128(sv, 16, 1024), ptx::smem_desc_sw128(sdo, 16, 1024), idesc_kt, 0);
           ptx::mma_commit(&sm.st_full);
-          // P/dS of this step; at an item's first step this also means the
-          // P/dS warps have read the previous item's dV / dK~ out of TMEM
-          ok = bwd_wait(&sm.p_full, gs & 1, P, abort_flag, 414);
+          // dV += P^T dO (P^T from TMEM: q 0-63 at cols 0-31, 64-127 at
+          // 64-95) and dK~ += dS^T Q~, each in two parts: the P/dS warps
+          // finish query columns 0-31 and 64-95 first (part 0), so those
+          // products run while they compute the rest (part 1). Part 0 of an
+          // item's first step also means the P/dS warps have read the
+          // previous item's dV / dK~ out of TMEM.
+          const uint64_t dv_b = ptx::smem_desc_sw128(sdo, 16384, 1024);
+          const uint64_t dk_a = ptx::smem_desc_sw128(sds, 16, 1024), dk_b = ptx::smem_desc_sw128(sq, 16384, 1024);
+          ok = bwd_wait(&sm.p_full[0], gs & 1, P, abort_flag, 414);
           if (!ok) break;
           ptx::tc_fence_after();
-          for (int kk = 0; kk < 8; ++kk)  // dV += P^T dO (P^T from TMEM: q 0-63 at cols 0-31, 64-127 at 64-95)
-            ptx::mma_bf16_ts(t_dv, t_s + (kk < 4 ? kk * 8 : 64 + (kk - 4) * 8),
-                             ptx::smem_desc_sw128(sdo + kk * 2048, 16384, 1024), idesc_kd,
-                             (step > 0 || kk > 0) ? 1u : 0u);
-          for (int kk = 0; kk < 8; ++kk) {  // dK~ += dS^T Q~
-            const uint32_t aoff = (kk >> 2) * 16384 + (kk & 3) * 32;
-            ptx::mma_bf16(t_dk, ptx::smem_desc_sw128(sds + aoff, 16, 1024),
-                          ptx::smem_desc_sw128(sq + kk * 2048, 16384, 1024), idesc_kd,
-                          (step > 0 || kk > 0) ? 1u : 0u);
-          }
+          ptx::mma4_ts_part0(t_dv, t_s, dv_b, idesc_kd, step > 0 ? 1u : 0u);
+          ptx::mma4_ss_part0(t_dk, dk_a, dk_b, idesc_kd, step > 0 ? 1u : 0u);
+          ok = bwd_wait(&sm.p_full[1], gs & 1, P, abort_flag, 416);
+          if (!ok) break;
+          ptx::tc_fence_after();
+          ptx::mma4_ts_part1(t_dv, t_s, dv_b, idesc_kd, 1u);
+          ptx::mma4_ss_part1(t_dk, dk_a, dk_b, idesc_kd, 1u);
           if constexpr (HD == 128) {
             // dQ~^T = K~^T dS^T: TMEM lanes = channels, columns = query rows, so
             // the drain's reductions are 128-byte coalesced per warp
             constexpr uint32_t idesc_qt = ptx::idesc_bf16_f32(128, 128, 1, 1);
-            for (int kk = 0; kk < 8; ++kk)
-              ptx::mma_bf16(t_dq, ptx::smem_desc_sw128(sk + kk * 2048, 16384, 1024),
-                            ptx::smem_desc_sw128(sds + kk * 2048, 16384, 1024), idesc_qt, kk > 0 ? 1u : 0u);
+            ptx::mma8_ss_mm(t_dq, ptx::smem_desc_sw128(sk, 16384, 1024), ptx::smem_desc_sw128(sds, 16384, 1024),
+                            idesc_qt, 0);
           } else {
-            for (int kk = 0; kk < 8; ++kk)  // dQ~ = dS K~ (TMEM lanes = query rows)
-              ptx::mma_bf16(t_dq, ptx::smem_desc_sw128(sds + kk * 2048, 16384, 1024),
-                            ptx::smem_desc_sw128(sk + kk * 2048, 16384, 1024), idesc_qd, kk > 0 ? 1u : 0u);
+            // dQ~ = dS K~ (TMEM lanes = query rows)
+            ptx::mma8_ss_mm(t_dq, ptx::smem_desc_sw128(sds, 16384, 1024), ptx::smem_desc_sw128(sk, 16384, 1024),
+                            idesc_qd, 0);
           }
           ptx::mma_commit(&sm.dq_full);  // the drain hands stage s back to the producer
         }
@@ -594,11 +598,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             *reinterpret_cast<uint4*>(sm.dst[c8 >> 3] + sw128_chunk(r, c8 & 7)) =
                 make_uint4(dw[0], dw[1], dw[2], dw[3]);
           }
+          // this chunk's P^T and dS^T are in place: part c - 2 cq of the dV and
+          // dK~ products may run
+          ptx::tmem_wait_st();
+          ptx::fence_proxy_async_smem();
+          ptx::tc_fence_before();
+          ptx::mbar_arrive(&sm.p_full[c - 2 * cq]);
         }
-        ptx::tmem_wait_st();
-        ptx::fence_proxy_async_smem();
-        ptx::tc_fence_before();
-        ptx::mbar_arrive(&sm.p_full);
       }
       if (ok) ok = bwd_wait(&sm.o_full, li & 1, P, abort_flag, 423);
       ok = __all_sync(0xffffffffu, ok);
@@ -938,7 +944,7 @@ aa_status launch_bwd(aa_plan_s* p, const void* q, const void* k, const void* v, 
   if ((st = make_tile_map(&tv, v, p->T, p->Hkv, HD)) != AA_OK) return st;
   if ((st = make_tile_map(&tdo, dout, p->T, p->Hq, HD)) != AA_OK) return st;
   CUtensorMap tdq;
-  if ((st = make_f32_half_map(&tdq, ws.dq_acc, p->T, p->Hq, HD)) != AA_OK) return st;
+  if ((st = make_f32_map(&tdq, ws.dq_acc, p->T, p->Hq, HD, 64, kTile)) != AA_OK) return st;
   BwdParams P;
   P.dk = static_cast<__nv_bfloat16*>(dk);
   P.dv = static_cast<__nv_bfloat16*>(dv);

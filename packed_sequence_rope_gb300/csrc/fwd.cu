@@ -256,11 +256,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           ready[t] = true;
           ptx::tc_fence_after();
         }
-        for (int kk = 0; kk < HD / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-          ptx::mma_bf16(t_s[t], ptx::smem_desc_sw128(ptx::smem_u32(sm.q[t][0]) + off, 16, 1024),
-                        ptx::smem_desc_sw128(ptx::smem_u32(sm.k[s][0]) + off, 16, 1024), idesc_s, kk > 0);
-        }
+        const uint64_t qd = ptx::smem_desc_sw128(ptx::smem_u32(sm.q[t][0]), 16, 1024);
+        const uint64_t kd = ptx::smem_desc_sw128(ptx::smem_u32(sm.k[s][0]), 16, 1024);
+        if constexpr (HD == 128)
+          ptx::mma8_ss_kk(t_s[t], qd, kd, idesc_s, 0);
+        else
+          ptx::mma4_ss_kk(t_s[t], qd, kd, idesc_s, 0);
         ptx::mma_commit(&sm.s_full[t]);
         return true;
       };
@@ -268,10 +269,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!wait_or_abort(&sm.p_full[t], ph_p[t], P, abort_flag, 311)) return false;
         ph_p[t] ^= 1;
         ptx::tc_fence_after();
-        for (int kk = 0; kk < 8; ++kk)
-          ptx::mma_bf16_ts(t_o[t], t_s[t] + kk * 8,
-                           ptx::smem_desc_sw128(ptx::smem_u32(sm.v[s][0]) + kk * 2048, 16384, 1024), idesc_pv,
-                           (!first_pv[t] || kk > 0) ? 1u : 0u);
+        ptx::mma8_ts_seq(t_o[t], t_s[t], ptx::smem_desc_sw128(ptx::smem_u32(sm.v[s][0]), 16384, 1024), idesc_pv,
+                         first_pv[t] ? 0u : 1u);
         first_pv[t] = false;
         return true;
       };

@@ -197,8 +197,8 @@ __device__ __forceinline__ QuadRaw quad_pack(int layout, const float* x, const f
 // 128-byte swizzle (one 16 KB tile block per load).
 aa_status make_tile_map(CUtensorMap* m, const void* base, int T, int H, int D);
 
-// Host: tensor map over x [T, H, D] fp32 with a {64, 1, 128} box, no swizzle
-// (a [128 rows][64 channels] fp32 block, 32 KB).
-aa_status make_f32_half_map(CUtensorMap* m, const void* base, int T, int H, int D);
+// Host: tensor map over x [T, H, D] fp32 with a {box_c, 1, box_t} box, no
+// swizzle (a [box_t rows][box_c channels] fp32 block).
+aa_status make_f32_map(CUtensorMap* m, const void* base, int T, int H, int D, int box_c, int box_t);
 
 }  // namespace aa

@@ -136,27 +136,111 @@ __device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
   asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
 }
 
-// D[tmem] (+)= A[smem] * B[smem]^T, kind::f16 (bf16 in, fp32 accumulate).
-__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
-                                         uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
+// tcgen05.mma kind::f16 (bf16 in, fp32 accumulate): D[tmem] (+)= A * B^T with
+// A from shared memory (a descriptor) or from TMEM (M rows = TMEM lanes, two
+// bf16 K-elements per 32-bit column, K-major) and B from shared memory.
+// Eight (or four) MMAs of one product, issued from a single asm block: the
+// k-th (k > 0) adds compile-time offsets to the first step's descriptors (in
+// 16-byte units, i.e. straight into the descriptors' address fields; no carry
+// leaves them since every operand lies inside the 256 KB shared window) or to
+// the A operand's TMEM column. Issued one asm statement at a time, an MMA
+// holds its warp about twice as long as the tensor core needs for an N = 128
+// step; one block lets the issues run back to back. The first MMA accumulates
+// only if `accumulate` != 0, the others always.
+#define AA_MMA_SS_STEP(ao, bo)                                                            \
+  "add.s64 ra, %1, " #ao ";\n\tadd.s64 rb, %2, " #bo ";\n\t"                          \
+  "tcgen05.mma.cta_group::1.kind::f16 [%0], ra, rb, %3, t;\n\t"
+#define AA_MMA_TS_STEP(ao, bo)                                                            \
+  "add.u32 rt, %1, " #ao ";\n\tadd.s64 rb, %2, " #bo ";\n\t"                          \
+  "tcgen05.mma.cta_group::1.kind::f16 [%0], [rt], rb, %3, t;\n\t"
+#define AA_MMA_PROLOGUE                                                                   \
+  "{\n\t.reg .pred p, t;\n\t.reg .b64 ra, rb;\n\t.reg .b32 rt;\n\t"                 \
+  "setp.ne.b32 p, %4, 0;\n\tsetp.eq.u32 t, %4, %4;\n\t"
+
+// A and B K-major with the 128-byte swizzle, 64 K-elements per 16 KB block:
+// K-steps 0-3 advance 32 bytes inside a block, steps 4-7 start the next block.
+__device__ __forceinline__ void mma8_ss_kk(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+  asm volatile(AA_MMA_PROLOGUE
+               "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t"
+               AA_MMA_SS_STEP(2, 2) AA_MMA_SS_STEP(4, 4) AA_MMA_SS_STEP(6, 6) AA_MMA_SS_STEP(1024, 1024)
+               AA_MMA_SS_STEP(1026, 1026) AA_MMA_SS_STEP(1028, 1028) AA_MMA_SS_STEP(1030, 1030) "}"
+               ::"r"(d), "l"(a), "l"(b), "r"(idesc), "r"(acc) : "memory");
+}
+// Four K-steps of the same layout (one 64-element block: D = 64 products).
+__device__ __forceinline__ void mma4_ss_kk(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+  asm volatile(AA_MMA_PROLOGUE
+               "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t"
+               AA_MMA_SS_STEP(2, 2) AA_MMA_SS_STEP(4, 4) AA_MMA_SS_STEP(6, 6) "}"
+               ::"r"(d), "l"(a), "l"(b), "r"(idesc), "r"(acc) : "memory");
+}
+// A K-major with the 128-byte swizzle (as above), B MN-major: each K-step
+// (16 rows of 128 bytes) advances B by 2048 bytes.
+__device__ __forceinline__ void mma8_ss_km(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+  asm volatile(AA_MMA_PROLOGUE
+               "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t"
+               AA_MMA_SS_STEP(2, 128) AA_MMA_SS_STEP(4, 256) AA_MMA_SS_STEP(6, 384) AA_MMA_SS_STEP(1024, 512)
+               AA_MMA_SS_STEP(1026, 640) AA_MMA_SS_STEP(1028, 768) AA_MMA_SS_STEP(1030, 896) "}"
+               ::"r"(d), "l"(a), "l"(b), "r"(idesc), "r"(acc) : "memory");
+}
+// A and B MN-major: both advance 2048 bytes per K-step.
+__device__ __forceinline__ void mma8_ss_mm(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+  asm volatile(AA_MMA_PROLOGUE
+               "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t"
+               AA_MMA_SS_STEP(128, 128) AA_MMA_SS_STEP(256, 256) AA_MMA_SS_STEP(384, 384) AA_MMA_SS_STEP(512, 512)
+               AA_MMA_SS_STEP(640, 640) AA_MMA_SS_STEP(768, 768) AA_MMA_SS_STEP(896, 896) "}"
+               ::"r"(d), "l"(a), "l"(b), "r"(idesc), "r"(acc) : "memory");
+}
+// A from TMEM (two bf16 K-elements per column, 8 columns per K-step),
+// B MN-major (2048 bytes per K-step). `a` is the first step's TMEM address;
+// steps 0-3 take columns a + 8k, steps 4-7 columns a + 64 + 8(k - 4): the two
+// 32-column halves that two 64-column groups of a 128-wide operand use.
+__device__ __forceinline__ void mma8_ts_split(uint32_t d, uint32_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+  asm volatile(AA_MMA_PROLOGUE
+               "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t"
+               AA_MMA_TS_STEP(8, 128) AA_MMA_TS_STEP(16, 256) AA_MMA_TS_STEP(24, 384) AA_MMA_TS_STEP(64, 512)
+               AA_MMA_TS_STEP(72, 640) AA_MMA_TS_STEP(80, 768) AA_MMA_TS_STEP(88, 896) "}"
+               ::"r"(d), "r"(a), "l"(b), "r"(idesc), "r"(acc) : "memory");
+}
+// A from TMEM, consecutive: step k takes columns a + 8k; B MN-major.
+__device__ __forceinline__ void mma8_ts_seq(uint32_t d, uint32_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+  asm volatile(AA_MMA_PROLOGUE
+               "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t"
+               AA_MMA_TS_STEP(8, 128) AA_MMA_TS_STEP(16, 256) AA_MMA_TS_STEP(24, 384) AA_MMA_TS_STEP(32, 512)
+               AA_MMA_TS_STEP(40, 640) AA_MMA_TS_STEP(48, 768) AA_MMA_TS_STEP(56, 896) "}"
+               ::"r"(d), "r"(a), "l"(b), "r"(idesc), "r"(acc) : "memory");
 }
 
-// D[tmem] (+)= A[tmem] * B[smem]^T, kind::f16: A (M rows = TMEM lanes) holds
-// two bf16 K-elements per 32-bit column, K-major.
-__device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
-                                            uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
+// Half of an eight-step product whose K runs over two 64-wide halves (query
+// columns 0-63 and 64-127): part 0 takes K-steps 0, 1, 4, 5 (columns 0-31 and
+// 64-95), part 1 K-steps 2, 3, 6, 7. A from TMEM at columns a + 8k' (k' the
+// step's column offset within the 128-wide operand), B MN-major.
+__device__ __forceinline__ void mma4_ts_part0(uint32_t d, uint32_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+  asm volatile(AA_MMA_PROLOGUE
+               "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t"
+               AA_MMA_TS_STEP(8, 128) AA_MMA_TS_STEP(64, 512) AA_MMA_TS_STEP(72, 640) "}"
+               ::"r"(d), "r"(a), "l"(b), "r"(idesc), "r"(acc) : "memory");
+}
+__device__ __forceinline__ void mma4_ts_part1(uint32_t d, uint32_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+  asm volatile(AA_MMA_PROLOGUE
+               "add.u32 rt, %1, 16;\n\tadd.s64 rb, %2, 256;\n\t"
+               "tcgen05.mma.cta_group::1.kind::f16 [%0], [rt], rb, %3, p;\n\t"
+               AA_MMA_TS_STEP(24, 384) AA_MMA_TS_STEP(80, 768) AA_MMA_TS_STEP(88, 896) "}"
+               ::"r"(d), "r"(a), "l"(b), "r"(idesc), "r"(acc) : "memory");
+}
+// The same split for A K-major with the 128-byte swizzle (two 64-column
+// blocks) and B MN-major.
+__device__ __forceinline__ void mma4_ss_part0(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+  asm volatile(AA_MMA_PROLOGUE
+               "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t"
+               AA_MMA_SS_STEP(2, 128) AA_MMA_SS_STEP(1024, 512) AA_MMA_SS_STEP(1026, 640) "}"
+               ::"r"(d), "l"(a), "l"(b), "r"(idesc), "r"(acc) : "memory");
+}
+__device__ __forceinline__ void mma4_ss_part1(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+  asm volatile(AA_MMA_PROLOGUE
+               "add.s64 ra, %1, 4;\n\tadd.s64 rb, %2, 256;\n\t"
+               "tcgen05.mma.cta_group::1.kind::f16 [%0], ra, rb, %3, p;\n\t"
+               AA_MMA_SS_STEP(6, 384) AA_MMA_SS_STEP(1028, 768) AA_MMA_SS_STEP(1030, 896) "}"
+               ::"r"(d), "l"(a), "l"(b), "r"(idesc), "r"(acc) : "memory");
 }
 
 // Arrive once on `bar` when all previously issued MMAs of this thread finish.

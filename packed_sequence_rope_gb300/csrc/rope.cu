@@ -115,12 +115,12 @@ aa_status launch_rope(const aa_plan_s* p, const void* x, void* y, int H, int inv
   return e == cudaSuccess ? AA_OK : cuda_fail(e, "rope_apply_kernel launch");
 }
 
-aa_status make_f32_half_map(CUtensorMap* m, const void* base, int T, int H, int D) {
+aa_status make_f32_map(CUtensorMap* m, const void* base, int T, int H, int D, int box_c, int box_t) {
   auto enc = get_encode_fn();
   if (!enc) return fail(AA_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
   cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)T};
   cuuint64_t strides[2] = {(cuuint64_t)D * 4, (cuuint64_t)H * D * 4};
-  cuuint32_t box[3] = {64, 1, (cuuint32_t)kTile};
+  cuuint32_t box[3] = {(cuuint32_t)box_c, 1, (cuuint32_t)box_t};
   cuuint32_t estr[3] = {1, 1, 1};
   CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void*>(base), dims, strides, box, estr,
                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
