@@ -321,6 +321,37 @@ aa_status aa_shift_diag(aa_plan_t plan1, aa_plan_t plan2, const void* q, const v
                         float* first_logit_absdiff, double* result, void* workspace, size_t workspace_bytes,
                         aa_stream_t stream);
 
+/* Sharding of one packing across ranks [ARCH §3.4 Anchor] ("Mask
+ * construction": documents see nothing of one another; every row sees the
+ * anchor), architecture page §3.4 "AnchorContext: Implementation
+ * Infrastructure" (the pages shard attention over 8 GPUs). Host only: no
+ * plan, no device.
+ * A piece is document `doc` (1-based, as in cu_doclens) restricted to kv
+ * heads [kv_head_begin, kv_head_end) and their query heads (query head h
+ * belongs to kv head h / group); `cost` = its visible pairs, (N(N+1)/2 + N)
+ * per query head. Pieces go longest first to the least-loaded shard; a
+ * document whose all-head cost exceeds total / num_shards is first cut into
+ * ceil(cost / (total / num_shards)) kv-head ranges (at most num_kv_heads).
+ * Every (document, kv head) lies in exactly one piece, so each rank runs its
+ * pieces as ordinary packings (one per distinct head range, each with its
+ * own copy of the anchor token) and the only exchanges are the anchor's k_0 /
+ * v_0 (broadcast before the forward) and the sum of the ranks' dk_0 / dv_0
+ * (all-reduce after the backward).
+ *  - cu_doclens: host int32[num_docs + 1], as for aa_plan (cu[0] == 1).
+ *  - group = Hq / Hkv; num_shards >= 1.
+ *  - pieces: caller array of max_pieces entries, filled sorted by (shard,
+ *    kv_head_begin, doc); *num_pieces receives the count. If max_pieces is
+ *    too small, *num_pieces receives the count needed and AA_ERR_INVALID_ARG
+ *    is returned (call with pieces = NULL, max_pieces = 0 to size the array).
+ *  - shard_cost: optional int64[num_shards], each shard's summed cost. */
+typedef struct {
+  int32_t shard, doc, kv_head_begin, kv_head_end;
+  int64_t cost;
+} aa_shard_piece;
+aa_status aa_shard_plan(const int32_t* cu_doclens_host, int32_t num_docs, int32_t num_kv_heads, int32_t group,
+                        int32_t num_shards, aa_shard_piece* pieces, int32_t max_pieces, int32_t* num_pieces,
+                        int64_t* shard_cost);
+
 const char* aa_status_string(aa_status status);
 const char* aa_last_error(void);
 

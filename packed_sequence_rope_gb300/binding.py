@@ -25,7 +25,12 @@ EXPORTS = ["aa_plan", "aa_plan_with_theta", "aa_plan_segments", "aa_plan_destroy
            "aa_rope_apply", "aa_fwd", "aa_fwd_workspace_bytes", "aa_bwd_workspace_bytes", "aa_bwd", "aa_bwd_from_fwd",
            "aa_bwd_from_fwd_workspace_bytes", "aa_bwd_static_workspace", "aa_check_device_error",
            "aa_set_wait_limit", "aa_set_bwd_timing_events", "aa_selftest_bounded_wait", "aa_status_string",
-           "aa_last_error", "aa_shift_diag_workspace_bytes", "aa_shift_diag"]
+           "aa_last_error", "aa_shift_diag_workspace_bytes", "aa_shift_diag", "aa_shard_plan"]
+
+
+class AAShardPiece(ctypes.Structure):
+    _fields_ = [("shard", ctypes.c_int32), ("doc", ctypes.c_int32), ("kv_head_begin", ctypes.c_int32),
+                ("kv_head_end", ctypes.c_int32), ("cost", ctypes.c_int64)]
 
 
 class AAConfig(ctypes.Structure):
@@ -80,6 +85,8 @@ def lib():
             "aa_last_error": ([], ctypes.c_char_p),
             "aa_shift_diag_workspace_bytes": ([vp], ctypes.c_size_t),
             "aa_shift_diag": ([vp, vp, vp, vp, vp, vp, vp, vp, ctypes.c_size_t, vp], ctypes.c_int),
+            "aa_shard_plan": ([i32p, i32, i32, i32, i32, ctypes.POINTER(AAShardPiece), i32, i32p, i64p],
+                              ctypes.c_int),
         }
         for name, (args, res) in sig.items():
             f = getattr(L, name)
@@ -294,3 +301,21 @@ class Plan:
         _check(lib().aa_bwd_static_workspace(self._h, _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse),
                                              _ptr(dout), _ptr(dq), _ptr(dk), _ptr(dv), _stream(stream)))
         return dq, dk, dv
+
+
+def shard_plan(cu_doclens, num_kv_heads, group, num_shards):
+    """aa_shard_plan: pieces (shard, doc, kv_head_begin, kv_head_end, cost) and
+    each shard's total cost. Host only."""
+    cu = np.ascontiguousarray(np.asarray(cu_doclens, dtype=np.int32))
+    n = ctypes.c_int32()
+    ip = lambda a: a.ctypes.data_as(ctypes.POINTER(ctypes.c_int32))
+    st = lib().aa_shard_plan(ip(cu), int(cu.size) - 1, int(num_kv_heads), int(group), int(num_shards), None, 0,
+                             ctypes.byref(n), None)
+    if st != 0 and n.value == 0:
+        _check(st)
+    pieces = (AAShardPiece * max(n.value, 1))()
+    cost = np.zeros(int(num_shards), dtype=np.int64)
+    _check(lib().aa_shard_plan(ip(cu), int(cu.size) - 1, int(num_kv_heads), int(group), int(num_shards), pieces,
+                               n.value, ctypes.byref(n), cost.ctypes.data_as(ctypes.POINTER(ctypes.c_int64))))
+    out = [(p.shard, p.doc, p.kv_head_begin, p.kv_head_end, p.cost) for p in pieces[:n.value]]
+    return out, cost

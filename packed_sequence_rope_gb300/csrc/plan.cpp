@@ -468,6 +468,69 @@ extern "C" aa_status aa_check_device_error(aa_plan_t p, aa_stream_t stream) {
   return AA_OK;
 }
 
+// ---------------------------------------------------------------- sharding
+// Documents are independent apart from the anchor column ("Mask
+// construction": nothing crosses documents; every row sees token 0), so a
+// packing splits across ranks along documents and heads. A piece is one
+// document with a range of kv heads (and their query heads); its cost is the
+// visible pairs it covers: (N(N+1)/2 + N) per query head (intra-document
+// causal pairs plus one anchor edge per token). Pieces are dealt longest
+// first to the least-loaded shard (LPT). A document whose all-head cost
+// exceeds one shard's share of the total is cut into that many kv-head ranges
+// (as even as the kv heads allow) before dealing, so no rank holds a
+// disproportionate document and no piece needs another rank's keys.
+extern "C" aa_status aa_shard_plan(const int32_t* cu, int32_t num_docs, int32_t num_kv_heads, int32_t group,
+                                   int32_t num_shards, aa_shard_piece* pieces, int32_t max_pieces,
+                                   int32_t* num_pieces, int64_t* shard_cost) {
+  if (!cu || !num_pieces) return fail(AA_ERR_INVALID_ARG, "aa_shard_plan: cu_doclens and num_pieces are required");
+  if (num_docs < 1 || num_kv_heads < 1 || group < 1 || num_shards < 1)
+    return fail(AA_ERR_INVALID_ARG, "aa_shard_plan: num_docs, num_kv_heads, group and num_shards must be >= 1");
+  if (cu[0] != 1) return fail(AA_ERR_INVALID_ARG, "aa_shard_plan: cu_doclens[0] must be 1 (token 0 is the anchor)");
+  for (int k = 1; k <= num_docs; ++k)
+    if (cu[k] <= cu[k - 1]) return fail(AA_ERR_INVALID_ARG, "aa_shard_plan: cu_doclens must increase strictly");
+  auto pair_cost = [&](int d) {  // one query head of document d (0-based)
+    const int64_t n = cu[d + 1] - cu[d];
+    return n * (n + 1) / 2 + n;
+  };
+  int64_t total = 0;
+  for (int d = 0; d < num_docs; ++d) total += pair_cost(d) * num_kv_heads * group;
+  const double share = (double)total / num_shards;
+  std::vector<aa_shard_piece> out;
+  for (int d = 0; d < num_docs; ++d) {
+    const int64_t all = pair_cost(d) * num_kv_heads * group;
+    int parts = (int)std::min<int64_t>(num_kv_heads, std::max<int64_t>(1, (int64_t)std::ceil(all / share - 1e-9)));
+    for (int j = 0; j < parts; ++j) {
+      const int g0 = (int)((int64_t)num_kv_heads * j / parts), g1 = (int)((int64_t)num_kv_heads * (j + 1) / parts);
+      out.push_back(aa_shard_piece{-1, d + 1, g0, g1, pair_cost(d) * (g1 - g0) * group});
+    }
+  }
+  if ((int64_t)out.size() > max_pieces || (!pieces && max_pieces > 0)) {
+    *num_pieces = (int32_t)out.size();
+    return fail(AA_ERR_INVALID_ARG, "aa_shard_plan: pieces[] is too small (num_pieces holds the count needed)");
+  }
+  std::vector<size_t> order(out.size());
+  for (size_t i = 0; i < order.size(); ++i) order[i] = i;
+  std::stable_sort(order.begin(), order.end(), [&](size_t a, size_t b) { return out[a].cost > out[b].cost; });
+  std::vector<int64_t> load(num_shards, 0);
+  for (size_t i : order) {
+    int best = 0;
+    for (int r = 1; r < num_shards; ++r)
+      if (load[r] < load[best]) best = r;
+    out[i].shard = best;
+    load[best] += out[i].cost;
+  }
+  std::stable_sort(out.begin(), out.end(), [](const aa_shard_piece& a, const aa_shard_piece& b) {
+    if (a.shard != b.shard) return a.shard < b.shard;
+    if (a.kv_head_begin != b.kv_head_begin) return a.kv_head_begin < b.kv_head_begin;
+    return a.doc < b.doc;
+  });
+  for (size_t i = 0; i < out.size(); ++i) pieces[i] = out[i];
+  *num_pieces = (int32_t)out.size();
+  if (shard_cost)
+    for (int r = 0; r < num_shards; ++r) shard_cost[r] = load[r];
+  return AA_OK;
+}
+
 extern "C" const char* aa_status_string(aa_status s) {
   switch (s) {
     case AA_OK: return "AA_OK";
