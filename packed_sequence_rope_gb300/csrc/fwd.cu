@@ -51,9 +51,6 @@ struct FwdSmem {
   alignas(1024) uint8_t q[2][kB][16384];
   alignas(1024) uint8_t k[kStages][kB][16384];
   alignas(1024) uint8_t v[kStages][kB][16384];
-  alignas(1024) uint8_t ostage[kB][16384];  // one finished O tile, bf16, 128-byte swizzle
-  uint64_t ost_full, ost_free;              // O stage written (128 rows) / read by its TMA store
-  int ost_row0, ost_head;                   // where the staged tile goes
   uint64_t q_full[2], q_free[2];
   uint64_t item_full[2], item_empty[2];
   int item_slot[2];  // claimed work-list index (-1: none left)
@@ -125,10 +122,10 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, co
 // The li-th item this CTA runs (its work-list index, or -1 when the list is
 // exhausted or the CTA aborted), as the producer published it in slot li & 1.
 // warp_read: the whole (converged) warp reads it and lane 0 frees the slot;
-// otherwise the calling thread alone. Slot readers: the MMA thread, the O
-// storer thread and the 8 softmax warps.
-constexpr int kFwdItemReaders = 10;
-static_assert(kFwdItemReaders == 2 + (kThreads / 32 - 4), "item readers: MMA thread, storer thread, warps 4-11");
+// otherwise the calling thread alone. Slot readers: the MMA thread and the 8
+// softmax warps.
+constexpr int kFwdItemReaders = 9;
+static_assert(kFwdItemReaders == 1 + (kThreads / 32 - 4), "item readers: the MMA thread and warps 4-11");
 
 template <class Smem>
 __device__ __forceinline__ int read_fwd_item(Smem& sm, int li, const FwdParams& P, volatile int* abort_flag,
@@ -157,8 +154,7 @@ __device__ __forceinline__ int read_fwd_item(Smem& sm, int li, const FwdParams& 
 template <int HD>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                    const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
-                    const FwdParams P) {
+                    const __grid_constant__ CUtensorMap tmV, const FwdParams P) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   if (ptx::smem_u32(smem_raw) & 1023u) {  // swizzled tiles need a 1 KB aligned base
     if (threadIdx.x == 0) atomicCAS(P.err, 0, 398);
@@ -174,7 +170,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::tma_prefetch_desc(&tmQ);
     ptx::tma_prefetch_desc(&tmK);
     ptx::tma_prefetch_desc(&tmV);
-    ptx::tma_prefetch_desc(&tmO);
     for (int t = 0; t < 2; ++t) {
       ptx::mbar_init(&sm.q_full[t], 1);
       ptx::mbar_init(&sm.q_free[t], 128);
@@ -191,8 +186,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::mbar_init(&sm.item_empty[s], kFwdItemReaders);
     }
     ptx::mbar_init(&sm.drain, 1);
-    ptx::mbar_init(&sm.ost_full, 128);
-    ptx::mbar_init(&sm.ost_free, 1);
     sm.abort_flag = 0;
     ptx::fence_mbar_init();
   }
@@ -324,32 +317,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::mma_commit(&sm.drain);
       ptx::mbar_wait(&sm.drain, 0, kDrainLimitNs, P.err, 319);
     }
-  } else if (warp == 2) {
-    // ------------------------------------------------------------ O storer
-    // Each item's finished O tiles (tile 0, then tile 1 when it exists) pass
-    // through the one staging buffer: the softmax group writes its rows
-    // there, this thread stores the tile with TMA and frees the buffer once
-    // the store has read it.
-    if (lane == 0) {
-      int k = 0;
-      bool ok = true;
-      for (int li = 0; ok; ++li) {
-        const int it = read_fwd_item(sm, li, P, abort_flag, false, 340);
-        if (it < 0) break;
-        const FwdItem w = load_fwd_item(P, it);
-        for (int u = 0; u < (w.has1 ? 2 : 1) && ok; ++u, ++k) {
-          ok = wait_or_abort(&sm.ost_full, k & 1, P, abort_flag, 341);
-          if (!ok) break;
-          const int h = *reinterpret_cast<volatile int*>(&sm.ost_head);
-          const int row0 = *reinterpret_cast<volatile int*>(&sm.ost_row0);
-          for (int b = 0; b < HD / 64; ++b) ptx::tma_store_3d(&tmO, sm.ostage[b], b * 64, h, row0);
-          ptx::bulk_commit();
-          ptx::bulk_wait_read0();
-          ptx::mbar_arrive(&sm.ost_free);
-        }
-      }
-      ptx::bulk_wait0();  // the stores are complete before the CTA exits
-    }
   } else if (warp >= 4 && warp < 12) {
     // ------------------------------------------------------------ softmax
     const int t = (warp - 4) >> 2;
@@ -359,14 +326,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t t_s = tmem + 128 * t + lane_off, t_o = tmem + 256 + HD * t + lane_off;
     uint32_t ph_s = 0;
     int nq = 0;
-    int nstage = 0;  // O-stage uses before this item (both groups, in item order: tile 0, then tile 1)
     bool ok = true;
     for (int li = 0; ok; ++li) {
       const int it = read_fwd_item(sm, li, P, abort_flag, true, 320);
       if (it < 0) break;
       const FwdItem w = load_fwd_item(P, it);
-      const int use = nstage + t;  // this group's stage use in this item
-      nstage += w.has1 ? 2 : 1;
       if (t == 1 && !w.has1) continue;
       const int h = w.h, g = h / P.group;
       const int lo_t = w.lo[t], hi_t = w.hi[t];
@@ -414,25 +378,18 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int c = 0; c < 4; ++c) ptx::tmem_ld32(t_s + c * 32, sv + c * 32);
         ptx::tmem_wait_ld();
-        // pass 1: row max of the visible logits (scaled once at the end):
-        // four 3-input max chains, so the dependent chain is 16 deep
-        float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+        // pass 1: row max of the visible logits (scaled once at the end)
+        float mt = -INFINITY;
         if (full) {
 #pragma unroll
-          for (int e = 0; e < 128; e += 8)
-#pragma unroll
-            for (int a = 0; a < 4; ++a) mx[a] = ptx::fmax3(mx[a], sv[e + 2 * a], sv[e + 2 * a + 1]);
+          for (int e = 0; e < 128; e += 2) mt = fmaxf(mt, fmaxf(sv[e], sv[e + 1]));
         } else {
 #pragma unroll
-          for (int e = 0; e < 128; e += 8)
-#pragma unroll
-            for (int a = 0; a < 4; ++a) {
-              const int j = j0 + e + 2 * a;
-              mx[a] = ptx::fmax3(mx[a], (j >= lo && j <= hi) ? sv[e + 2 * a] : -INFINITY,
-                                 (j + 1 >= lo && j + 1 <= hi) ? sv[e + 2 * a + 1] : -INFINITY);
-            }
+          for (int e = 0; e < 128; ++e) {
+            const int j = j0 + e;
+            if (j >= lo && j <= hi) mt = fmaxf(mt, sv[e]);
+          }
         }
-        float mt = fmaxf(ptx::fmax3(mx[0], mx[1], mx[2]), mx[3]);
         mt *= sl2;
         // TMEM access is warp-collective, so a rescale of O is decided per warp
         const bool need = (mt > m + kRescaleThreshold) || (m == -INFINITY && mt > -INFINITY);
@@ -492,42 +449,32 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) break;
       // ---- epilogue. Its TMEM reads complete (tmem_wait_ld) before this
       // thread's next p_full arrival, which the next item's first PV of this
-      // tile (overwriting O) waits for. The row goes into the O stage (once
-      // the previous tile's store has read it); the storer thread writes the
-      // tile with TMA, so the group moves on without waiting for the stores.
+      // tile (overwriting O) waits for.
       ptx::tc_fence_after();
-      if (use > 0) ok = __all_sync(0xffffffffu, wait_or_abort(&sm.ost_free, (use - 1) & 1, P, abort_flag, 325));
-      if (!ok) break;
-      if (r == 0) {
-        sm.ost_head = h;
-        sm.ost_row0 = (w.qt0 + t) * kTile;
-      }
       const float w0 = P.anchor ? exp2f(s0 - m) : 0.f;
       const float inv_l = 1.f / l;
+      __nv_bfloat16* orow = P.o + ((size_t)(row_valid ? i : 0) * P.Hq + h) * HD;
 #pragma unroll 1
       for (int c = 0; c < HD / 32; ++c) {
         float ov[32];
         ptx::tmem_ld32(t_o + c * 32, ov);
         ptx::tmem_wait_ld();
-        uint32_t ow[16];
+        if (row_valid) {
+          uint32_t ow[16];
 #pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          float2 v0 = make_float2(0.f, 0.f);
-          if (P.anchor)
-            v0 = ptx::unpack_bf16x2(__ldg(reinterpret_cast<const uint32_t*>(P.v + (size_t)g * HD + c * 32) + e));
-          const float a = (ov[2 * e] + w0 * v0.x) * inv_l;
-          const float b = (ov[2 * e + 1] + w0 * v0.y) * inv_l;
-          ow[e] = ptx::pack_bf16x2(a, b);
-        }
+          for (int e = 0; e < 16; ++e) {
+            float2 v0 = make_float2(0.f, 0.f);
+            if (P.anchor)
+              v0 = ptx::unpack_bf16x2(__ldg(reinterpret_cast<const uint32_t*>(P.v + (size_t)g * HD + c * 32) + e));
+            const float a = (ov[2 * e] + w0 * v0.x) * inv_l;
+            const float b = (ov[2 * e + 1] + w0 * v0.y) * inv_l;
+            ow[e] = ptx::pack_bf16x2(a, b);
+          }
+          uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {  // 16-byte chunk c8 of the row's 128-byte swizzled block
-          const int c8 = c * 4 + e;
-          *reinterpret_cast<uint4*>(sm.ostage[c8 >> 3] + sw128_chunk(r, c8 & 7)) =
-              make_uint4(ow[4 * e], ow[4 * e + 1], ow[4 * e + 2], ow[4 * e + 3]);
+          for (int e = 0; e < 4; ++e) dst[e] = make_uint4(ow[4 * e], ow[4 * e + 1], ow[4 * e + 2], ow[4 * e + 3]);
         }
       }
-      ptx::fence_proxy_async_smem();
-      ptx::mbar_arrive(&sm.ost_full);  // rows past T are staged too; the store drops them
       if (row_valid) P.lse[(size_t)h * P.T + i] = (m + log2f(l)) * 0.69314718055994531f;
       ++nq;
     }
@@ -564,8 +511,6 @@ aa_status launch_fwd(aa_plan_s* p, const void* q, const void* k, const void* v, 
   if ((st = make_tile_map(&tq, qr, p->T, p->Hq, HD)) != AA_OK) return st;
   if ((st = make_tile_map(&tk, kr, p->T, p->Hkv, HD)) != AA_OK) return st;
   if ((st = make_tile_map(&tv, v, p->T, p->Hkv, HD)) != AA_OK) return st;
-  CUtensorMap to;
-  if ((st = make_tile_map(&to, o, p->T, p->Hq, HD)) != AA_OK) return st;
   FwdParams P;
   P.kr = static_cast<const __nv_bfloat16*>(kr);
   P.v = static_cast<const __nv_bfloat16*>(v);
@@ -603,7 +548,7 @@ aa_status launch_fwd(aa_plan_s* p, const void* q, const void* k, const void* v, 
   if ((e = cudaMemsetAsync(P.next_item, 0, sizeof(int32_t), s)) != cudaSuccess)
     return cuda_fail(e, "resetting the forward work counter");
   const unsigned n_cta = (unsigned)std::min<size_t>(p->fwd_items.size(), (size_t)std::max(p->num_sms, 1));
-  attn_fwd_kernel<HD><<<n_cta, kThreads, smem, s>>>(tq, tk, tv, to, P);
+  attn_fwd_kernel<HD><<<n_cta, kThreads, smem, s>>>(tq, tk, tv, P);
   e = cudaGetLastError();
   return e == cudaSuccess ? AA_OK : cuda_fail(e, "attn_fwd_kernel launch");
 }

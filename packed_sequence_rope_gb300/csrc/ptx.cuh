@@ -107,18 +107,6 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* m, uin
       : "memory");
 }
 
-// 3-D tiled store of a shared-memory box {c, h, t} to global memory, tracked
-// by the issuing thread's bulk group (elements outside the tensor are not
-// written).
-__device__ __forceinline__ void tma_store_3d(const CUtensorMap* m, const void* src, int32_t c, int32_t h,
-                                             int32_t t) {
-  asm volatile(
-      "cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group"
-      " [%0, {%2, %3, %4}], [%1];" ::"l"(reinterpret_cast<uint64_t>(m)),
-      "r"(smem_u32(src)), "r"(c), "r"(h), "r"(t)
-      : "memory");
-}
-
 // 3-D tiled reduce-add of a shared-memory box into global memory (fp32 add),
 // tracked by the issuing thread's bulk group.
 __device__ __forceinline__ void tma_reduce_add_3d(const CUtensorMap* m, const void* src, int32_t c, int32_t h,
@@ -133,8 +121,6 @@ __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.comm
 // Wait until all committed bulk groups of this thread have finished reading
 // their shared-memory sources.
 __device__ __forceinline__ void bulk_wait_read0() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
-// Wait until all committed bulk groups of this thread have completed.
-__device__ __forceinline__ void bulk_wait0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
 // ------------------------------------------------------------------ tcgen05
 // Allocate `ncols` TMEM columns (power of two >= 32); the base address is
@@ -355,13 +341,6 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, int a_mn, in
 }
 
 // ------------------------------------------------------------------ misc
-// max(a, b, c) in one instruction.
-__device__ __forceinline__ float fmax3(float a, float b, float c) {
-  float r;
-  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
-  return r;
-}
-
 // 2^x with the hardware approximation (ex2.approx.ftz.f32).
 __device__ __forceinline__ float ex2(float x) {
   float y;
