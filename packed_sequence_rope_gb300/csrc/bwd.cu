@@ -705,16 +705,22 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           const int s = gs & 1;
           float* stage = reinterpret_cast<float*>((r >> 6) == 0 ? sm.q[s][0] : sm.dout[s][0]);
           const int ch = r & 63;
+          // query rows 0-63, then 64-127: the second pair of TMEM reads is
+          // signalled (dq_free) before its shared-memory stores, so the next
+          // dP^T product starts as soon as TMEM has been read
 #pragma unroll 1
-          for (int c = 0; c < 4; ++c) {
-            float dq[32];
-            ptx::tmem_ld32(t_dq + lane_off + c * 32, dq);
+          for (int hh = 0; hh < 2; ++hh) {
+            float dq[64];
+            ptx::tmem_ld32(t_dq + lane_off + hh * 64, dq);
+            ptx::tmem_ld32(t_dq + lane_off + hh * 64 + 32, dq + 32);
             ptx::tmem_wait_ld();
+            if (hh == 1) {
+              ptx::tc_fence_before();
+              ptx::mbar_arrive(&sm.dq_free);
+            }
 #pragma unroll
-            for (int e = 0; e < 32; ++e) stage[(c * 32 + e) * 64 + ch] = P.scale * dq[e];
+            for (int e = 0; e < 64; ++e) stage[(hh * 64 + e) * 64 + ch] = P.scale * dq[e];
           }
-          ptx::tc_fence_before();
-          ptx::mbar_arrive(&sm.dq_free);
           ptx::fence_proxy_async_smem();
           asm volatile("bar.sync 3, 128;" ::: "memory");
           if (r == 0) {
