@@ -190,9 +190,8 @@ def run_ours(args):
     # kernel, dq finalize (+ anchor)
     n_launch_per_step = 3 + 3 + (2 if args.bwd == "recompute" else 0) + (1 if mask == aa.MASK_ANCHOR else 0)
     if args.chunks > 0:
-        # gathers of q, k, v (fwd), scatters of o, lse; backward gathers of
-        # v, o, lse, dout and scatters of dq, dk, dv
-        n_launch_per_step += 5 + (7 if args.bwd == "from_fwd" else 9)
+        # the forward gathers v into its grouped order (aa_bwd gathers it again)
+        n_launch_per_step += 1 + (0 if args.bwd == "from_fwd" else 1)
 
     def step():
         plan.fwd(q, k, v, o, lse, fws)

@@ -137,9 +137,13 @@ aa_status aa_plan_with_theta(const aa_config* cfg, const int32_t* cu_doclens_hos
  * document's tokens in order, CONTINUOUS is the token index; pos_shift adds.
  * cfg->mask_mode must be ANCHOR or INTRA_DOC. aa_fwd / aa_bwd /
  * aa_bwd_from_fwd / aa_bwd_static_workspace / aa_rope_apply take and return
- * tensors in the caller's token order (the library groups the tokens by document, runs its
- * kernels and scatters the results back; the workspace sizes include the
- * grouped copies); aa_plan_metadata returns the caller's document ids and
+ * tensors in the caller's token order (the library's kernels run on the
+ * tokens grouped by document: the rotation passes read q and k through the
+ * grouping, V is gathered once per forward (aa_bwd_from_fwd reads the
+ * forward's copy), the backward's first kernel reads o, dout and lse through
+ * it and keeps a grouped dout, and every output is written at its caller
+ * position; the workspace sizes include those copies); aa_plan_metadata
+ * returns the caller's document ids and
  * positions; aa_plan_stats / aa_plan_work count the grouped layout's tiles.
  * aa_shift_diag refuses segment plans (AA_ERR_UNSUPPORTED). Errors: NULL
  * doc_of_token, doc_of_token[0] != 0, an id < 1 after it, or the aa_plan
@@ -189,8 +193,8 @@ aa_status aa_fwd(aa_plan_t plan, const void* q, const void* k, const void* v, vo
 
 /* Bytes of device scratch aa_fwd needs: the rotated K and Q, T*(Hkv+Hq)*D
  * bf16, which it leaves there for aa_bwd_from_fwd (none with AA_ROPE_NONE),
- * plus 256 bytes for the work counter; segment plans add their grouped
- * copies. */
+ * plus 256 bytes for the work counter; segment plans add a grouped copy of
+ * v (read again by aa_bwd_from_fwd) and, without RoPE, of q and k. */
 size_t aa_fwd_workspace_bytes(aa_plan_t plan);
 
 /* Bytes of device scratch aa_bwd needs (rotated Q and K, fp32 dQ
@@ -251,9 +255,8 @@ size_t aa_bwd_from_fwd_workspace_bytes(aa_plan_t plan);
  *    from cu_doclens with RoPE at D = 128 a query row needs about 1 KB
  *    (rotated Q and K and the fp32 dQ accumulator) and each query head
  *    0.25 MiB of anchor partials, so T * Hq up to about 55K query rows fit.
- *    Segment plans (aa_plan_segments) also need grouped copies of q, k, v,
- *    o, lse, dout and of the gradients, about twice as much per row, so
- *    roughly half as many rows fit.
+ *    Segment plans (aa_plan_segments) also need grouped copies of v and
+ *    dout (and, without RoPE, of q and k), so somewhat fewer rows fit.
  *  - The plan's device must be current. The first call on a device looks up
  *    the array's device address (cudaGetSymbolAddress) once and keeps it for
  *    the life of the process; make that first call before any stream capture

@@ -86,12 +86,17 @@ aa_status cuda_fail(cudaError_t e, const char* what);
 bool aligned16(const void* p);
 aa_status check_compute_plan(const aa_plan_s* p);
 // Rotate x [T, H, D] into y with the canonical tile rotation (no checks);
-// positions from `pos` (default: the plan's kernel-order pos_id).
+// positions from `pos` (default: the plan's kernel-order pos_id); y's row t
+// reads x's row src_rows[t] (default: row t).
 aa_status launch_rope(const aa_plan_s* p, const void* x, void* y, int H, int inverse, cudaStream_t s,
-                      const int32_t* pos = nullptr);
-// Forward kernels with an already-validated workspace (no segment handling).
+                      const int32_t* pos = nullptr, const int32_t* src_rows = nullptr);
+// Forward kernels with an already-validated workspace. rows (segment plans):
+// q and k are in the caller's order and are read through rows[t] (the caller
+// token at kernel position t) by the rotation passes, v is already in kernel
+// order, and o / lse are written at the caller's rows. NULL: all in kernel
+// order.
 aa_status launch_fwd_with_workspace(aa_plan_s* p, const void* q, const void* k, const void* v, void* o, float* lse,
-                                    void* workspace, cudaStream_t s);
+                                    void* workspace, cudaStream_t s, const int32_t* rows = nullptr);
 size_t fwd_base_workspace_bytes(const aa_plan_s* p);
 // Where a forward workspace keeps the rotated Q and K (kernel token order);
 // only meaningful when the plan rotates (rope_layout != AA_ROPE_NONE).
@@ -104,15 +109,23 @@ size_t seg_fwd_extra_bytes(const aa_plan_s* p);
 size_t seg_bwd_extra_bytes(const aa_plan_s* p, bool with_qk = true);
 aa_status seg_fwd(aa_plan_s* p, const void* q, const void* k, const void* v, void* o, float* lse, void* workspace,
                   cudaStream_t s);
-// qr / kr (both or neither): rotated Q and K already in the kernels' token
-// order, replacing q and k (which may then be NULL).
+// qr / kr / vg (all or none): rotated Q and K and the grouped V already in
+// the kernels' token order (a forward workspace), replacing q and k (which
+// may then be NULL) and v.
 aa_status seg_bwd(aa_plan_s* p, const void* q, const void* k, const void* v, const void* o, const float* lse,
                   const void* dout, void* dq, void* dk, void* dv, void* workspace, cudaStream_t s,
-                  const void* qr = nullptr, const void* kr = nullptr);
+                  const void* qr = nullptr, const void* kr = nullptr, const void* vg = nullptr);
+// Segment plans: where a forward workspace keeps the grouped V.
+const void* fwd_grouped_v(const aa_plan_s* p, const void* fwd_workspace);
 // Launch the backward kernels with an already-validated workspace pointer;
-// qr / kr as for seg_bwd.
+// qr / kr as for seg_bwd. rows (segment plans): q, k, o, lse, dout, dq, dk,
+// dv are in the caller's order (read and written through rows[t], the
+// caller token at kernel position t), v is in kernel order, and dout_g
+// receives dout in kernel order (written by the preprocess kernel, read by
+// the tile kernel). NULL: all in kernel order.
 aa_status launch_bwd_with_workspace(aa_plan_s* p, const void* q, const void* k, const void* v, const void* o,
                                     const float* lse, const void* dout, void* dq, void* dk, void* dv,
                                     void* workspace, cudaStream_t s, const void* qr = nullptr,
-                                    const void* kr = nullptr);
+                                    const void* kr = nullptr, const int32_t* rows = nullptr,
+                                    void* dout_g = nullptr);
 }  // namespace aa

@@ -82,7 +82,13 @@ __global__ void __launch_bounds__(kPrepThreads) bwd_prep_kernel(const __nv_bfloa
                                                                 const __nv_bfloat16* __restrict__ o,
                                                                 const __nv_bfloat16* __restrict__ dout,
                                                                 const float* __restrict__ lse, Workspace ws, int T,
-                                                                int Hq, int group, int anchor, float scale) {
+                                                                int Hq, int group, int anchor, float scale,
+                                                                const int32_t* __restrict__ rows,
+                                                                __nv_bfloat16* __restrict__ dout_g) {
+  // rows (segment plans): o, dout and lse are in the caller's order, kernel
+  // row i reading caller row rows[i]; dout_g then receives dout in kernel
+  // order for the tile kernel. q (rotated) and every output are in kernel
+  // order.
   constexpr int LPR = HD / 8;          // lanes per row
   constexpr int RPW = 32 / LPR;        // rows per warp pass
   constexpr int NW = kPrepThreads / 32;
@@ -138,16 +144,19 @@ __global__ void __launch_bounds__(kPrepThreads) bwd_prep_kernel(const __nv_bfloa
       const int i = ib + b * NW * RPW + sub;
       const bool valid = i < r_end;
       const size_t base = ((size_t)i * Hq + h) * HD + c0;
-      ro[b] = valid ? *reinterpret_cast<const uint4*>(o + base) : z;
-      rd[b] = valid ? *reinterpret_cast<const uint4*>(dout + base) : z;
+      const int is = valid && rows ? __ldg(rows + i) : i;  // the caller's row
+      const size_t sbase = ((size_t)is * Hq + h) * HD + c0;
+      ro[b] = valid ? *reinterpret_cast<const uint4*>(o + sbase) : z;
+      rd[b] = valid ? *reinterpret_cast<const uint4*>(dout + sbase) : z;
       rq[b] = valid && anchor ? *reinterpret_cast<const uint4*>(q + base) : z;
-      lse_v[b] = valid && anchor ? __ldg(lse + (size_t)h * T + i) : 0.f;
+      lse_v[b] = valid && anchor ? __ldg(lse + (size_t)h * T + is) : 0.f;
     }
 #pragma unroll
     for (int b = 0; b < NB; ++b) {
       const int i = ib + b * NW * RPW + sub;
       const bool valid = i < r_end;
       const size_t base = ((size_t)i * Hq + h) * HD + c0;
+      if (dout_g && valid) *reinterpret_cast<uint4*>(dout_g + base) = rd[b];
       float ov[8], dov[8];
       unpack8(ro[b], ov);
       unpack8(rd[b], dov);
@@ -280,6 +289,7 @@ struct BwdParams {
   Workspace ws;
   const int32_t* pos_id;
   const int32_t* key_hi;
+  const int32_t* rows;        // caller row of each kernel row for lse, dk, dv (NULL: the same row)
   const WorkItem* items;      // the work list, in the planner's order
   int32_t* next_item;         // next unclaimed index (zeroed by bwd_prep)
   int n_items;
@@ -613,8 +623,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       // Its TMEM reads all complete (tmem_wait_ld) before this thread's next
       // p_full arrival, which the next item's dV / dK~ products wait for.
       ptx::tc_fence_after();
-      __nv_bfloat16* dvrow = P.dv + ((size_t)(key_valid ? j : 0) * P.Hkv + w.g) * HD;
-      __nv_bfloat16* dkrow = P.dk + ((size_t)(key_valid ? j : 0) * P.Hkv + w.g) * HD;
+      const int j_out = key_valid ? (P.rows ? __ldg(P.rows + j) : j) : 0;
+      __nv_bfloat16* dvrow = P.dv + ((size_t)j_out * P.Hkv + w.g) * HD;
+      __nv_bfloat16* dkrow = P.dk + ((size_t)j_out * P.Hkv + w.g) * HD;
       const int pos = key_valid ? __ldg(P.pos_id + j) : 0;
       auto store32 = [&](__nv_bfloat16* row, int c0, const float* x) {
         uint4* dst = reinterpret_cast<uint4*>(row + c0);
@@ -774,7 +785,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const size_t hrow = (size_t)w.head(step, P.group) * P.T;
         for (int r = t; r < kTile; r += 64) {
           const int i = i0 + r;
-          sm.lse2[s][r] = i < P.T ? -__ldg(P.lse + hrow + i) * kLog2e : -INFINITY;  // -LSE log2(e)
+          const int is = i < P.T && P.rows ? __ldg(P.rows + i) : i;
+          sm.lse2[s][r] = i < P.T ? -__ldg(P.lse + hrow + is) * kLog2e : -INFINITY;  // -LSE log2(e)
           sm.dsum[s][r] = i < P.T ? -__ldg(P.ws.dsum + hrow + i) : 0.f;             // -D
         }
         ptx::mbar_arrive(&sm.q_ready[s]);
@@ -800,7 +812,9 @@ __global__ void __launch_bounds__(256) dq_finalize_kernel(const float* __restric
                                                           const int32_t* __restrict__ pos_id,
                                                           const float2* __restrict__ hi_tab,
                                                           const float2* __restrict__ lo_tab, int rows, int H,
-                                                          int layout) {
+                                                          int layout, const int32_t* __restrict__ out_tok) {
+  // out_tok (segment plans): the caller token of each kernel token, where
+  // its dq row is written (NULL: the same token)
   constexpr int half = HD / 2, quads = half / 4;
   constexpr int RPB = 256 / quads;          // rows per block sub-pass
   constexpr int PASS = kFinNB * RPB;        // rows per pass: at most PASS tokens
@@ -832,7 +846,7 @@ __global__ void __launch_bounds__(256) dq_finalize_kernel(const float* __restric
     for (int b = 0; b < kFinNB; ++b) {
       const int row = r0 + b * RPB + rsub;
       if (row >= rows) break;
-      __nv_bfloat16* y = dq + (size_t)row * HD;
+      __nv_bfloat16* y = dq + (out_tok ? ((size_t)__ldg(out_tok + row / H) * H + row % H) : (size_t)row) * HD;
       float x0[4], x1[4];
       if (layout == 1) {
         x0[0] = u[b].x; x0[1] = u[b].y; x0[2] = u[b].z; x0[3] = u[b].w;
@@ -920,7 +934,7 @@ __global__ void __launch_bounds__(kAnchorThreads)
 template <int HD>
 aa_status launch_bwd(aa_plan_s* p, const void* q, const void* k, const void* v, const void* o, const float* lse,
                      const void* dout, void* dq, void* dk, void* dv, void* workspace, cudaStream_t s,
-                     const void* qr_in, const void* kr_in) {
+                     const void* qr_in, const void* kr_in, const int32_t* rows, void* dout_g) {
   size_t need = 0;
   const bool given = qr_in != nullptr;  // rotated Q and K from a forward workspace
   Workspace ws = carve(workspace, p, &need, !given);
@@ -931,8 +945,8 @@ aa_status launch_bwd(aa_plan_s* p, const void* q, const void* k, const void* v, 
   const void* qr = given ? qr_in : q;
   const void* kr = given ? kr_in : k;
   if (rope_layout != AA_ROPE_NONE && !given) {
-    aa_status rs = launch_rope(p, q, ws.qr, p->Hq, 0, s);
-    if (rs == AA_OK) rs = launch_rope(p, k, ws.kr, p->Hkv, 0, s);
+    aa_status rs = launch_rope(p, q, ws.qr, p->Hq, 0, s, nullptr, rows);
+    if (rs == AA_OK) rs = launch_rope(p, k, ws.kr, p->Hkv, 0, s, nullptr, rows);
     if (rs != AA_OK) return rs;
     qr = ws.qr;
     kr = ws.kr;
@@ -940,7 +954,8 @@ aa_status launch_bwd(aa_plan_s* p, const void* q, const void* k, const void* v, 
   bwd_prep_kernel<HD><<<dim3(p->Hq, kPrepChunks), kPrepThreads, 0, s>>>(
       static_cast<const __nv_bfloat16*>(qr), static_cast<const __nv_bfloat16*>(kr),
       static_cast<const __nv_bfloat16*>(v), static_cast<const __nv_bfloat16*>(o),
-      static_cast<const __nv_bfloat16*>(dout), lse, ws, p->T, p->Hq, p->group, p->anchor ? 1 : 0, p->scale);
+      static_cast<const __nv_bfloat16*>(dout), lse, ws, p->T, p->Hq, p->group, p->anchor ? 1 : 0, p->scale, rows,
+      rows ? static_cast<__nv_bfloat16*>(dout_g) : nullptr);
   if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(e, "bwd_prep_kernel launch");
 
   CUtensorMap tq, tk, tv, tdo;
@@ -948,7 +963,7 @@ aa_status launch_bwd(aa_plan_s* p, const void* q, const void* k, const void* v, 
   if ((st = make_tile_map(&tq, qr, p->T, p->Hq, HD)) != AA_OK) return st;
   if ((st = make_tile_map(&tk, kr, p->T, p->Hkv, HD)) != AA_OK) return st;
   if ((st = make_tile_map(&tv, v, p->T, p->Hkv, HD)) != AA_OK) return st;
-  if ((st = make_tile_map(&tdo, dout, p->T, p->Hq, HD)) != AA_OK) return st;
+  if ((st = make_tile_map(&tdo, rows ? dout_g : dout, p->T, p->Hq, HD)) != AA_OK) return st;
   CUtensorMap tdq;
   if ((st = make_f32_map(&tdq, ws.dq_acc, p->T, p->Hq, HD, 64, kTile)) != AA_OK) return st;
   BwdParams P;
@@ -958,6 +973,7 @@ aa_status launch_bwd(aa_plan_s* p, const void* q, const void* k, const void* v, 
   P.ws = ws;
   P.pos_id = p->dev.pos_id;
   P.key_hi = p->dev.key_hi;
+  P.rows = rows;
   P.items = p->dev.bwd_items;
   P.next_item = ws.next_item;
   P.n_items = (int)p->bwd_items.size();
@@ -999,12 +1015,13 @@ aa_status launch_bwd(aa_plan_s* p, const void* q, const void* k, const void* v, 
                ? n
                : 4;
   });
-  const int rows = p->T * p->Hq;  // below 2^31: the plan checks T * Hq
+  const int rows_total = p->T * p->Hq;  // below 2^31: the plan checks T * Hq
   const int per_block = kFinNB * (256 / (HD / 8));
-  const int64_t blocks = std::min<int64_t>((rows + per_block - 1) / per_block, (int64_t)p->num_sms * std::max(occ, 1));
+  const int64_t blocks =
+      std::min<int64_t>((rows_total + per_block - 1) / per_block, (int64_t)p->num_sms * std::max(occ, 1));
   dq_finalize_kernel<HD><<<(unsigned)blocks, 256, 0, s>>>(ws.dq_acc, static_cast<__nv_bfloat16*>(dq),
-                                                          p->dev.pos_id, p->dev.rope_hi, p->dev.rope_lo, rows,
-                                                          p->Hq, rope_layout);
+                                                          p->dev.pos_id, p->dev.rope_hi, p->dev.rope_lo, rows_total,
+                                                          p->Hq, rope_layout, rows);
   if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(e, "dq_finalize_kernel launch");
   if (p->anchor) {
     anchor_finalize_kernel<<<p->Hkv, kAnchorThreads, (2 * kAnchorThreads + 2 * HD) * sizeof(float), s>>>(
@@ -1019,9 +1036,10 @@ aa_status launch_bwd(aa_plan_s* p, const void* q, const void* k, const void* v, 
 
 aa_status launch_bwd_with_workspace(aa_plan_s* p, const void* q, const void* k, const void* v, const void* o,
                                     const float* lse, const void* dout, void* dq, void* dk, void* dv,
-                                    void* workspace, cudaStream_t s, const void* qr, const void* kr) {
-  return p->D == 128 ? launch_bwd<128>(p, q, k, v, o, lse, dout, dq, dk, dv, workspace, s, qr, kr)
-                     : launch_bwd<64>(p, q, k, v, o, lse, dout, dq, dk, dv, workspace, s, qr, kr);
+                                    void* workspace, cudaStream_t s, const void* qr, const void* kr,
+                                    const int32_t* rows, void* dout_g) {
+  return p->D == 128 ? launch_bwd<128>(p, q, k, v, o, lse, dout, dq, dk, dv, workspace, s, qr, kr, rows, dout_g)
+                     : launch_bwd<64>(p, q, k, v, o, lse, dout, dq, dk, dv, workspace, s, qr, kr, rows, dout_g);
 }
 
 size_t bwd_base_workspace_bytes(const aa_plan_s* p, bool with_rot) {
@@ -1085,6 +1103,8 @@ extern "C" aa_status aa_bwd_from_fwd(aa_plan_t p, const void* fwd_workspace, con
   const void *qr = nullptr, *kr = nullptr;
   fwd_rotated_operands(p, fwd_workspace, &qr, &kr);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  if (p->segmented) return seg_bwd(p, nullptr, nullptr, v, o, lse, dout, dq, dk, dv, workspace, s, qr, kr);
+  if (p->segmented)
+    return seg_bwd(p, nullptr, nullptr, v, o, lse, dout, dq, dk, dv, workspace, s, qr, kr,
+                   fwd_grouped_v(p, fwd_workspace));
   return launch_bwd_with_workspace(p, nullptr, nullptr, v, o, lse, dout, dq, dk, dv, workspace, s, qr, kr);
 }

@@ -68,6 +68,7 @@ struct FwdParams {
   const int32_t* pos_id;
   const int32_t* row_lo;
   const int32_t* qtile_klo;
+  const int32_t* out_rows;   // caller row of each kernel row for O / LSE (NULL: the same row)
   const WorkItem* items;     // the work list, longest first
   int32_t* next_item;        // next unclaimed index (zeroed before the launch)
   int n_items;
@@ -151,7 +152,9 @@ __device__ __forceinline__ int read_fwd_item(Smem& sm, int li, const FwdParams& 
 // abort in one role never strands another at a named barrier; inside a warp
 // each wait's outcome is made uniform by a vote before any warp-collective
 // step, so no lane leaves a loop that the rest of its warp stays in.
-template <int HD>
+// kRows: O and LSE rows go to P.out_rows (segment plans); the contiguous
+// instantiation carries no row map.
+template <int HD, bool kRows>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const FwdParams P) {
@@ -453,7 +456,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::tc_fence_after();
       const float w0 = P.anchor ? exp2f(s0 - m) : 0.f;
       const float inv_l = 1.f / l;
-      __nv_bfloat16* orow = P.o + ((size_t)(row_valid ? i : 0) * P.Hq + h) * HD;
+      const int i_out = !row_valid ? 0 : kRows ? __ldg(P.out_rows + i) : i;
+      __nv_bfloat16* orow = P.o + ((size_t)i_out * P.Hq + h) * HD;
 #pragma unroll 1
       for (int c = 0; c < HD / 32; ++c) {
         float ov[32];
@@ -475,7 +479,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int e = 0; e < 4; ++e) dst[e] = make_uint4(ow[4 * e], ow[4 * e + 1], ow[4 * e + 2], ow[4 * e + 3]);
         }
       }
-      if (row_valid) P.lse[(size_t)h * P.T + i] = (m + log2f(l)) * 0.69314718055994531f;
+      if (row_valid) P.lse[(size_t)h * P.T + i_out] = (m + log2f(l)) * 0.69314718055994531f;
       ++nq;
     }
   }
@@ -498,15 +502,15 @@ int32_t* fwd_counter(const aa_plan_s* p, void* workspace) {
 
 template <int HD>
 aa_status launch_fwd(aa_plan_s* p, const void* q, const void* k, const void* v, void* o, float* lse,
-                     void* workspace, cudaStream_t s) {
+                     void* workspace, cudaStream_t s, const int32_t* rows) {
   CUtensorMap tq, tk, tv;
   aa_status st;
   const void* qr = q;
   const void* kr = k;
   if (p->cfg.rope_layout != AA_ROPE_NONE) {
     fwd_rotated_operands(p, workspace, &qr, &kr);  // they stay there for aa_bwd_from_fwd
-    if ((st = launch_rope(p, k, workspace, p->Hkv, 0, s)) != AA_OK) return st;
-    if ((st = launch_rope(p, q, const_cast<void*>(qr), p->Hq, 0, s)) != AA_OK) return st;
+    if ((st = launch_rope(p, k, workspace, p->Hkv, 0, s, nullptr, rows)) != AA_OK) return st;
+    if ((st = launch_rope(p, q, const_cast<void*>(qr), p->Hq, 0, s, nullptr, rows)) != AA_OK) return st;
   }
   if ((st = make_tile_map(&tq, qr, p->T, p->Hq, HD)) != AA_OK) return st;
   if ((st = make_tile_map(&tk, kr, p->T, p->Hkv, HD)) != AA_OK) return st;
@@ -519,6 +523,7 @@ aa_status launch_fwd(aa_plan_s* p, const void* q, const void* k, const void* v, 
   P.pos_id = p->dev.pos_id;
   P.row_lo = p->dev.row_lo;
   P.qtile_klo = p->dev.qtile_klo;
+  P.out_rows = rows;
   P.items = p->dev.fwd_items;
   P.next_item = fwd_counter(p, workspace);
   P.n_items = (int)p->fwd_items.size();
@@ -539,7 +544,11 @@ aa_status launch_fwd(aa_plan_s* p, const void* q, const void* k, const void* v, 
   static std::once_flag attr_once[kMaxDevices];
   static cudaError_t attr_result[kMaxDevices];
   cudaError_t e = once_per_device(attr_once, attr_result, p->device, [&] {
-    return cudaFuncSetAttribute(attn_fwd_kernel<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    cudaError_t r = cudaFuncSetAttribute(attn_fwd_kernel<HD, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)smem);
+    if (r == cudaSuccess)
+      r = cudaFuncSetAttribute(attn_fwd_kernel<HD, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    return r;
   });
   if (e != cudaSuccess) return cuda_fail(e, "attn_fwd_kernel smem attribute");
   // persistent: one CTA per SM (fewer for short work lists), claiming the
@@ -548,7 +557,10 @@ aa_status launch_fwd(aa_plan_s* p, const void* q, const void* k, const void* v, 
   if ((e = cudaMemsetAsync(P.next_item, 0, sizeof(int32_t), s)) != cudaSuccess)
     return cuda_fail(e, "resetting the forward work counter");
   const unsigned n_cta = (unsigned)std::min<size_t>(p->fwd_items.size(), (size_t)std::max(p->num_sms, 1));
-  attn_fwd_kernel<HD><<<n_cta, kThreads, smem, s>>>(tq, tk, tv, P);
+  if (rows)
+    attn_fwd_kernel<HD, true><<<n_cta, kThreads, smem, s>>>(tq, tk, tv, P);
+  else
+    attn_fwd_kernel<HD, false><<<n_cta, kThreads, smem, s>>>(tq, tk, tv, P);
   e = cudaGetLastError();
   return e == cudaSuccess ? AA_OK : cuda_fail(e, "attn_fwd_kernel launch");
 }
@@ -566,9 +578,9 @@ size_t fwd_base_workspace_bytes(const aa_plan_s* p) {
 }
 
 aa_status launch_fwd_with_workspace(aa_plan_s* p, const void* q, const void* k, const void* v, void* o, float* lse,
-                                    void* workspace, cudaStream_t s) {
-  return p->D == 128 ? launch_fwd<128>(p, q, k, v, o, lse, workspace, s)
-                     : launch_fwd<64>(p, q, k, v, o, lse, workspace, s);
+                                    void* workspace, cudaStream_t s, const int32_t* rows) {
+  return p->D == 128 ? launch_fwd<128>(p, q, k, v, o, lse, workspace, s, rows)
+                     : launch_fwd<64>(p, q, k, v, o, lse, workspace, s, rows);
 }
 
 }  // namespace aa

@@ -17,20 +17,25 @@ namespace aa {
 
 // Accessor over one head of a [T, H, D] bf16 tensor in global memory, rows
 // relative to a 128-row tile; reads from x, writes to y (which may equal x).
-template <int HD, int L>
+template <int HD, int L, bool kRows>
 struct GlobalTile {
   using Raw = QuadRaw;
   const __nv_bfloat16* x;
   __nv_bfloat16* y;
   int row0, H, head;
+  const int32_t* src_rows;  // x row of each y row (kRows only)
   __device__ __forceinline__ size_t off(int r, int e) const { return ((size_t)(row0 + r) * H + head) * HD + e; }
+  __device__ __forceinline__ size_t src_off(int r, int e) const {
+    const int row = kRows ? __ldg(src_rows + row0 + r) : row0 + r;
+    return ((size_t)row * H + head) * HD + e;
+  }
   __device__ __forceinline__ QuadRaw load_raw(int r, int qd) const {
     QuadRaw q;
     if (L == 0) {
-      q.w = *reinterpret_cast<const uint4*>(x + off(r, 8 * qd));
+      q.w = *reinterpret_cast<const uint4*>(x + src_off(r, 8 * qd));
     } else {
-      const uint2 a = *reinterpret_cast<const uint2*>(x + off(r, 4 * qd));
-      const uint2 b = *reinterpret_cast<const uint2*>(x + off(r, HD / 2 + 4 * qd));
+      const uint2 a = *reinterpret_cast<const uint2*>(x + src_off(r, 4 * qd));
+      const uint2 b = *reinterpret_cast<const uint2*>(x + src_off(r, HD / 2 + 4 * qd));
       q.w = make_uint4(a.x, a.y, b.x, b.y);
     }
     return q;
@@ -49,14 +54,14 @@ struct GlobalTile {
 
 // One CTA of 128 threads per (128-row tile, head): the canonical tile
 // rotation of kcommon.cuh, straight from and to global memory.
-template <int HD, int L>
+template <int HD, int L, bool kRows>
 __global__ void __launch_bounds__(128) rope_apply_kernel(const __nv_bfloat16* __restrict__ x,
                                                          __nv_bfloat16* y, const int32_t* __restrict__ pos_id,
                                                          const float2* __restrict__ hi_tab,
                                                          const float2* __restrict__ lo_tab,
                                                          const float2* __restrict__ step_tab, int T, int H,
-                                                         int inverse) {
-  GlobalTile<HD, L> tile{x, y, (int)blockIdx.x * kTile, H, (int)blockIdx.y};
+                                                         int inverse, const int32_t* __restrict__ src_rows) {
+  GlobalTile<HD, L, kRows> tile{x, y, (int)blockIdx.x * kTile, H, (int)blockIdx.y, src_rows};
   RopeUnits<HD, 128> st;
   st.begin(tile.row0, T, pos_id, inverse != 0, hi_tab, lo_tab, threadIdx.x);
   st.run(tile, inverse != 0, hi_tab, lo_tab, step_tab, threadIdx.x);
@@ -64,16 +69,14 @@ __global__ void __launch_bounds__(128) rope_apply_kernel(const __nv_bfloat16* __
 
 template <int HD>
 void launch_rope_apply(const aa_plan_s* p, const void* x, void* y, int H, int inverse, cudaStream_t s,
-                       const int32_t* pos) {
+                       const int32_t* pos, const int32_t* src_rows) {
   const dim3 grid((unsigned)p->n_tiles, (unsigned)H);
   const auto* xi = static_cast<const __nv_bfloat16*>(x);
   auto* yo = static_cast<__nv_bfloat16*>(y);
-  if (p->cfg.rope_layout == AA_ROPE_ADJACENT)
-    rope_apply_kernel<HD, 0><<<grid, 128, 0, s>>>(xi, yo, pos, p->dev.rope_hi, p->dev.rope_lo, p->dev.rope_step,
-                                                  p->T, H, inverse);
-  else
-    rope_apply_kernel<HD, 1><<<grid, 128, 0, s>>>(xi, yo, pos, p->dev.rope_hi, p->dev.rope_lo, p->dev.rope_step,
-                                                  p->T, H, inverse);
+  const bool adj = p->cfg.rope_layout == AA_ROPE_ADJACENT;
+  auto k = adj ? (src_rows ? rope_apply_kernel<HD, 0, true> : rope_apply_kernel<HD, 0, false>)
+               : (src_rows ? rope_apply_kernel<HD, 1, true> : rope_apply_kernel<HD, 1, false>);
+  k<<<grid, 128, 0, s>>>(xi, yo, pos, p->dev.rope_hi, p->dev.rope_lo, p->dev.rope_step, p->T, H, inverse, src_rows);
 }
 
 static PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {
@@ -105,12 +108,12 @@ aa_status make_tile_map(CUtensorMap* m, const void* base, int T, int H, int D) {
 }
 
 aa_status launch_rope(const aa_plan_s* p, const void* x, void* y, int H, int inverse, cudaStream_t s,
-                      const int32_t* pos) {
+                      const int32_t* pos, const int32_t* src_rows) {
   if (!pos) pos = p->dev.pos_id;
   if (p->D == 128)
-    launch_rope_apply<128>(p, x, y, H, inverse, s, pos);
+    launch_rope_apply<128>(p, x, y, H, inverse, s, pos, src_rows);
   else
-    launch_rope_apply<64>(p, x, y, H, inverse, s, pos);
+    launch_rope_apply<64>(p, x, y, H, inverse, s, pos, src_rows);
   cudaError_t e = cudaGetLastError();
   return e == cudaSuccess ? AA_OK : cuda_fail(e, "rope_apply_kernel launch");
 }

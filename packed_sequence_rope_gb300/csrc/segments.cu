@@ -7,9 +7,13 @@
 // they sit in the packing. The planner groups the tokens by document (stable:
 // the order inside a document is kept), which turns the problem into an
 // ordinary contiguous packing with the same visible pairs and the same
-// positions; aa_fwd / aa_bwd gather their inputs into that order, run the
-// usual kernels, and scatter the outputs back. The gathers and scatters are
-// HBM-bound copies of whole token rows.
+// positions. The kernels run on that grouped order and meet the caller's
+// order only at their edges: the rotation passes read q and k through the
+// permutation, the backward's preprocess kernel reads o, dout and lse through
+// it (and leaves a grouped dout for the tile kernel), and every output row
+// (O, LSE, dq, dk, dv) is written at its caller position by the kernel that
+// produces it. Only V is gathered, once per forward (the training step's
+// backward reads the forward's copy).
 #include "kcommon.cuh"
 
 namespace aa {
@@ -17,119 +21,100 @@ namespace {
 
 inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
-// Row permutation of a [T, row] tensor in 16-byte vectors: gather
-// (dst[t] = src[perm[t]]) or scatter (dst[perm[t]] = src[t]).
-__global__ void __launch_bounds__(256) permute_rows_kernel(const uint4* __restrict__ src, uint4* __restrict__ dst,
-                                                           const int32_t* __restrict__ perm, int T, int row_vecs,
-                                                           int scatter) {
+// Row gather of a [T, row] tensor in 16-byte vectors: dst[t] = src[perm[t]].
+__global__ void __launch_bounds__(256) gather_rows_kernel(const uint4* __restrict__ src, uint4* __restrict__ dst,
+                                                          const int32_t* __restrict__ perm, int T, int row_vecs) {
   const int64_t n = (int64_t)T * row_vecs;
   for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < n; e += (int64_t)gridDim.x * blockDim.x) {
     const int t = (int)(e / row_vecs), c = (int)(e - (int64_t)t * row_vecs);
-    const int64_t o = (int64_t)__ldg(perm + t) * row_vecs + c;
-    if (scatter)
-      dst[o] = src[e];
-    else
-      dst[e] = src[o];
+    dst[e] = src[(int64_t)__ldg(perm + t) * row_vecs + c];
   }
 }
 
-// Column permutation of a [H, T] fp32 array (the LSE rows).
-__global__ void __launch_bounds__(256) permute_cols_kernel(const float* __restrict__ src, float* __restrict__ dst,
-                                                           const int32_t* __restrict__ perm, int T, int H,
-                                                           int scatter) {
-  const int64_t n = (int64_t)T * H;
-  for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < n; e += (int64_t)gridDim.x * blockDim.x) {
-    const int h = (int)(e / T), t = (int)(e - (int64_t)h * T);
-    const int64_t o = (int64_t)h * T + __ldg(perm + t);
-    if (scatter)
-      dst[o] = src[e];
-    else
-      dst[e] = src[o];
-  }
-}
-
-aa_status permute_rows(const aa_plan_s* p, const void* src, void* dst, int H, int scatter, cudaStream_t s) {
+aa_status gather_rows(const aa_plan_s* p, const void* src, void* dst, int H, cudaStream_t s) {
   const int row_vecs = H * p->D * 2 / 16;
   const int64_t n = (int64_t)p->T * row_vecs;
   const int64_t blocks = std::min<int64_t>((n + 255) / 256, (int64_t)p->num_sms * 8);
-  permute_rows_kernel<<<(unsigned)blocks, 256, 0, s>>>(static_cast<const uint4*>(src), static_cast<uint4*>(dst),
-                                                       p->dev.perm, p->T, row_vecs, scatter);
+  gather_rows_kernel<<<(unsigned)blocks, 256, 0, s>>>(static_cast<const uint4*>(src), static_cast<uint4*>(dst),
+                                                      p->dev.perm, p->T, row_vecs);
   cudaError_t e = cudaGetLastError();
-  return e == cudaSuccess ? AA_OK : cuda_fail(e, "permute_rows_kernel launch");
-}
-
-aa_status permute_cols(const aa_plan_s* p, const float* src, float* dst, int scatter, cudaStream_t s) {
-  const int64_t n = (int64_t)p->T * p->Hq;
-  const int64_t blocks = std::min<int64_t>((n + 255) / 256, (int64_t)p->num_sms * 8);
-  permute_cols_kernel<<<(unsigned)blocks, 256, 0, s>>>(src, dst, p->dev.perm, p->T, p->Hq, scatter);
-  cudaError_t e = cudaGetLastError();
-  return e == cudaSuccess ? AA_OK : cuda_fail(e, "permute_cols_kernel launch");
+  return e == cudaSuccess ? AA_OK : cuda_fail(e, "gather_rows_kernel launch");
 }
 
 size_t tensor_bytes(const aa_plan_s* p, int H) { return align256((size_t)p->T * H * p->D * 2); }
-size_t lse_bytes(const aa_plan_s* p) { return align256((size_t)p->Hq * p->T * 4); }
 
 }  // namespace
 
-// Forward extras: grouped Q, K, V, O and LSE.
+// Forward extras: the grouped V, which stays there for aa_bwd_from_fwd (and,
+// without RoPE, grouped Q and K: no rotation pass reads them through the
+// permutation then).
 size_t seg_fwd_extra_bytes(const aa_plan_s* p) {
-  return 2 * tensor_bytes(p, p->Hq) + 2 * tensor_bytes(p, p->Hkv) + lse_bytes(p);
+  const bool rope = p->cfg.rope_layout != AA_ROPE_NONE;
+  return tensor_bytes(p, p->Hkv) + (rope ? 0 : tensor_bytes(p, p->Hq) + tensor_bytes(p, p->Hkv));
 }
 
-// Backward extras: grouped Q, K (unless the rotated ones are given), V, O,
-// dO, LSE and dQ, dK, dV.
+const void* fwd_grouped_v(const aa_plan_s* p, const void* fwd_workspace) {
+  return static_cast<const uint8_t*>(fwd_workspace) + fwd_base_workspace_bytes(p);
+}
+
+// Backward extras: the grouped dO (written by the preprocess kernel) and,
+// unless the forward's grouped V is given (aa_bwd_from_fwd), the grouped V;
+// without RoPE also grouped Q and K.
 size_t seg_bwd_extra_bytes(const aa_plan_s* p, bool with_qk) {
-  const int n = with_qk ? 4 : 3;
-  return n * tensor_bytes(p, p->Hq) + n * tensor_bytes(p, p->Hkv) + lse_bytes(p);
+  const bool rope = p->cfg.rope_layout != AA_ROPE_NONE;
+  size_t n = tensor_bytes(p, p->Hq);
+  if (with_qk) n += tensor_bytes(p, p->Hkv);
+  if (with_qk && !rope) n += tensor_bytes(p, p->Hq) + tensor_bytes(p, p->Hkv);
+  return n;
 }
 
+// The kernels run on the grouped token order. Q and K are read through the
+// permutation by the rotation passes (or gathered, without RoPE), V is
+// gathered once per forward, and every output (O, LSE, dq, dk, dv) is written
+// straight to the caller's rows by the kernel that produces it.
 aa_status seg_fwd(aa_plan_s* p, const void* q, const void* k, const void* v, void* o, float* lse, void* workspace,
                   cudaStream_t s) {
   uint8_t* w = static_cast<uint8_t*>(workspace) + fwd_base_workspace_bytes(p);
   const size_t tq = tensor_bytes(p, p->Hq), tk = tensor_bytes(p, p->Hkv);
-  void* qg = w;
-  void* kg = w + tq;
-  void* vg = w + tq + tk;
-  void* og = w + tq + 2 * tk;
-  float* lg = reinterpret_cast<float*>(w + 2 * tq + 2 * tk);
+  void* vg = w;
   aa_status st;
-  if ((st = permute_rows(p, q, qg, p->Hq, 0, s)) != AA_OK || (st = permute_rows(p, k, kg, p->Hkv, 0, s)) != AA_OK ||
-      (st = permute_rows(p, v, vg, p->Hkv, 0, s)) != AA_OK)
-    return st;
-  if ((st = launch_fwd_with_workspace(p, qg, kg, vg, og, lg, workspace, s)) != AA_OK) return st;
-  if ((st = permute_rows(p, og, o, p->Hq, 1, s)) != AA_OK) return st;
-  return permute_cols(p, lg, lse, 1, s);
+  if ((st = gather_rows(p, v, vg, p->Hkv, s)) != AA_OK) return st;
+  if (p->cfg.rope_layout == AA_ROPE_NONE) {
+    void* qg = w + tk;
+    void* kg = w + tk + tq;
+    if ((st = gather_rows(p, q, qg, p->Hq, s)) != AA_OK || (st = gather_rows(p, k, kg, p->Hkv, s)) != AA_OK)
+      return st;
+    q = qg;
+    k = kg;
+  }
+  return launch_fwd_with_workspace(p, q, k, vg, o, lse, workspace, s, p->dev.perm);
 }
 
 aa_status seg_bwd(aa_plan_s* p, const void* q, const void* k, const void* v, const void* o, const float* lse,
                   const void* dout, void* dq, void* dk, void* dv, void* workspace, cudaStream_t s, const void* qr,
-                  const void* kr) {
-  // qr / kr: the forward's rotated Q and K, already in the grouped order
+                  const void* kr, const void* vg_in) {
+  // qr / kr / vg_in: the forward's rotated Q, K and grouped V, already in the
+  // grouped order
   const bool given = qr != nullptr;
   uint8_t* w = static_cast<uint8_t*>(workspace) + bwd_base_workspace_bytes(p, !given);
   const size_t tq = tensor_bytes(p, p->Hq), tk = tensor_bytes(p, p->Hkv);
-  void* og = w;
-  void* dog = w + tq;
-  void* dqg = w + 2 * tq;
-  void* vg = w + 3 * tq;
-  void* dkg = w + 3 * tq + tk;
-  void* dvg = w + 3 * tq + 2 * tk;
-  float* lg = reinterpret_cast<float*>(w + 3 * tq + 3 * tk);
-  void* qg = w + 3 * tq + 3 * tk + lse_bytes(p);  // only without qr / kr
-  void* kg = static_cast<uint8_t*>(qg) + tq;
+  void* dog = w;
   aa_status st;
-  if (!given &&
-      ((st = permute_rows(p, q, qg, p->Hq, 0, s)) != AA_OK || (st = permute_rows(p, k, kg, p->Hkv, 0, s)) != AA_OK))
-    return st;
-  if ((st = permute_rows(p, v, vg, p->Hkv, 0, s)) != AA_OK || (st = permute_rows(p, o, og, p->Hq, 0, s)) != AA_OK ||
-      (st = permute_rows(p, dout, dog, p->Hq, 0, s)) != AA_OK || (st = permute_cols(p, lse, lg, 0, s)) != AA_OK)
-    return st;
-  st = given ? launch_bwd_with_workspace(p, nullptr, nullptr, vg, og, lg, dog, dqg, dkg, dvg, workspace, s, qr, kr)
-             : launch_bwd_with_workspace(p, qg, kg, vg, og, lg, dog, dqg, dkg, dvg, workspace, s);
-  if (st != AA_OK) return st;
-  if ((st = permute_rows(p, dqg, dq, p->Hq, 1, s)) != AA_OK || (st = permute_rows(p, dkg, dk, p->Hkv, 1, s)) != AA_OK)
-    return st;
-  return permute_rows(p, dvg, dv, p->Hkv, 1, s);
+  const void* vg = vg_in;
+  if (!given) {
+    void* vgw = w + tq;
+    if ((st = gather_rows(p, v, vgw, p->Hkv, s)) != AA_OK) return st;
+    vg = vgw;
+    if (p->cfg.rope_layout == AA_ROPE_NONE) {
+      void* qg = w + tq + tk;
+      void* kg = w + 2 * tq + tk;
+      if ((st = gather_rows(p, q, qg, p->Hq, s)) != AA_OK || (st = gather_rows(p, k, kg, p->Hkv, s)) != AA_OK)
+        return st;
+      q = qg;
+      k = kg;
+    }
+  }
+  return launch_bwd_with_workspace(p, q, k, vg, o, lse, dout, dq, dk, dv, workspace, s, qr, kr, p->dev.perm, dog);
 }
 
 }  // namespace aa

@@ -110,8 +110,7 @@ def test_compute_on_host_only_plan_is_refused(aa):
 def test_workspace_sizes(aa, layout, segmented):
     # Forward: rotated K then rotated Q (bf16), nothing without RoPE, then a
     # 256-byte work counter; the
-    # backward from the forward's rotated operands needs no copies of them,
-    # and segment plans add grouped copies of their tensors.
+    # backward from the forward's rotated operands needs no copies of them.
     T, Hq, Hkv, D = 1000, 4, 2, 128
     al = lambda n: (n + 255) // 256 * 256
     doc = np.repeat(np.arange(1, 5, dtype=np.int32), [250, 250, 250, 249]) if segmented else None
@@ -122,11 +121,15 @@ def test_workspace_sizes(aa, layout, segmented):
         fwd, bwd, from_fwd = (int(L.aa_fwd_workspace_bytes(p._h)), int(L.aa_bwd_workspace_bytes(p._h)),
                               int(L.aa_bwd_from_fwd_workspace_bytes(p._h)))
     rot = al(T * Hkv * D * 2) + al(T * Hq * D * 2) if layout != orc.ROPE_NONE else 0
-    seg_fwd = 2 * al(T * Hq * D * 2) + 2 * al(T * Hkv * D * 2) + al(Hq * T * 4) if segmented else 0
+    tq, tk = al(T * Hq * D * 2), al(T * Hkv * D * 2)
+    # segment plans: the forward keeps a grouped V (and, without RoPE, grouped
+    # Q and K, which no rotation pass reads through the permutation)
+    seg_fwd = (tk + (0 if layout != orc.ROPE_NONE else tq + tk)) if segmented else 0
     assert fwd == rot + 256 + seg_fwd
-    # the two backward entry points differ by the rotated copies (and, for
-    # segment plans, by the grouped copies of q and k)
-    seg_qk = al(T * Hq * D * 2) + al(T * Hkv * D * 2) if segmented else 0
+    # the two backward entry points differ by the rotated copies and, for
+    # segment plans, by the grouped V (from the forward in aa_bwd_from_fwd)
+    # and, without RoPE, grouped q and k; both hold the grouped dO
+    seg_qk = (tk + (0 if layout != orc.ROPE_NONE else tq + tk)) if segmented else 0
     assert bwd - from_fwd == rot + seg_qk
 
 
