@@ -820,11 +820,15 @@ __global__ void __launch_bounds__(256) dq_finalize_kernel(const float* __restric
   constexpr int PASS = kFinNB * RPB;        // rows per pass: at most PASS tokens
   __shared__ float2 cs_s[PASS][half];
   const int qd = threadIdx.x % quads, rsub = threadIdx.x / quads;
-  for (int r0 = blockIdx.x * PASS; r0 < rows; r0 += gridDim.x * PASS) {
+  // rows < 2^31, but a pass start plus the grid stride need not be
+  for (int64_t p0 = (int64_t)blockIdx.x * PASS; p0 < rows; p0 += (int64_t)gridDim.x * PASS) {
+    const int r0 = (int)p0;
+    const int r_last = (int)(p0 + PASS < rows ? p0 + PASS - 1 : rows - 1);  // the pass's last row
     float4 u[kFinNB], w[kFinNB];
 #pragma unroll
     for (int b = 0; b < kFinNB; ++b) {
-      const float* a = acc + (size_t)min(r0 + b * RPB + rsub, rows - 1) * HD;
+      const int64_t ra = p0 + b * RPB + rsub;
+      const float* a = acc + (size_t)(ra < rows ? ra : rows - 1) * HD;
       if (layout == 1) {
         u[b] = *reinterpret_cast<const float4*>(a + qd * 4);
         w[b] = *reinterpret_cast<const float4*>(a + half + qd * 4);
@@ -835,7 +839,7 @@ __global__ void __launch_bounds__(256) dq_finalize_kernel(const float* __restric
     }
     const int t_first = r0 / H;
     if (layout != 2) {
-      const int n = (min(r0 + PASS, rows) - 1) / H - t_first + 1;
+      const int n = r_last / H - t_first + 1;
       for (int e = threadIdx.x; e < n * half; e += blockDim.x) {
         const int tt = e / half, pr = e % half;
         cs_s[tt][pr] = rope_cs(hi_tab, lo_tab, __ldg(pos_id + t_first + tt), pr, half);
@@ -844,8 +848,8 @@ __global__ void __launch_bounds__(256) dq_finalize_kernel(const float* __restric
     }
 #pragma unroll
     for (int b = 0; b < kFinNB; ++b) {
+      if (p0 + b * RPB + rsub >= rows) break;
       const int row = r0 + b * RPB + rsub;
-      if (row >= rows) break;
       __nv_bfloat16* y = dq + (out_tok ? ((size_t)__ldg(out_tok + row / H) * H + row % H) : (size_t)row) * HD;
       float x0[4], x1[4];
       if (layout == 1) {

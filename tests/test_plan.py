@@ -226,3 +226,20 @@ def test_random_packings_vs_oracle(aa, seed):
         assert st["unmasked_pairs"] == orc.unmasked_pairs(c, T, mode)
         assert (st["live_tiles"], st["causal_tiles"]) == orc.tile_counts(c, T, mode)
         assert w["fwd_tiles"] == w["bwd_tiles"]
+
+
+@pytest.mark.parametrize("pos", [orc.POS_RESET, orc.POS_CONTINUOUS])
+def test_metadata_at_one_million_tokens(aa, pos):
+    # the largest packing the GPU tests run (2^20 tokens, 32 heads of 128):
+    # metadata bit-exact, and the visible pairs against the closed form
+    # sum_k N_k (N_k + 1) / 2 + (T - 1) + 1 (each document's causal triangle,
+    # every token's anchor pair, the anchor itself), which the oracle's
+    # explicit-mask count is pinned to at small sizes
+    T = 1 << 20
+    cu = pack(doc_lengths("lognormal", T - 1, np.random.default_rng(3), median=3000, sigma=1.0, lo=64, hi=T - 1), T)
+    with aa.Plan(cu, T, 32, 32, 128, 5e6, orc.MASK_ANCHOR, pos, host_only=True) as p:
+        doc, posv = p.metadata()
+        assert np.array_equal(doc, orc.document_ids(cu, T, orc.MASK_ANCHOR))
+        assert np.array_equal(posv, orc.position_ids(cu, T, orc.MASK_ANCHOR, pos))
+        n = np.diff(cu).astype(np.int64)
+        assert p.stats()["unmasked_pairs"] == int((n * (n + 1) // 2).sum()) + (T - 1) + 1
