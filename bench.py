@@ -132,16 +132,24 @@ def _barrier(world):
         torch.cuda.synchronize()
 
 
+def code_hash(path):
+    """sha256 of a C/CUDA source with its // comments and all whitespace removed:
+    it changes when the code does, not when a comment is edited."""
+    import hashlib
+    import re
+    text = open(path, encoding="utf-8").read()
+    code = "".join(re.sub(r"//.*", "", line) for line in text.splitlines())
+    return hashlib.sha256(re.sub(r"\s+", "", code).encode()).hexdigest()
+
+
 def _captured_traffic(key):
     """DRAM bytes per launch of the dominant kernel from the committed ncu capture
-    (profiles/traffic.json), or None when there is none or the kernel's source has
+    (profiles/traffic.json), or None when there is none or the kernel's code has
     changed since the counters were taken."""
-    import hashlib
     tpath = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         rec = json.load(open(tpath)).get(key)
-        src = open(os.path.join(ROOT, rec["kernel_source"]), "rb").read()
-        if hashlib.sha256(src).hexdigest() != rec["source_sha256"]:
+        if code_hash(os.path.join(ROOT, rec["kernel_source"])) != rec["code_sha256"]:
             return None
         return int(rec["bytes"])
     except Exception:
@@ -286,7 +294,7 @@ def run_ours(args):
                                   f"maximum clock", "frac_of_sustained": round(achieved / sustained, 4),
                      "traffic": traffic,
                      "traffic_source": "DRAM bytes per launch from the committed ncu capture of this kernel "
-                                       "(profiles/traffic.json, checked against the kernel source's hash; "
+                                       "(profiles/traffic.json, checked against a hash of the kernel source's code; "
                                        "null once the source changed), not measured in this run"},
         "cpu_baseline": cpu,
         "e2e": e2e,

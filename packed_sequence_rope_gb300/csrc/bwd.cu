@@ -246,8 +246,8 @@ __global__ void __launch_bounds__(kPrepThreads) bwd_prep_kernel(const __nv_bfloa
 //               dS^T bf16 into shared memory, each group in two 32-column
 //               chunks: the first chunks of both groups release half of the
 //               dV / dK~ products while the second chunks are computed; at
-//               the end of an item they read dV and dK~ out of TMEM and write
-//               dv, dk
+//               the end of an item group 0 reads dV out of TMEM and writes
+//               dv, group 1 reads dK~ and writes dk = R^T (scale dK~)
 //   warps 12-15 dQ drain: dQ~ from TMEM into the fp32 accumulator. For
 //               D = 128 the MMA produces dQ~^T (lane = channel); the drain
 //               copies it into the step's dead Q~/dO stage buffers, releases
