@@ -295,7 +295,7 @@ def run_ours(args):
                      "traffic": traffic,
                      "traffic_source": "DRAM bytes per launch from the committed ncu capture of this kernel "
                                        "(profiles/traffic.json, checked against a hash of the kernel source's code; "
-                                       "null once the source changed), not measured in this run"},
+                                       "null once the code changed), not measured in this run"},
         "cpu_baseline": cpu,
         "e2e": e2e,
         "gpu_launches": n_launch_per_step * args.steps,
