@@ -92,3 +92,70 @@ def test_segments_static_workspace_backward(aa):
         torch.cuda.synchronize()
     assert torch.equal(dk0, dk1) and torch.equal(dv0, dv1)
     assert rel_l2(dq0, f64(dq1)) <= 1e-6
+
+
+def test_full_size_interleaved_chunks_bench_path(aa):
+    # the benchmark's --chunks 4 layout: the 64K packing's 38 documents cut
+    # into 4 chunks each and interleaved, through aa_fwd + aa_bwd_from_fwd.
+    # The kernels run on the tokens grouped by document (in order of first
+    # appearance) and meet the caller's order only through their row maps, so
+    # the contiguous plan on the grouped inputs gives O, LSE, dk and dv bit for
+    # bit and dq up to the order of its fp32 additions; and one document is
+    # checked against the oracle in the caller's order.
+    from aa_synth import WORKLOADS, make_qkv, workload_cu_doclens
+    w = WORKLOADS["llama7b_64k"]
+    T, Hq, Hkv, D = w.total_tokens, w.num_q_heads, w.num_kv_heads, w.head_dim
+    doc = interleaved_chunks(np.diff(workload_cu_doclens(w)), 4, np.random.default_rng(0))
+    assert doc.size == T
+    q, k, v, do = make_qkv(w, device="cuda")
+    outs = []
+    with aa.Plan(None, T, Hq, Hkv, D, w.rope_base, doc_of_token=doc) as p:
+        fws = p.alloc_fwd_workspace(q.device)
+        o, lse = p.fwd(q, k, v, workspace=fws)
+        outs = [o, lse, *p.bwd_from_fwd(fws, v, o, lse, do)]
+        torch.cuda.synchronize()
+        p.check_device_error()
+        del fws
+    first = {}
+    for i, d in enumerate(doc[1:].tolist(), start=1):
+        first.setdefault(d, i)
+    order = sorted(first, key=first.get)
+    perm = np.concatenate([[0]] + [np.flatnonzero(doc == d) for d in order])
+    cu_g = np.concatenate([[1], 1 + np.cumsum([int((doc == d).sum()) for d in order])]).astype(np.int32)
+    pg = torch.as_tensor(perm, device=q.device)
+    with aa.Plan(cu_g, T, Hq, Hkv, D, w.rope_base) as p:
+        fws = p.alloc_fwd_workspace(q.device)
+        o_g, lse_g = p.fwd(q[pg], k[pg], v[pg], workspace=fws)
+        dq_g, dk_g, dv_g = p.bwd_from_fwd(fws, v[pg], o_g, lse_g, do[pg])
+        torch.cuda.synchronize()
+        p.check_device_error()
+        del fws
+    o, lse, dq, dk, dv = outs
+    assert torch.equal(o[pg], o_g)
+    assert torch.equal(lse[:, pg], lse_g)
+    assert torch.equal(dk[pg], dk_g)
+    assert torch.equal(dv[pg], dv_g)
+    # dq: the fp32 accumulator receives the same contributions in another order
+    # (k additions per value: relative error ~ k 2^-24, far below bf16's half
+    # ulp 2^-9), so after the bf16 rounding a value moves by at most one ulp;
+    # the absolute floor covers sums that cancel to near zero
+    a, b = dq[pg].double(), dq_g.double()
+    mag = torch.maximum(a.abs(), b.abs()).clamp_min(1e-30)
+    bound = torch.exp2(torch.floor(torch.log2(mag)) - 7) + 1e-6 * b.abs().max()  # bf16 spacing at |x|
+    bad = int(((a - b).abs() > bound).sum())
+    assert bad == 0, f"dq: {bad} values beyond one bf16 ulp of the contiguous plan's"
+    # one document against the oracle: [anchor + its tokens in the caller's
+    # order] is that document laid out contiguously (positions count its tokens)
+    d = order[len(order) // 2]
+    idx = np.concatenate([[0], np.flatnonzero(doc == d)])
+    n = idx.size - 1
+    it = torch.as_tensor(idx, device=q.device)
+    heads = torch.tensor([0, Hq - 1], device=q.device)
+    sub = [x[it][:, heads].cpu() for x in (q, k, v, do)]
+    prob = orc.Problem([1, 1 + n], 1 + n, 2, 2, D, w.rope_base)
+    O, L = orc.forward(prob, *sub[:3])
+    check_forward(o[it[1:]][:, heads], lse[heads][:, it[1:]], O[1:], L[:, 1:], tag=f"document {d}")
+    gq, gk, gv = orc.backward(prob, *sub)
+    for nm, got, ref in (("dq", dq, gq), ("dk", dk, gk), ("dv", dv, gv)):
+        err = rel_l2(got[it[1:]][:, heads], ref[1:])
+        assert err <= REL_L2, f"document {d} {nm} rel-L2 {err:.3e}"
