@@ -74,3 +74,19 @@ def test_reference_arm_json_line():
     assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["value"] == d["value"]
     assert d["cpu_baseline"]["cores"] >= 1
     assert d["e2e"] == {"value": d["value"], "unit": d["unit"], "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
+
+
+def test_traffic_record_follows_code_not_comments(tmp_path):
+    # the stored DRAM traffic stays valid across comment edits of the kernel
+    # source and is dropped once its code changes
+    sys.path.insert(0, ROOT)
+    import bench
+    src = tmp_path / "k.cu"
+    src.write_text("__global__ void k(int* x) {\n  x[0] = 1;  // one\n}\n")
+    h0 = bench.code_hash(str(src))
+    src.write_text("// a kernel\n__global__ void k(int* x) {\n    x[0] = 1;   // the first element\n}\n")
+    assert bench.code_hash(str(src)) == h0
+    src.write_text("__global__ void k(int* x) {\n  x[0] = 2;\n}\n")
+    assert bench.code_hash(str(src)) != h0
+    rec = bench._captured_traffic("llama7b_64k:attn_bwd_kernel")
+    assert rec is None or rec > 0
