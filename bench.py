@@ -333,22 +333,28 @@ def _time_steps(plan, fwd, bwd, steps, warmup):
 
 def _other_configs(aa, dev, args, causal_ms_64k):
     """The secondary configurations, a few timed steps each: GQA 128K, and the
-    mask-paradigm sweep at 64K (document-length medians 512 / 4096 / one
-    document under CAUSAL, INTRA_DOC + RESET and ANCHOR + RESET) with the
-    skipped-tile fraction and the speedup over the same kernels on the causal
-    mask. The causal step ignores the documents, so one causal timing (the
-    main workload's, same shape) serves every 64K sweep point."""
+    mask-paradigm sweep at 64K (document-length medians 512 / 1500 (the main
+    packing) / 4096 / one document under CAUSAL, INTRA_DOC + RESET, ANCHOR +
+    RESET and ANCHOR + CONTINUOUS) with the skipped-tile fraction and the
+    speedup over the same kernels on the causal mask. The causal step ignores
+    the documents, so one causal timing (the main workload's, same shape)
+    serves every 64K sweep point; the main packing's ANCHOR + RESET point is
+    the headline line itself."""
     import torch
     out = {}
-    runs = [("gqa_128k", "anchor")] + [(w, m) for w in ("sweep_64k_m512", "sweep_64k_m4096", "sweep_64k_single")
-                                       for m in ("intra_doc", "anchor")]
-    for name, mname in runs:
+    runs = [("gqa_128k", "anchor", "reset")]
+    for wname in ("sweep_64k_m512", "llama7b_64k", "sweep_64k_m4096", "sweep_64k_single"):
+        if wname != "llama7b_64k":
+            runs += [(wname, "intra_doc", "reset"), (wname, "anchor", "reset")]
+        runs.append((wname, "anchor", "continuous"))
+    for name, mname, pname in runs:
         w = WORKLOADS[name]
         cu = workload_cu_doclens(w)
         T, Hq, Hkv, D = w.total_tokens, w.num_q_heads, w.num_kv_heads, w.head_dim
         mask = {"anchor": aa.MASK_ANCHOR, "intra_doc": aa.MASK_INTRA_DOC}[mname]
+        pos = {"reset": aa.POS_RESET, "continuous": aa.POS_CONTINUOUS}[pname]
         q, k, v, do = make_qkv(w, device=dev)
-        with aa.Plan(cu, T, Hq, Hkv, D, w.rope_base, mask, aa.POS_RESET) as p:
+        with aa.Plan(cu, T, Hq, Hkv, D, w.rope_base, mask, pos) as p:
             st = p.stats()
             o = torch.empty_like(q)
             lse = torch.empty(Hq, T, device=dev, dtype=torch.float32)
@@ -357,12 +363,12 @@ def _other_configs(aa, dev, args, causal_ms_64k):
             bwd = _bwd_call(p, args.bwd, q, k, v, o, lse, do, dq, dk, dv, fws, dev)
             ms = _time_steps(p, lambda: p.fwd(q, k, v, o, lse, fws), bwd, args.other_steps, 2)
             flops = 14.0 * D * Hq * st["unmasked_pairs"]
-            rec = {"mask": mname, "pos": "reset", "documents": int(len(cu) - 1), "ms_per_step": round(ms, 3),
+            rec = {"mask": mname, "pos": pname, "documents": int(len(cu) - 1), "ms_per_step": round(ms, 3),
                    "tflops": round(flops / (ms * 1e-3) / 1e12, 2),
                    "skipped_tile_fraction": round(1 - st["live_tiles"] / st["causal_tiles"], 4)}
-            if name.startswith("sweep_64k") and causal_ms_64k:
+            if w.total_tokens == 65536 and causal_ms_64k:
                 rec["speedup_vs_causal"] = round(causal_ms_64k / ms, 3)
-            out[f"{name}:{mname}"] = rec
+            out[f"{name}:{mname}" + (":continuous" if pname == "continuous" else "")] = rec
             del bwd, fws, o, lse, dq, dk, dv
         del q, k, v, do
         torch.cuda.empty_cache()
