@@ -252,7 +252,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t t_o[2] = {tmem + 256, tmem + 256 + HD};
       uint32_t ph_p[2] = {0, 0};
       int nq[2] = {0, 0}, ks = 0;
-      bool first_pv[2], ready[2];
+      bool first_pv[2] = {true, true}, ready[2] = {false, false};
       auto issue_s = [&](int t, int s) -> bool {
         if (!ready[t]) {  // this item's Q tile t has landed (first use only)
           if (!wait_or_abort(&sm.q_full[t], nq[t] & 1, P, abort_flag, 312)) return false;
