@@ -563,16 +563,23 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           float sv[32], dpv[32];
           ptx::tmem_ld32(t_s + lane_off + c * 32, sv);
           ptx::tmem_ld32(t_dp + lane_off + c * 32, dpv);
+          // the first 8 columns' -LSE log2(e) and -D, read while TMEM answers;
+          // each group's values are read one group ahead
+          float4 na0 = lse_s[c * 8], na1 = lse_s[c * 8 + 1], nb0 = d_s[c * 8], nb1 = d_s[c * 8 + 1];
           ptx::tmem_wait_ld();
 #pragma unroll
           for (int gq = 0; gq < 4; ++gq) {  // 8 query columns at a time
             const int cb = c * 32 + gq * 8;
             float lse2[8], dd[8];
-#pragma unroll
-            for (int e = 0; e < 8; e += 4) {
-              const float4 a4 = lse_s[(cb + e) >> 2], b4 = d_s[(cb + e) >> 2];
-              lse2[e] = a4.x; lse2[e + 1] = a4.y; lse2[e + 2] = a4.z; lse2[e + 3] = a4.w;
-              dd[e] = b4.x; dd[e + 1] = b4.y; dd[e + 2] = b4.z; dd[e + 3] = b4.w;
+            lse2[0] = na0.x; lse2[1] = na0.y; lse2[2] = na0.z; lse2[3] = na0.w;
+            lse2[4] = na1.x; lse2[5] = na1.y; lse2[6] = na1.z; lse2[7] = na1.w;
+            dd[0] = nb0.x; dd[1] = nb0.y; dd[2] = nb0.z; dd[3] = nb0.w;
+            dd[4] = nb1.x; dd[5] = nb1.y; dd[6] = nb1.z; dd[7] = nb1.w;
+            if (gq < 3) {
+              na0 = lse_s[(cb + 8) >> 2];
+              na1 = lse_s[(cb + 12) >> 2];
+              nb0 = d_s[(cb + 8) >> 2];
+              nb1 = d_s[(cb + 12) >> 2];
             }
             uint32_t pw[4], dw[4];
             if (full) {
