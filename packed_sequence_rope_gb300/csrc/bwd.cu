@@ -567,6 +567,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           // each group's values are read one group ahead
           float4 na0 = lse_s[c * 8], na1 = lse_s[c * 8 + 1], nb0 = d_s[c * 8], nb1 = d_s[c * 8 + 1];
           ptx::tmem_wait_ld();
+          // query columns this key row is not seen by become -inf (P = 2^-inf = 0, dS = 0)
+          if (!full) {
+#pragma unroll
+            for (int x = 0; x < 32; ++x) {
+              const int i = i0 + c * 32 + x;
+              sv[x] = (i >= j && i <= jhi) ? sv[x] : -INFINITY;
+            }
+          }
 #pragma unroll
           for (int gq = 0; gq < 4; ++gq) {  // 8 query columns at a time
             const int cb = c * 32 + gq * 8;
@@ -582,31 +590,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
               nb1 = d_s[(cb + 12) >> 2];
             }
             uint32_t pw[4], dw[4];
-            if (full) {
-              const float2 sl22 = make_float2(sl2, sl2);
+            const float2 sl22 = make_float2(sl2, sl2);
 #pragma unroll
-              for (int e = 0; e < 8; e += 2) {
-                const int x = gq * 8 + e;
-                const float2 a =
-                    __ffma2_rn(make_float2(sv[x], sv[x + 1]), sl22, make_float2(lse2[e], lse2[e + 1]));
-                const float2 pp = make_float2(ptx::ex2(a.x), ptx::ex2(a.y));
-                const float2 dd2 =
-                    __fmul2_rn(pp, __fadd2_rn(make_float2(dpv[x], dpv[x + 1]), make_float2(dd[e], dd[e + 1])));
-                pw[e / 2] = ptx::pack_bf16x2(pp.x, pp.y);
-                dw[e / 2] = ptx::pack_bf16x2(dd2.x, dd2.y);
-              }
-            } else {
-#pragma unroll
-              for (int e = 0; e < 8; e += 2) {
-                const int x = gq * 8 + e;
-                const int i = i0 + cb + e;
-                // masked elements feed -inf to ex2 (2^-inf = 0): selects, no branches
-                const float p0 = ptx::ex2((i >= j && i <= jhi) ? fmaf(sv[x], sl2, lse2[e]) : -INFINITY);
-                const float p1 =
-                    ptx::ex2((i + 1 >= j && i + 1 <= jhi) ? fmaf(sv[x + 1], sl2, lse2[e + 1]) : -INFINITY);
-                pw[e / 2] = ptx::pack_bf16x2(p0, p1);
-                dw[e / 2] = ptx::pack_bf16x2(p0 * (dpv[x] + dd[e]), p1 * (dpv[x + 1] + dd[e + 1]));
-              }
+            for (int e = 0; e < 8; e += 2) {
+              const int x = gq * 8 + e;
+              const float2 a = __ffma2_rn(make_float2(sv[x], sv[x + 1]), sl22, make_float2(lse2[e], lse2[e + 1]));
+              const float2 pp = make_float2(ptx::ex2(a.x), ptx::ex2(a.y));
+              const float2 dd2 =
+                  __fmul2_rn(pp, __fadd2_rn(make_float2(dpv[x], dpv[x + 1]), make_float2(dd[e], dd[e + 1])));
+              pw[e / 2] = ptx::pack_bf16x2(pp.x, pp.y);
+              dw[e / 2] = ptx::pack_bf16x2(dd2.x, dd2.y);
             }
             // P^T packs over S^T columns this group has already read: query
             // columns [64 cq, 64 cq + 64) land in TMEM columns [64 cq, 64 cq + 32)

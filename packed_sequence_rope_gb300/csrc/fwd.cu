@@ -381,18 +381,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int c = 0; c < 4; ++c) ptx::tmem_ld32(t_s + c * 32, sv + c * 32);
         ptx::tmem_wait_ld();
+        // keys this row does not see become -inf (their P is 2^-inf = 0)
+        if (!full) {
+#pragma unroll
+          for (int e = 0; e < 128; ++e) sv[e] = (j0 + e >= lo && j0 + e <= hi) ? sv[e] : -INFINITY;
+        }
         // pass 1: row max of the visible logits (scaled once at the end)
         float mt = -INFINITY;
-        if (full) {
 #pragma unroll
-          for (int e = 0; e < 128; e += 2) mt = fmaxf(mt, fmaxf(sv[e], sv[e + 1]));
-        } else {
-#pragma unroll
-          for (int e = 0; e < 128; ++e) {
-            const int j = j0 + e;
-            if (j >= lo && j <= hi) mt = fmaxf(mt, sv[e]);
-          }
-        }
+        for (int e = 0; e < 128; e += 2) mt = fmaxf(mt, fmaxf(sv[e], sv[e + 1]));
         mt *= sl2;
         // TMEM access is warp-collective, so a rescale of O is decided per warp
         const bool need = (mt > m + kRescaleThreshold) || (m == -INFINITY && mt > -INFINITY);
@@ -420,27 +417,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int c = 0; c < 4; ++c) {
           const float* sc = sv + c * 32;
           uint32_t pw[16];
-          if (full) {
-            const float2 sl22 = make_float2(sl2, sl2), nm2 = make_float2(-mm, -mm);
-            float2 rs2 = make_float2(0.f, 0.f);
+          const float2 sl22 = make_float2(sl2, sl2), nm2 = make_float2(-mm, -mm);
+          float2 rs2 = make_float2(0.f, 0.f);
 #pragma unroll
-            for (int e = 0; e < 16; ++e) {
-              const float2 a = __ffma2_rn(make_float2(sc[2 * e], sc[2 * e + 1]), sl22, nm2);
-              const float2 pp = make_float2(ptx::ex2(a.x), ptx::ex2(a.y));
-              rs2 = __fadd2_rn(rs2, pp);
-              pw[e] = ptx::pack_bf16x2(pp.x, pp.y);
-            }
-            rs += rs2.x + rs2.y;
-          } else {
-#pragma unroll
-            for (int e = 0; e < 16; ++e) {
-              const int j = j0 + c * 32 + 2 * e;
-              const float p0 = (j >= lo && j <= hi) ? ptx::ex2(fmaf(sc[2 * e], sl2, -mm)) : 0.f;
-              const float p1 = (j + 1 >= lo && j + 1 <= hi) ? ptx::ex2(fmaf(sc[2 * e + 1], sl2, -mm)) : 0.f;
-              rs += p0 + p1;
-              pw[e] = ptx::pack_bf16x2(p0, p1);
-            }
+          for (int e = 0; e < 16; ++e) {
+            const float2 a = __ffma2_rn(make_float2(sc[2 * e], sc[2 * e + 1]), sl22, nm2);
+            const float2 pp = make_float2(ptx::ex2(a.x), ptx::ex2(a.y));
+            rs2 = __fadd2_rn(rs2, pp);
+            pw[e] = ptx::pack_bf16x2(pp.x, pp.y);
           }
+          rs += rs2.x + rs2.y;
           ptx::tmem_st16(t_s + c * 16, pw);
         }
         l += rs;
