@@ -45,6 +45,25 @@ constexpr uint64_t kDrainLimitNs = 1000000000ull;
 constexpr int kStages = 2;
 constexpr int kThreads = 384;
 
+// One item as the roles see it: query tiles qt0 and qt0 + 1 (when it exists)
+// of head h over key tiles [kt_lo, kt_hi]; query tile t visits [lo[t], hi[t]].
+struct FwdItem {
+  int h, qt0, kt_lo, kt_hi, lo[2], hi[2];
+  bool has1;
+};
+
+// A claimed item as the producer publishes it: the work-list index (-1: none
+// left), its decoded description and the anchor's rotated key and value rows
+// for the item's kv head (bf16 pairs), so that no role starts an item with
+// dependent global loads.
+template <int HD>
+struct ItemSlot {
+  alignas(16) uint32_t k0[HD / 2];
+  alignas(16) uint32_t v0[HD / 2];
+  FwdItem w;
+  int it;
+};
+
 template <int HD>
 struct FwdSmem {
   static constexpr int kB = HD / 64;
@@ -53,7 +72,7 @@ struct FwdSmem {
   alignas(1024) uint8_t v[kStages][kB][16384];
   uint64_t q_full[2], q_free[2];
   uint64_t item_full[2], item_empty[2];
-  int item_slot[2];  // claimed work-list index (-1: none left)
+  ItemSlot<HD> slot[2];
   uint64_t kv_full[kStages], kv_empty[kStages];
   uint64_t s_full[2], p_full[2], o_full[2], drain;
   uint32_t tmem_base;
@@ -81,12 +100,6 @@ struct FwdParams {
   float scale;
 };
 
-// One item as the roles see it: query tiles qt0 and qt0 + 1 (when it exists)
-// of head h over key tiles [kt_lo, kt_hi]; query tile t visits [lo[t], hi[t]].
-struct FwdItem {
-  int h, qt0, kt_lo, kt_hi, lo[2], hi[2];
-  bool has1;
-};
 
 __device__ __forceinline__ FwdItem load_fwd_item(const FwdParams& P, int it) {
   const WorkItem w = P.items[it];
@@ -122,9 +135,10 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, co
 
 // The li-th item this CTA runs (its work-list index, or -1 when the list is
 // exhausted or the CTA aborted), as the producer published it in slot li & 1.
-// warp_read: the whole (converged) warp reads it and lane 0 frees the slot;
-// otherwise the calling thread alone. Slot readers: the MMA thread and the 8
-// softmax warps.
+// warp_read: the whole (converged) warp waits. Each reader frees the slot
+// (release_fwd_item) once it no longer reads it: the MMA thread after the
+// item's last product, the softmax warps after the epilogue (it reads v_0
+// from the slot). Slot readers: the MMA thread and the 8 softmax warps.
 constexpr int kFwdItemReaders = 9;
 static_assert(kFwdItemReaders == 1 + (kThreads / 32 - 4), "item readers: the MMA thread and warps 4-11");
 
@@ -135,14 +149,17 @@ __device__ __forceinline__ int read_fwd_item(Smem& sm, int li, const FwdParams& 
   bool ok = wait_or_abort(&sm.item_full[slot], (li >> 1) & 1, P, abort_flag, site);
   if (warp_read) ok = __all_sync(0xffffffffu, ok);
   if (!ok) return -1;
-  const int it = *reinterpret_cast<volatile int*>(&sm.item_slot[slot]);
+  return *reinterpret_cast<volatile int*>(&sm.slot[slot].it);
+}
+
+template <class Smem>
+__device__ __forceinline__ void release_fwd_item(Smem& sm, int li, bool warp_read) {
   if (warp_read) {
     __syncwarp();
-    if ((threadIdx.x & 31) == 0) ptx::mbar_arrive(&sm.item_empty[slot]);
+    if ((threadIdx.x & 31) == 0) ptx::mbar_arrive(&sm.item_empty[li & 1]);
   } else {
-    ptx::mbar_arrive(&sm.item_empty[slot]);
+    ptx::mbar_arrive(&sm.item_empty[li & 1]);
   }
-  return it;
 }
 
 // Barrier phases: the item ring counts the CTA's items; the K/V ring counts
@@ -210,10 +227,31 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!ok) break;
         int it = atomicAdd(P.next_item, 1);
         if (it >= P.n_items) it = -1;
-        sm.item_slot[slot] = it;
+        ItemSlot<HD>& sl = sm.slot[slot];
+        sl.it = it;
+        FwdItem w{};
+        if (it >= 0) {
+          w = load_fwd_item(P, it);
+          sl.w = w;
+          if (P.anchor) {
+            const size_t row0 = (size_t)(w.h / P.group) * HD;
+            const uint4* ks = reinterpret_cast<const uint4*>(P.kr + row0);
+            const uint4* vs = reinterpret_cast<const uint4*>(P.v + row0);
+            uint4 kq[HD / 8], vq[HD / 8];
+#pragma unroll
+            for (int c = 0; c < HD / 8; ++c) {
+              kq[c] = __ldg(ks + c);
+              vq[c] = __ldg(vs + c);
+            }
+#pragma unroll
+            for (int c = 0; c < HD / 8; ++c) {
+              reinterpret_cast<uint4*>(sl.k0)[c] = kq[c];
+              reinterpret_cast<uint4*>(sl.v0)[c] = vq[c];
+            }
+          }
+        }
         ptx::mbar_arrive(&sm.item_full[slot]);  // release: the slot is written
         if (it < 0) break;
-        const FwdItem w = load_fwd_item(P, it);
         const int g = w.h / P.group;
         for (int t = 0; t < (w.has1 ? 2 : 1) && ok; ++t) {
           // the tile's previous Q has had its last S product and its anchor dot
@@ -281,7 +319,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int li = 0; ok; ++li) {
         const int it = read_fwd_item(sm, li, P, abort_flag, false, 310);
         if (it < 0) break;
-        const FwdItem w = load_fwd_item(P, it);
+        const FwdItem w = sm.slot[li & 1].w;
         first_pv[0] = first_pv[1] = true;
         ready[0] = false;
         ready[1] = !w.has1;
@@ -313,6 +351,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (ok) ptx::mma_commit(&sm.o_full[1]);
         }
         if (ok) ptx::mma_commit(&sm.kv_empty[(ks - 1) % kStages]);
+        release_fwd_item(sm, li, false);
         ++nq[0];
         if (w.has1) ++nq[1];
       }
@@ -333,9 +372,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int li = 0; ok; ++li) {
       const int it = read_fwd_item(sm, li, P, abort_flag, true, 320);
       if (it < 0) break;
-      const FwdItem w = load_fwd_item(P, it);
-      if (t == 1 && !w.has1) continue;
-      const int h = w.h, g = h / P.group;
+      const ItemSlot<HD>& sl = sm.slot[li & 1];
+      const FwdItem w = sl.w;
+      if (t == 1 && !w.has1) {
+        release_fwd_item(sm, li, true);
+        continue;
+      }
+      const int h = w.h;
       const int lo_t = w.lo[t], hi_t = w.hi[t];
       const int i = (w.qt0 + t) * kTile + r;
       const bool row_valid = i < P.T;
@@ -345,12 +388,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (P.anchor) {
         ok = __all_sync(0xffffffffu, wait_or_abort(&sm.q_full[t], nq & 1, P, abort_flag, 324));
         if (!ok) break;
-        // s_i0 = q~_i . k~_0 with the rotated anchor key from the workspace
-        const uint4* k0 = reinterpret_cast<const uint4*>(P.kr + (size_t)g * HD);
+        // s_i0 = q~_i . k~_0 with the rotated anchor key the producer staged
+        const uint4* k0 = reinterpret_cast<const uint4*>(sl.k0);
         float acc = 0.f;
 #pragma unroll 4
         for (int c8 = 0; c8 < HD / 8; ++c8) {
-          const uint4 kq = __ldg(k0 + c8);
+          const uint4 kq = k0[c8];
           const uint4 qq = *reinterpret_cast<const uint4*>(sm.q[t][0] + (c8 >> 3) * 16384 + sw128_chunk(r, c8 & 7));
           const uint32_t ka[4] = {kq.x, kq.y, kq.z, kq.w}, qa[4] = {qq.x, qq.y, qq.z, qq.w};
 #pragma unroll
@@ -455,7 +498,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int e = 0; e < 16; ++e) {
             float2 v0 = make_float2(0.f, 0.f);
             if (P.anchor)
-              v0 = ptx::unpack_bf16x2(__ldg(reinterpret_cast<const uint32_t*>(P.v + (size_t)g * HD + c * 32) + e));
+              v0 = ptx::unpack_bf16x2(sl.v0[c * 16 + e]);
             const float a = (ov[2 * e] + w0 * v0.x) * inv_l;
             const float b = (ov[2 * e + 1] + w0 * v0.y) * inv_l;
             ow[e] = ptx::pack_bf16x2(a, b);
@@ -466,6 +509,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       if (row_valid) P.lse[(size_t)h * P.T + i_out] = (m + log2f(l)) * 0.69314718055994531f;
+      release_fwd_item(sm, li, true);
       ++nq;
     }
   }
