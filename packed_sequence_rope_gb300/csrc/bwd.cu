@@ -794,14 +794,22 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       for (int step = 0; step < w.n_steps && ok; ++step, ++gs) {
         const int s = gs & 1;
         const int i0 = w.qtile(step) * kTile;
+        const size_t hrow = (size_t)w.head(step, P.group) * P.T;
+        // the step's rows are read from global memory while its tiles land
+        float a[kTile / 64], b[kTile / 64];
+#pragma unroll
+        for (int u = 0; u < kTile / 64; ++u) {
+          const int i = i0 + t + 64 * u;
+          const int is = i < P.T && P.rows ? __ldg(P.rows + i) : i;
+          a[u] = i < P.T ? -__ldg(P.lse + hrow + is) * kLog2e : -INFINITY;  // -LSE log2(e)
+          b[u] = i < P.T ? -__ldg(P.ws.dsum + hrow + i) : 0.f;             // -D
+        }
         ok = bwd_wait(&sm.qd_full[s], (gs >> 1) & 1, P, abort_flag, 442);
         if (!ok) break;
-        const size_t hrow = (size_t)w.head(step, P.group) * P.T;
-        for (int r = t; r < kTile; r += 64) {
-          const int i = i0 + r;
-          const int is = i < P.T && P.rows ? __ldg(P.rows + i) : i;
-          sm.lse2[s][r] = i < P.T ? -__ldg(P.lse + hrow + is) * kLog2e : -INFINITY;  // -LSE log2(e)
-          sm.dsum[s][r] = i < P.T ? -__ldg(P.ws.dsum + hrow + i) : 0.f;             // -D
+#pragma unroll
+        for (int u = 0; u < kTile / 64; ++u) {
+          sm.lse2[s][t + 64 * u] = a[u];
+          sm.dsum[s][t + 64 * u] = b[u];
         }
         ptx::mbar_arrive(&sm.q_ready[s]);
       }
