@@ -246,8 +246,9 @@ __global__ void __launch_bounds__(kPrepThreads) bwd_prep_kernel(const __nv_bfloa
 //               dS^T bf16 into shared memory, each group in two 32-column
 //               chunks: the first chunks of both groups release half of the
 //               dV / dK~ products while the second chunks are computed; at
-//               the end of an item group 0 reads dV out of TMEM and writes
-//               dv, group 1 reads dK~ and writes dk = R^T (scale dK~)
+//               the end of an item they read dV and dK~ out of TMEM and write
+//               dv and dk = R^T (scale dK~): group 0 dv and half of dk,
+//               group 1 the other half
 //   warps 12-15 dQ drain: dQ~ from TMEM into the fp32 accumulator. For
 //               D = 128 the MMA produces dQ~^T (lane = channel); the drain
 //               copies it into the step's dead Q~/dO stage buffers, releases
@@ -689,9 +690,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           }
         }
       };
-      // group 0 writes dv, group 1 the rotated dk units (measured faster than
-      // dealing the dk units out by cost: 4.52 against 4.58 ms per backward
-      // at 64K)
+      // group 0 writes dv and, when there are four dk units (D = 128, adjacent
+      // pairs), the first two; group 1 the other dk units
       if (cq == 0) {
 #pragma unroll 1
         for (int c = 0; c < HD / 32; ++c) {
@@ -700,9 +700,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           ptx::tmem_wait_ld();
           if (key_valid) store32(dvrow, c * 32, x);
         }
-      } else {
+        const int nd = P.layout == 1 ? HD / 64 : HD / 32, sp = nd >= 4 ? 2 : 0;  // dk units: all, group 0's
 #pragma unroll 1
-        for (int u = 0; u < (P.layout == 1 ? HD / 64 : HD / 32); ++u) dk_unit(u);
+        for (int u = 0; u < sp; ++u) dk_unit(u);
+      } else {
+        const int nd = P.layout == 1 ? HD / 64 : HD / 32, sp = nd >= 4 ? 2 : 0;
+#pragma unroll 1
+        for (int u = sp; u < nd; ++u) dk_unit(u);
       }
     }
   } else if (warp >= 12) {
