@@ -103,9 +103,10 @@ typedef struct aa_plan_s* aa_plan_t;
  * §3.4 Index]: per-token document and position IDs, each query row's visible
  * key interval, the live 128x128 tile lists (fully cross-document tiles are
  * dropped; the anchor column is folded in separately) in the order the
- * persistent attention kernels claim them (longest first; the backward's
- * grouped by document and head), and the two-level fp32 cos/sin tables of
- * Eq. 6 built in fp64.
+ * persistent attention kernels claim them (grouped by document, longest
+ * group first: the forward's heads interleaved in each document, the
+ * backward's one group per document and head), and the two-level fp32
+ * cos/sin tables of Eq. 6 built in fp64.
  * cu_doclens: host int32[num_docs + 1] (see conventions). Device metadata is
  * uploaded with copies ordered on `stream`. On success *out owns everything;
  * release it with aa_plan_destroy. */

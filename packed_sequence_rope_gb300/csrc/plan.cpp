@@ -120,13 +120,18 @@ static void build_stats_and_work(aa_plan_s* p) {
       if (hi < j0) continue;  // no key of this tile is seen through the tile path
       p->bwd_items.push_back(WorkItem{b, g, b, hi / kTile});
     }
-  // Backward work order: CTAs that touch the same (document, head) run
-  // together, so that document's Q/dO tiles and dQ accumulator rows stay in
-  // L2 while they are re-read and reduced into (otherwise the fp32
-  // accumulator, 1 GiB at 64K x 32 heads, is read and written back to HBM on
-  // every reduction). Groups
-  // run longest first (LPT over groups); inside a group the items follow
-  // the tile order. Ties resolve in a fixed order so plans are reproducible.
+  // Work order. Items that read the same document run together, so its
+  // tiles are fetched from HBM about once and re-read from L2, and groups
+  // run longest first (LPT over groups). Ties resolve in a fixed order so
+  // plans are reproducible.
+  //  - backward: one group per (document, head), items in tile order: the
+  //    document's Q/dO tiles and dQ accumulator rows stay in L2 while they
+  //    are re-read and reduced into (otherwise the fp32 accumulator, 1 GiB
+  //    at 64K x 32 heads, goes to HBM and back on every reduction);
+  //  - forward: one group per document with its heads interleaved, items
+  //    longest first: the CTAs running together read neighbouring head
+  //    slices of the same K/V rows (a [T, H, D] row holds every head), which
+  //    a group per (document, head) does not.
   auto order = [&](std::vector<WorkItem>& items, bool fwd) {
     auto doc_of = [&](const WorkItem& w) {
       const int row = fwd ? 2 * w.tile * kTile : w.tile * kTile;
@@ -134,34 +139,33 @@ static void build_stats_and_work(aa_plan_s* p) {
     };
     std::vector<int64_t> key_doc(items.size());
     std::map<std::pair<int, int>, int64_t> group_cost;
+    auto group = [&](size_t n) { return std::make_pair((int)key_doc[n], fwd ? 0 : items[n].head); };
     for (size_t n = 0; n < items.size(); ++n) {
       key_doc[n] = doc_of(items[n]);
-      group_cost[{(int)key_doc[n], items[n].head}] += items[n].hi - items[n].lo + 1;
+      group_cost[group(n)] += items[n].hi - items[n].lo + 1;
     }
     std::vector<size_t> idx(items.size());
     for (size_t n = 0; n < idx.size(); ++n) idx[n] = n;
     std::stable_sort(idx.begin(), idx.end(), [&](size_t a, size_t b) {
       const WorkItem &x = items[a], &y = items[b];
-      const int64_t cx = group_cost[{(int)key_doc[a], x.head}], cy = group_cost[{(int)key_doc[b], y.head}];
+      const int64_t cx = group_cost[group(a)], cy = group_cost[group(b)];
       if (cx != cy) return cx > cy;
       if (key_doc[a] != key_doc[b]) return key_doc[a] < key_doc[b];
+      if (fwd) {
+        const int lx = x.hi - x.lo, ly = y.hi - y.lo;
+        if (lx != ly) return lx > ly;
+        if (x.tile != y.tile) return x.tile < y.tile;
+        return x.head < y.head;
+      }
       if (x.head != y.head) return x.head < y.head;
-      return fwd ? x.tile > y.tile : x.tile < y.tile;
+      return x.tile < y.tile;
     });
     std::vector<WorkItem> sorted;
     sorted.reserve(items.size());
     for (size_t n : idx) sorted.push_back(items[n]);
     items.swap(sorted);
   };
-  // the forward streams K/V at a rate HBM sustains, so it keeps plain
-  // longest-first order for load balance; the backward's dQ reductions and
-  // Q/dO re-reads need the document grouping
-  std::stable_sort(p->fwd_items.begin(), p->fwd_items.end(), [](const WorkItem& x, const WorkItem& y) {
-    const int cx = x.hi - x.lo, cy = y.hi - y.lo;
-    if (cx != cy) return cx > cy;
-    if (x.tile != y.tile) return x.tile < y.tile;
-    return x.head < y.head;
-  });
+  order(p->fwd_items, true);
   order(p->bwd_items, false);
   p->fwd_tiles = 0;
   for (int a = 0; a < nt; ++a) p->fwd_tiles += (int64_t)(q_ranges[a].hi - q_ranges[a].lo + 1) * p->Hq;
