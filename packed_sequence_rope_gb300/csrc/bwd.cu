@@ -30,7 +30,10 @@ namespace {
 
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr uint64_t kDrainLimitNs = 1000000000ull;
-constexpr int kPrepChunks = 256;  // row chunks of the anchor partial sums
+// Row chunks of the anchor partial sums: one prep block per (head, chunk).
+// 64 blocks of about 1K rows per head ran the prep pass faster than 256 short
+// ones (fewer block prologues and epilogue reductions).
+constexpr int kPrepChunks = 64;
 
 struct Workspace {
   __nv_bfloat16* qr;  // [T, Hq, D] rotated Q (unused without RoPE)
@@ -906,11 +909,12 @@ __global__ void __launch_bounds__(256) dq_finalize_kernel(const float* __restric
 }
 
 // ---------------------------------------------------------------- 4. anchor
-// One block per kv head. The 256 row chunks are split into runs of
+// One block per kv head. The kPrepChunks row chunks are split into runs of
 // consecutive chunks, each summed by its own thread (many loads in flight
 // instead of one long dependent walk), and the runs are combined in run
 // order, so the sums are run-to-run deterministic.
 constexpr int kAnchorThreads = 512;
+static_assert(kPrepChunks % (kAnchorThreads / 64) == 0, "row chunks split evenly into runs at D = 64 and 128");
 
 __global__ void __launch_bounds__(kAnchorThreads)
     anchor_finalize_kernel(Workspace ws, __nv_bfloat16* __restrict__ dk, __nv_bfloat16* __restrict__ dv,
