@@ -420,6 +420,55 @@ def _causal_speedup(aa, w, q, k, v, do, dev, ms_anchor, args):
     return {"causal_ms_per_step": round(ms_causal, 3), "speedup": round(ms_causal / ms_anchor, 3)}
 
 
+def _gpu_numa_node(dev):
+    """The NUMA node the GPU's PCI function reports (sysfs) and that node's
+    CPUs, or (None, None) where the system does not say."""
+    import torch
+    try:
+        pr = torch.cuda.get_device_properties(dev)
+        bdf = f"{pr.pci_domain_id:04x}:{pr.pci_bus_id:02x}:{pr.pci_device_id:02x}.0"
+        with open(f"/sys/bus/pci/devices/{bdf}/numa_node") as f:
+            node = int(f.read())
+        if node < 0:
+            return None, None
+        cpus = set()
+        with open(f"/sys/devices/system/node/node{node}/cpulist") as f:
+            for part in f.read().strip().split(","):
+                lo, _, hi = part.partition("-")
+                cpus.update(range(int(lo), int(hi or lo) + 1))
+        return node, cpus
+    except (OSError, ValueError, AttributeError):
+        return None, None
+
+
+def _link_probe(h_src, d_dst, d_src, h_dst):
+    """Host link bandwidth with the e2e run's own pinned buffers (GB/s): one
+    copy host -> device, one device -> host, then both at once (each rate
+    over the pair's common wall time). Outside the timed region."""
+    import torch
+    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+    nb_in, nb_out = h_src.numel() * h_src.element_size(), d_src.numel() * d_src.element_size()
+
+    def timed(pairs):
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in pairs]
+        torch.cuda.synchronize()
+        for (a, z), (st, dst, src) in zip(ev, pairs):
+            a.record(st)
+            with torch.cuda.stream(st):
+                dst.copy_(src, non_blocking=True)
+            z.record(st)
+        torch.cuda.synchronize()
+        return [a.elapsed_time(z) for a, z in ev]
+
+    timed([(s1, d_dst, h_src), (s2, h_dst, d_src)])  # warm-up
+    t_in = timed([(s1, d_dst, h_src)])[0]
+    t_out = timed([(s2, h_dst, d_src)])[0]
+    both = max(timed([(s1, d_dst, h_src), (s2, h_dst, d_src)]))
+    gbs = lambda b, ms: round(b / (ms * 1e-3) / 1e9, 1)
+    return {"h2d": gbs(nb_in, t_in), "d2h": gbs(nb_out, t_out),
+            "h2d_concurrent": gbs(nb_in, both), "d2h_concurrent": gbs(nb_out, both), "bytes_each": int(nb_in)}
+
+
 def _e2e(aa, plan, w, dev, args, flops, world):
     """Same step through the public C-ABI with host buffers: every step copies its
     Q/K/V/dO in from pinned host memory, runs fwd + bwd, and copies O, LSE, dQ,
@@ -430,10 +479,22 @@ def _e2e(aa, plan, w, dev, args, flops, world):
     buffer's reuse)."""
     import torch
     T, Hq, Hkv, D = w.total_tokens, w.num_q_heads, w.num_kv_heads, w.head_dim
-    hq, hk, hv, hdo = (t.pin_memory() for t in make_qkv(w, device="cpu"))
+    # pinned host buffers on the GPU's own NUMA node where the system names
+    # one (pages land on the node of the thread that first writes them)
+    node, cpus = _gpu_numa_node(dev)
+    old_aff = os.sched_getaffinity(0)
+    if cpus and cpus & old_aff:
+        os.sched_setaffinity(0, cpus & old_aff)
+    try:
+        hq, hk, hv, hdo = (t.pin_memory() for t in make_qkv(w, device="cpu"))
+        h_out = (torch.empty_like(hq).pin_memory(), torch.empty(Hq, T, dtype=torch.float32).pin_memory(),
+                 torch.empty_like(hq).pin_memory(), torch.empty_like(hk).pin_memory(),
+                 torch.empty_like(hv).pin_memory())
+        for t in h_out:
+            t.zero_()
+    finally:
+        os.sched_setaffinity(0, old_aff)
     h_in = (hq, hk, hv, hdo)
-    h_out = (torch.empty_like(hq).pin_memory(), torch.empty(Hq, T, dtype=torch.float32).pin_memory(),
-             torch.empty_like(hq).pin_memory(), torch.empty_like(hk).pin_memory(), torch.empty_like(hv).pin_memory())
     d_in = [tuple(torch.empty_like(t, device=dev) for t in h_in) for _ in range(2)]
     d_out = [(torch.empty_like(d_in[b][0]), torch.empty(Hq, T, device=dev, dtype=torch.float32),
               torch.empty_like(d_in[b][0]), torch.empty_like(d_in[b][1]), torch.empty_like(d_in[b][2]))
@@ -447,6 +508,8 @@ def _e2e(aa, plan, w, dev, args, flops, world):
         bwds.append(_bwd_call(plan, args.bwd, q, k, v, o, lse, do, dq, dk, dv, fws, dev))
     h2d = sum(t.numel() * t.element_size() for t in h_in)
     d2h = sum(t.numel() * t.element_size() for t in h_out)
+    link = _link_probe(hq, d_in[0][0], d_out[0][0], h_out[0])
+    link["gpu_numa_node"] = node
     ev = lambda: torch.cuda.Event()
     in_done, comp_done, out_done = [ev(), ev()], [ev(), ev()], [ev(), ev()]
     used = [False, False]
@@ -491,7 +554,9 @@ def _e2e(aa, plan, w, dev, args, flops, world):
     ms = _max_over_ranks(a.elapsed_time(z) / n, world)
     return {"value": round(world * flops / (ms * 1e-3) / 1e12, 2), "unit": UNIT, "ms_per_step": round(ms, 3),
             "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
-            "pipelined": "inputs of step i+1 in and results of step i-1 out on their own streams while step i computes"}
+            "pipelined": "inputs of step i+1 in and results of step i-1 out on their own streams while step i computes",
+            "link_gbs": link,
+            "link_bound_ms": round(1e3 * max(h2d / (link["h2d_concurrent"] * 1e9), d2h / (link["d2h_concurrent"] * 1e9)), 3)}
 
 
 # ----------------------------------------------------------------------------- CPU oracle
