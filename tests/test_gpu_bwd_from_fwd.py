@@ -165,3 +165,50 @@ def test_full_size_training_step(aa, name, heads):
     for nm, got, ref in (("dk_0", dk[0], gk0), ("dv_0", dv[0], gv0)):
         e = rel_l2(got, ref)
         assert e <= REL_L2, f"{name} anchor {nm} over all {T} rows: rel-L2 {e:.3e}"
+
+
+def test_training_step_replays_from_a_cuda_graph(aa):
+    # The training step (aa_fwd + aa_bwd_from_fwd) issues only stream-ordered
+    # work (kernel launches and the work counters' async resets), so a caller
+    # may capture it in a CUDA graph: each replay re-runs the whole step and
+    # gives the eager step's O, LSE, dk and dv bit for bit and its dq up to the
+    # order of the fp32 dQ additions (within one bf16 ulp of each value).
+    cu, T, Hq, Hkv, D = [1, 90, 600, 1100, 1500], 1500, 4, 2, 128
+    q, k, v, do = inputs(T, Hq, Hkv, D, seed=61)
+    with aa.Plan(cu, T, Hq, Hkv, D, 5e6) as p:
+        fws = p.alloc_fwd_workspace(q.device)
+        ws = torch.empty(p.bwd_from_fwd_workspace_bytes(), device=q.device, dtype=torch.uint8)
+        o, lse = torch.empty_like(q), torch.empty(Hq, T, device=q.device, dtype=torch.float32)
+        dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+        outs = (o, lse, dq, dk, dv)
+
+        def step():
+            p.fwd(q, k, v, o, lse, fws)
+            p.bwd_from_fwd(fws, v, o, lse, do, dq, dk, dv, ws)
+
+        step()
+        torch.cuda.synchronize()
+        p.check_device_error()
+        ref = [t.clone() for t in outs]
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            step()
+        torch.cuda.current_stream().wait_stream(side)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            step()
+        torch.cuda.synchronize()
+        for _ in range(2):
+            for t in outs:
+                t.fill_(float("nan"))
+            g.replay()
+            torch.cuda.synchronize()
+            p.check_device_error()
+            for name, got, want in zip(("o", "lse", "dk", "dv"), (o, lse, dk, dv), (ref[0], ref[1], ref[3], ref[4])):
+                assert torch.equal(got, want), f"graph replay: {name} differs from the eager step"
+            a, b = dq.double(), ref[2].double()
+            mag = torch.maximum(a.abs(), b.abs()).clamp_min(1e-30)
+            bound = torch.exp2(torch.floor(torch.log2(mag)) - 7) + 1e-6 * b.abs().max()
+            assert bool(((a - b).abs() <= bound).all()), "graph replay: dq beyond one bf16 ulp of the eager step"
