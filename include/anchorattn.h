@@ -42,6 +42,13 @@
  *    (the persistent kernels keep their work counters there); calls with one
  *    plan share its device error word, so aa_check_device_error() reports a
  *    timeout from any of them.
+ *  - The compute calls enqueue only stream-ordered work (kernel launches and
+ *    asynchronous memsets of their work counters), so a sequence of them may
+ *    be captured in a CUDA graph and replayed while the plan, the tensors and
+ *    the workspaces it names stay alive. Make one uncaptured call of each
+ *    entry point per device first: the first call sets the kernels'
+ *    shared-memory attributes (aa_bwd_static_workspace also looks up its
+ *    array's address then).
  *  - A thread-local message describing the last failure is available from
  *    aa_last_error().
  */
