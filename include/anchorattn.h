@@ -262,7 +262,7 @@ size_t aa_bwd_from_fwd_workspace_bytes(aa_plan_t plan);
  *    aa_bwd_workspace_bytes() is the exact test. As a guide, for plans built
  *    from cu_doclens with RoPE at D = 128 a query row needs about 1 KB
  *    (rotated Q and K and the fp32 dQ accumulator) and each query head
- *    0.25 MiB of anchor partials, so T * Hq up to about 55K query rows fit.
+ *    64 KB of anchor partials, so T * Hq up to about 60K query rows fit.
  *    Segment plans (aa_plan_segments) also need grouped copies of v and
  *    dout (and, without RoPE, of q and k), so somewhat fewer rows fit.
  *  - The plan's device must be current. The first call on a device looks up
