@@ -484,7 +484,10 @@ def _e2e(aa, plan, w, dev, args, flops, world):
     node, cpus = _gpu_numa_node(dev)
     old_aff = os.sched_getaffinity(0)
     if cpus and cpus & old_aff:
-        os.sched_setaffinity(0, cpus & old_aff)
+        try:
+            os.sched_setaffinity(0, cpus & old_aff)
+        except OSError:  # a placement hint only
+            pass
     try:
         hq, hk, hv, hdo = (t.pin_memory() for t in make_qkv(w, device="cpu"))
         h_out = (torch.empty_like(hq).pin_memory(), torch.empty(Hq, T, dtype=torch.float32).pin_memory(),
@@ -493,7 +496,10 @@ def _e2e(aa, plan, w, dev, args, flops, world):
         for t in h_out:
             t.zero_()
     finally:
-        os.sched_setaffinity(0, old_aff)
+        try:
+            os.sched_setaffinity(0, old_aff)
+        except OSError:
+            pass
     h_in = (hq, hk, hv, hdo)
     d_in = [tuple(torch.empty_like(t, device=dev) for t in h_in) for _ in range(2)]
     d_out = [(torch.empty_like(d_in[b][0]), torch.empty(Hq, T, device=dev, dtype=torch.float32),
