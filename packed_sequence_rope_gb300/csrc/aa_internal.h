@@ -27,7 +27,7 @@ struct DevicePlan {
   int32_t* pos_id = nullptr;   // [T] rotation index (shift included)
   int32_t* row_lo = nullptr;   // [T] first key of row i's tile-path interval [row_lo, i]
   int32_t* key_hi = nullptr;   // [T] last query row that sees key j in the tile path
-  WorkItem* fwd_items = nullptr;  // longest first (claimed by the CTAs in that order)
+  WorkItem* fwd_items = nullptr;  // grouped by document, longest group first (claimed in that order)
   WorkItem* bwd_items = nullptr;  // in work-list order (claimed by the CTAs in that order)
   int32_t* qtile_klo = nullptr;  // [n_tiles] first live key tile of each query tile
   float2* rope_hi = nullptr;   // [n_hi][D/2]  cos/sin((32*h) * theta_p)

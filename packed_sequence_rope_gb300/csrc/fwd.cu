@@ -13,7 +13,8 @@
 // rotated inside the attention kernel would put the rotation between one
 // item's last products and the next item's first. The attention kernel is
 // persistent: one CTA per SM; the CTAs claim (pair of 128-row query tiles,
-// head) items longest first from a counter, 384 threads:
+// head) items from a counter in work-list order (grouped by document with
+// the heads interleaved, longest document first), 384 threads:
 //   warp 0      claims the next item (published to the other roles through a
 //               2-slot shared-memory ring) and is the TMA producer: each
 //               item's rotated Q0/Q1 as soon as the previous item's last S
@@ -88,7 +89,7 @@ struct FwdParams {
   const int32_t* row_lo;
   const int32_t* qtile_klo;
   const int32_t* out_rows;   // caller row of each kernel row for O / LSE (NULL: the same row)
-  const WorkItem* items;     // the work list, longest first
+  const WorkItem* items;     // the work list: grouped by document, longest group first
   int32_t* next_item;        // next unclaimed index (zeroed before the launch)
   int n_items;
   const float2* rope_hi;
@@ -582,7 +583,7 @@ aa_status launch_fwd(aa_plan_s* p, const void* q, const void* k, const void* v, 
   });
   if (e != cudaSuccess) return cuda_fail(e, "attn_fwd_kernel smem attribute");
   // persistent: one CTA per SM (fewer for short work lists), claiming the
-  // items longest first from the counter in this call's workspace
+  // items in work-list order from the counter in this call's workspace
   if (p->fwd_items.empty()) return AA_OK;
   if ((e = cudaMemsetAsync(P.next_item, 0, sizeof(int32_t), s)) != cudaSuccess)
     return cuda_fail(e, "resetting the forward work counter");
