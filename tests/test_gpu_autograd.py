@@ -95,3 +95,32 @@ def test_autograd_through_a_following_op(aa):
         torch.cuda.synchronize()
     assert torch.equal(k.grad, dk_ref) and torch.equal(v.grad, dv_ref)
     assert _within_one_ulp(q.grad, dq_ref)
+
+
+def test_autograd_on_a_segment_plan(aa):
+    # documents given per token (interleaved chunks): the entry goes through
+    # the same calls, so its gradients are aa_bwd's and meet the oracle in the
+    # caller's token order
+    import numpy as np
+    from aa_synth import interleaved_chunks
+    doc = interleaved_chunks([200, 37, 410, 3, 150], 4, np.random.default_rng(9))
+    T, Hq, Hkv, D = doc.size, 4, 2, 128
+    q0, k0, v0, do = inputs(T, Hq, Hkv, D, seed=73)
+    with aa.Plan(None, T, Hq, Hkv, D, 5e5, doc_of_token=doc) as p:
+        q, k, v = (x.clone().requires_grad_(True) for x in (q0, k0, v0))
+        o = aa.anchor_attention(p, q, k, v)
+        (o.float() * do.float()).sum().backward()
+        torch.cuda.synchronize()
+        p.check_device_error()
+        o_ref, lse_ref = p.fwd(q0, k0, v0)
+        dq_ref, dk_ref, dv_ref = p.bwd(q0, k0, v0, o_ref, lse_ref, do)
+        torch.cuda.synchronize()
+        p.check_device_error()
+    assert torch.equal(o.detach(), o_ref)
+    assert torch.equal(k.grad, dk_ref) and torch.equal(v.grad, dv_ref)
+    assert _within_one_ulp(q.grad, dq_ref)
+    prob = orc.Problem(None, T, Hq, Hkv, D, 5e5, orc.MASK_ANCHOR, orc.POS_RESET, orc.ROPE_ADJACENT,
+                       doc_of_token=doc)
+    gq, gk, gv = orc.backward(prob, q0.cpu(), k0.cpu(), v0.cpu(), do.cpu())
+    for nm, got, ref in (("dq", q.grad, gq), ("dk", k.grad, gk), ("dv", v.grad, gv)):
+        assert rel_l2(got, ref) <= REL_L2, nm
