@@ -112,8 +112,10 @@ typedef struct aa_plan_s* aa_plan_t;
  * dropped; the anchor column is folded in separately) in the order the
  * persistent attention kernels claim them (grouped by document, longest
  * group first: the forward's heads interleaved in each document, the
- * backward's one group per document and head), and the two-level fp32
- * cos/sin tables of Eq. 6 built in fp64.
+ * backward's one group per document and head; a forward item is two query
+ * tiles of one head, or one query tile of two heads sharing a kv head when
+ * Hq/Hkv is even), and the two-level fp32 cos/sin tables of Eq. 6 built in
+ * fp64.
  * cu_doclens: host int32[num_docs + 1] (see conventions). Device metadata is
  * uploaded with copies ordered on `stream`. On success *out owns everything;
  * release it with aa_plan_destroy. */

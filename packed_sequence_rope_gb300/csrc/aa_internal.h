@@ -53,7 +53,11 @@ struct aa_plan_s {
   // by document; perm[t] is the caller's token at grouped position t.
   bool segmented = false;
   std::vector<int32_t> perm, seg_doc, seg_pos;  // seg_*: the caller's order
-  std::vector<aa::WorkItem> fwd_items, bwd_items;  // fwd: one item per (query-tile pair, head)
+  // fwd: one item per (query-tile pair, head), or with fwd_head_pairs (an even
+  // number of query heads per kv head) one per (query tile, two heads of one
+  // kv group), whose two tiles then see the same key tiles
+  std::vector<aa::WorkItem> fwd_items, bwd_items;
+  bool fwd_head_pairs = false;
   std::vector<int32_t> qtile_klo;
   std::vector<double> theta;    // [D/2] rotation frequency of each pair (Eq. 6's theta_p)
   std::vector<float2> rope_hi, rope_lo, rope_step;

@@ -13,8 +13,10 @@
 // rotated inside the attention kernel would put the rotation between one
 // item's last products and the next item's first. The attention kernel is
 // persistent: one CTA per SM; the CTAs claim (pair of 128-row query tiles,
-// head) items from a counter in work-list order (grouped by document with
-// the heads interleaved, longest document first), 384 threads:
+// head) items — with an even number of query heads per kv head, (query tile,
+// two heads of one kv group) items — from a counter in work-list order
+// (grouped by document with the heads interleaved, longest document first),
+// 384 threads:
 //   warp 0      claims the next item (published to the other roles through a
 //               2-slot shared-memory ring) and is the TMA producer: each
 //               item's rotated Q0/Q1 as soon as the previous item's last S
@@ -98,6 +100,7 @@ struct FwdParams {
   int32_t* err;
   uint64_t wait_limit_ns;
   int T, Hq, Hkv, group, layout, anchor, n_tiles;
+  int head_pairs;  // items are (query tile, two heads of one kv group) instead of (two query tiles, head)
   float scale;
 };
 
@@ -106,6 +109,15 @@ __device__ __forceinline__ FwdItem load_fwd_item(const FwdParams& P, int it) {
   const WorkItem w = P.items[it];
   FwdItem f;
   f.h = w.head;
+  if (P.head_pairs) {
+    f.qt0 = w.tile;
+    f.kt_lo = w.lo;
+    f.kt_hi = w.hi;
+    f.has1 = true;
+    f.lo[0] = f.lo[1] = __ldg(P.qtile_klo + w.tile);
+    f.hi[0] = f.hi[1] = w.tile;
+    return f;
+  }
   f.qt0 = 2 * w.tile;
   f.kt_lo = w.lo;
   f.kt_hi = w.hi;
@@ -260,7 +272,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!ok) break;
           ptx::mbar_arrive_expect_tx(&sm.q_full[t], kTileBytes);
           for (int b = 0; b < HD / 64; ++b)
-            ptx::tma_load_3d(sm.q[t][b], &tmQ, &sm.q_full[t], b * 64, w.h, (w.qt0 + t) * kTile);
+            ptx::tma_load_3d(sm.q[t][b], &tmQ, &sm.q_full[t], b * 64, w.h + (P.head_pairs ? t : 0),
+                             (w.qt0 + (P.head_pairs ? 0 : t)) * kTile);
           ++nq[t];
         }
         for (int kt = w.kt_lo; kt <= w.kt_hi && ok; ++kt) {
@@ -379,9 +392,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         release_fwd_item(sm, li, true);
         continue;
       }
-      const int h = w.h;
+      const int h = w.h + (P.head_pairs ? t : 0);
       const int lo_t = w.lo[t], hi_t = w.hi[t];
-      const int i = (w.qt0 + t) * kTile + r;
+      const int i = (w.qt0 + (P.head_pairs ? 0 : t)) * kTile + r;
       const bool row_valid = i < P.T;
       const int lo = row_valid ? __ldg(P.row_lo + i) : 1;
       const int hi = row_valid ? i : 0;
@@ -570,6 +583,7 @@ aa_status launch_fwd(aa_plan_s* p, const void* q, const void* k, const void* v, 
   P.layout = p->cfg.rope_layout;
   P.anchor = p->anchor ? 1 : 0;
   P.n_tiles = p->n_tiles;
+  P.head_pairs = p->fwd_head_pairs ? 1 : 0;
   P.scale = p->scale;
   const size_t smem = sizeof(FwdSmem<HD>);
   static std::once_flag attr_once[kMaxDevices];

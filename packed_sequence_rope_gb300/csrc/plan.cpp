@@ -103,15 +103,24 @@ static void build_stats_and_work(aa_plan_s* p) {
     if (p->anchor && kt_lo > 0) live += 1;  // the anchor column's block
     p->live_tiles += live;
   }
-  // forward: one item per pair of query tiles (2a, 2a+1) and head, visiting
-  // the union of the two tiles' key ranges
+  // forward: an item fills the attention kernel's two query-tile slots.
+  // With an even number of query heads per kv head, one query tile of two
+  // heads that share their K/V: both slots see the same key tiles. Otherwise
+  // the pair of query tiles (2a, 2a+1) of one head, visiting the union of
+  // their key ranges (tile 2a+1 has one more key tile, its diagonal).
   p->qtile_klo.assign(nt, 0);
   for (int a = 0; a < nt; ++a) p->qtile_klo[a] = q_ranges[a].lo;
-  for (int h = 0; h < p->Hq; ++h)
-    for (int a = 0; 2 * a < nt; ++a) {
-      const int t0 = 2 * a, t1 = std::min(nt - 1, 2 * a + 1);
-      p->fwd_items.push_back(WorkItem{a, h, std::min(q_ranges[t0].lo, q_ranges[t1].lo), t1});
-    }
+  p->fwd_head_pairs = p->group >= 2 && p->group % 2 == 0;
+  if (p->fwd_head_pairs) {
+    for (int h = 0; h < p->Hq; h += 2)
+      for (int a = 0; a < nt; ++a) p->fwd_items.push_back(WorkItem{a, h, q_ranges[a].lo, a});
+  } else {
+    for (int h = 0; h < p->Hq; ++h)
+      for (int a = 0; 2 * a < nt; ++a) {
+        const int t0 = 2 * a, t1 = std::min(nt - 1, 2 * a + 1);
+        p->fwd_items.push_back(WorkItem{a, h, std::min(q_ranges[t0].lo, q_ranges[t1].lo), t1});
+      }
+  }
   for (int g = 0; g < p->Hkv; ++g)
     for (int b = 0; b < nt; ++b) {
       const int j0 = b * kTile, j1 = std::min(T, j0 + kTile) - 1;
@@ -134,7 +143,7 @@ static void build_stats_and_work(aa_plan_s* p) {
   //    a group per (document, head) does not.
   auto order = [&](std::vector<WorkItem>& items, bool fwd) {
     auto doc_of = [&](const WorkItem& w) {
-      const int row = fwd ? 2 * w.tile * kTile : w.tile * kTile;
+      const int row = (fwd && !p->fwd_head_pairs) ? 2 * w.tile * kTile : w.tile * kTile;
       return p->doc_id[std::min(row + (row == 0 && T > 1 ? 1 : 0), T - 1)];
     };
     std::vector<int64_t> key_doc(items.size());
