@@ -65,6 +65,10 @@ CASES = [
     ("no_rope", [1, 50, 600], 600, 2, 1, 128, 1e4, orc.MASK_ANCHOR, orc.POS_RESET, orc.ROPE_NONE),
     ("single_doc", [1, 513], 513, 2, 2, 128, 1e4, orc.MASK_ANCHOR, orc.POS_RESET, orc.ROPE_ADJACENT),
     ("two_tokens", [1, 2], 2, 1, 1, 128, 1e4, orc.MASK_ANCHOR, orc.POS_RESET, orc.ROPE_ADJACENT),
+    # GQA with an even group: forward items of two heads on one query tile (here a single partial tile)
+    ("two_tokens_gqa", [1, 2], 2, 4, 2, 128, 1e4, orc.MASK_ANCHOR, orc.POS_RESET, orc.ROPE_ADJACENT),
+    # an odd group (3 query heads per kv head): forward items of two query tiles of one head
+    ("gqa_group3_d64", [1, 100, 130, 300], 300, 3, 1, 64, 1e4, orc.MASK_ANCHOR, orc.POS_RESET, orc.ROPE_ADJACENT),
 ]
 
 
